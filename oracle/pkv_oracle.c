@@ -1,0 +1,275 @@
+/*
+ * pkv_oracle.c -- plain fp64 CPU oracle for attention over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  It shares no code, header,
+ * table or helper with the CUDA library: it is written separately, from the
+ * definitions on the source pages, so that the two can be compared.
+ *
+ * Every step is a plain loop, in the order the definitions state it:
+ *   - token -> request assignment by cumulative sequence lengths and the
+ *     paged address of a logical position (transformers docs "paged_attention":
+ *     "Varlen path" example and "Decode path" example);
+ *   - logits s_j = sm_scale * <q, k_j>, computed on the exact values of the
+ *     inputs widened to double (sink_attention_reference.py, FlashInfer tests:
+ *     sink_attention_unified, the einsum followed by "* sm_scale");
+ *   - GQA: query head h reads kv head h / (Hq / Hkv)
+ *     (sink_attention_reference.py, repeat_interleave over the head axis;
+ *     vLLM attention.py, PagedAttention.head_mapping);
+ *   - causal mask aligned to the end of the kv sequence: the query in row i
+ *     of a request sits at position kv_len - q_len + i and keeps key j iff
+ *     j <= that position; a sliding window additionally needs
+ *     position - window_left <= j (sink_attention_reference.py, varlen branch
+ *     and the incremental-mode mask);
+ *   - sink softmax: the per-query-head sink logit is one extra softmax column
+ *     that is dropped after normalising, so the denominator gains exp(sink[h])
+ *     (sink_attention_reference.py, sink_softmax);
+ *   - o = sum_j p_j v_j (the final einsum).
+ *
+ * Readings where the pages are silent (they are listed with the design notes):
+ *   - sink[h] is a logit in natural-log units and is not multiplied by
+ *     sm_scale (it is concatenated after the logits were scaled);
+ *   - a NULL sink means "no sink" (-inf); with no sink the result is the
+ *     plain softmax;
+ *   - a row with no attended key has output 0 (and lse = the sink, or -inf);
+ *   - lse = log(sum_j exp(s_j) + exp(sink[h])), the full softmax
+ *     denominator, natural log.
+ *
+ * Precision: every input value (fp32, or bf16 given as its 16 raw bits) is
+ * widened exactly to double; all arithmetic is double; nothing is rounded.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* ------------------------------------------------------------------------ */
+/* indexing                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* For every token t in [0, total), the request r with cu[r] <= t < cu[r+1].
+ * Empty requests own no token.  Returns 0, or -1 if some token has no owner
+ * (cu not covering [0, total)). */
+int oracle_token_to_request(const int32_t *cu, int batch, int total, int32_t *out) {
+    for (int t = 0; t < total; ++t) {
+        out[t] = -1;
+        for (int r = 0; r < batch; ++r) {
+            if (cu[r] <= t && t < cu[r + 1]) {
+                out[t] = r;
+                break;
+            }
+        }
+        if (out[t] < 0) return -1;
+    }
+    return 0;
+}
+
+/* Flat cache slot of logical position pos of sequence b: the page that the
+ * block table names for that position, times the page size, plus the offset
+ * inside the page.  Returns -1 for an unallocated (-1) page entry. */
+int64_t oracle_slot(const int32_t *block_table, int max_blocks_per_seq, int b, int pos,
+                    int block_size) {
+    int32_t page = block_table[(int64_t)b * max_blocks_per_seq + pos / block_size];
+    if (page < 0) return -1;
+    return (int64_t)page * block_size + pos % block_size;
+}
+
+/* The cache write: row slot_mapping[t] of each pool receives row t of key and
+ * value, bit for bit.  A negative slot means "do not cache this token"
+ * (vLLM attention.py, PagedAttention.forward: the to_cache filter before
+ * reshape_and_cache).  row_bytes is the size of one token's row
+ * (num_kv_heads * head_dim * element size). */
+void oracle_reshape_and_cache(const uint8_t *key, const uint8_t *value, uint8_t *k_cache,
+                              uint8_t *v_cache, const int64_t *slot_mapping, int num_tokens,
+                              int64_t row_bytes) {
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        memcpy(k_cache + s * row_bytes, key + (int64_t)t * row_bytes, (size_t)row_bytes);
+        memcpy(v_cache + s * row_bytes, value + (int64_t)t * row_bytes, (size_t)row_bytes);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* attention                                                                 */
+/* ------------------------------------------------------------------------ */
+
+static double widen(const void *base, int dtype, int64_t idx) {
+    if (dtype == ORACLE_F32) return (double)((const float *)base)[idx];
+    /* bf16: the 16 bits are the upper half of an fp32 */
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    /* outputs */
+    double *out;           /* [nrows, Hq, D] */
+    double *lse;           /* [nrows, Hq] or NULL */
+    /* inputs */
+    const void *q;         /* [total_q, Hq, D] */
+    int q_dtype;
+    const void *k_cache;   /* [num_blocks, block_size, Hkv, D] */
+    const void *v_cache;
+    int kv_dtype;
+    int64_t num_blocks;
+    int block_size, num_kv_heads, head_dim;
+    const int32_t *block_table;
+    int max_blocks_per_seq;
+    const int32_t *cu_q;   /* [batch+1] */
+    const int32_t *kv_lens;/* [batch] */
+    int batch, num_qo_heads;
+    const float *sink;     /* [Hq] or NULL */
+    int causal, window_left;
+    double sm_scale;
+    const int32_t *rows;   /* which query rows to compute, or NULL = all */
+    int nrows;
+    /* work distribution */
+    int64_t next_unit;
+    pthread_mutex_t lock;
+    int status;
+} job_t;
+
+/* One (query row, query head) output: the definition written out. */
+static int attend_one(job_t *J, int out_row, int t, double *s_buf) {
+    const int Hq = J->num_qo_heads, Hkv = J->num_kv_heads, D = J->head_dim;
+    /* which request owns query row t */
+    int r = -1;
+    for (int i = 0; i < J->batch; ++i)
+        if (J->cu_q[i] <= t && t < J->cu_q[i + 1]) { r = i; break; }
+    if (r < 0) return -1;
+    const int q_len = J->cu_q[r + 1] - J->cu_q[r];
+    const int kv_len = J->kv_lens[r];
+    const int i_row = t - J->cu_q[r];
+    const int64_t qpos = (int64_t)kv_len - q_len + i_row; /* the query's position */
+    const int group = Hq / Hkv;
+
+    for (int h = 0; h < Hq; ++h) {
+        const int g = h / group;
+        const double sink = J->sink ? (double)J->sink[h] : -INFINITY;
+        double *o = J->out + ((int64_t)out_row * Hq + h) * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+
+        /* logits of the allowed keys; disallowed keys get -inf */
+        double m = sink;
+        int any = 0;
+        for (int j = 0; j < kv_len; ++j) {
+            int allowed = 1;
+            if (J->causal && !((int64_t)j <= qpos)) allowed = 0;
+            if (J->window_left >= 0 && !(qpos - J->window_left <= (int64_t)j)) allowed = 0;
+            if (!allowed) { s_buf[j] = -INFINITY; continue; }
+            int64_t slot = oracle_slot(J->block_table, J->max_blocks_per_seq, r, j, J->block_size);
+            if (slot < 0 || slot >= J->num_blocks * J->block_size) return -2;
+            const int64_t kbase = (slot * Hkv + g) * D;
+            const int64_t qbase = ((int64_t)t * Hq + h) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += widen(J->q, J->q_dtype, qbase + d) * widen(J->k_cache, J->kv_dtype, kbase + d);
+            s_buf[j] = J->sm_scale * dot;
+            if (s_buf[j] > m) m = s_buf[j];
+            any = 1;
+        }
+        if (!any) {
+            /* nothing attended: the sink column (if any) takes all the mass
+             * and is dropped, so the output is 0 */
+            if (J->lse) J->lse[(int64_t)out_row * Hq + h] = sink;
+            continue;
+        }
+        /* softmax over [s_0 .. s_{n-1}, sink], sink column dropped */
+        double z = exp(sink - m); /* exp(-inf) = 0 when there is no sink */
+        for (int j = 0; j < kv_len; ++j)
+            if (s_buf[j] != -INFINITY) z += exp(s_buf[j] - m);
+        for (int j = 0; j < kv_len; ++j) {
+            if (s_buf[j] == -INFINITY) continue;
+            const double p = exp(s_buf[j] - m) / z;
+            int64_t slot = oracle_slot(J->block_table, J->max_blocks_per_seq, r, j, J->block_size);
+            const int64_t vbase = (slot * Hkv + g) * D;
+            for (int d = 0; d < D; ++d) o[d] += p * widen(J->v_cache, J->kv_dtype, vbase + d);
+        }
+        if (J->lse) J->lse[(int64_t)out_row * Hq + h] = m + log(z);
+    }
+    return 0;
+}
+
+static void *worker(void *arg) {
+    job_t *J = (job_t *)arg;
+    int64_t max_kv = 1;
+    for (int r = 0; r < J->batch; ++r)
+        if (J->kv_lens[r] > max_kv) max_kv = J->kv_lens[r];
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)max_kv);
+    if (!s_buf) {
+        pthread_mutex_lock(&J->lock);
+        J->status = -3;
+        pthread_mutex_unlock(&J->lock);
+        return NULL;
+    }
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int64_t u = J->next_unit++;
+        pthread_mutex_unlock(&J->lock);
+        if (u >= J->nrows) break;
+        int t = J->rows ? J->rows[u] : (int)u;
+        int st = attend_one(J, (int)u, t, s_buf);
+        if (st != 0) {
+            pthread_mutex_lock(&J->lock);
+            J->status = st;
+            pthread_mutex_unlock(&J->lock);
+        }
+    }
+    free(s_buf);
+    return NULL;
+}
+
+/* Attention of every (listed) query row over its request's paged K/V.
+ *
+ * Decode is the special case cu_q = [0, 1, ..., batch] with kv_lens =
+ * cache_seqlens: the single query sits at position kv_len - 1.
+ *
+ * rows: NULL computes all cu_q[batch] rows (nrows must equal that);
+ * otherwise out row u is query row rows[u].
+ * nthreads <= 0 uses every online core.  Returns 0; -1 if a row has no
+ * request; -2 if an attended key's page is unallocated or out of the pool;
+ * -3 on allocation failure; -4 on bad arguments. */
+int oracle_attention(double *out, double *lse, const void *q, int q_dtype, const void *k_cache,
+                     const void *v_cache, int kv_dtype, int64_t num_blocks, int block_size,
+                     int num_kv_heads, int head_dim, const int32_t *block_table,
+                     int max_blocks_per_seq, const int32_t *cu_q, const int32_t *kv_lens,
+                     int batch, int num_qo_heads, const float *sink, int causal,
+                     int window_left, double sm_scale, const int32_t *rows, int nrows,
+                     int nthreads) {
+    if (num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || batch < 0 || nrows < 0)
+        return -4;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.out = out; J.lse = lse; J.q = q; J.q_dtype = q_dtype;
+    J.k_cache = k_cache; J.v_cache = v_cache; J.kv_dtype = kv_dtype;
+    J.num_blocks = num_blocks; J.block_size = block_size;
+    J.num_kv_heads = num_kv_heads; J.head_dim = head_dim;
+    J.block_table = block_table; J.max_blocks_per_seq = max_blocks_per_seq;
+    J.cu_q = cu_q; J.kv_lens = kv_lens; J.batch = batch; J.num_qo_heads = num_qo_heads;
+    J.sink = sink; J.causal = causal; J.window_left = window_left; J.sm_scale = sm_scale;
+    J.rows = rows; J.nrows = nrows;
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > nrows && nrows > 0) nthreads = nrows;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th) return -3;
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i)
+        if (pthread_create(&th[i], NULL, worker, &J) == 0) ++started;
+    if (started == 0) worker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return J.status;
+}
+
+int oracle_online_cores(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }

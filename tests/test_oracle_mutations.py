@@ -1,0 +1,61 @@
+"""The pins reject a plausibly broken oracle (CPU only).
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped
+term, a wrong sign or bound, a wrong index, a swapped operand), compiles the
+copy to a temporary library and runs the pin suite against it in a child
+process: the pins must fail.  The committed oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
+
+MUTATIONS = {
+    "sink scaled by sm_scale": (
+        "const double sink = J->sink ? (double)J->sink[h] : -INFINITY;",
+        "const double sink = J->sink ? (double)J->sink[h] * J->sm_scale : -INFINITY;"),
+    "sink dropped from the denominator": (
+        "double z = exp(sink - m);", "double z = 0.0 * exp(sink - m);"),
+    "window bound off by one": (
+        "qpos - J->window_left <= (int64_t)j", "qpos - J->window_left < (int64_t)j"),
+    "causal bound off by one": (
+        "(int64_t)j <= qpos", "(int64_t)j < qpos"),
+    "GQA head mapping modulo": (
+        "const int g = h / group;", "const int g = h % Hkv;"),
+    "causal mask aligned to the start": (
+        "const int64_t qpos = (int64_t)kv_len - q_len + i_row;",
+        "const int64_t qpos = (int64_t)i_row;"),
+    "page offset dropped from the slot": (
+        "return (int64_t)page * block_size + pos % block_size;",
+        "return (int64_t)page * block_size;"),
+    "values read from the key pool": (
+        "o[d] += p * widen(J->v_cache, J->kv_dtype, vbase + d);",
+        "o[d] += p * widen(J->k_cache, J->kv_dtype, vbase + d);"),
+    "sm_scale dropped": (
+        "s_buf[j] = J->sm_scale * dot;", "s_buf[j] = dot;"),
+    "request bound inclusive": (
+        "if (cu[r] <= t && t < cu[r + 1]) {", "if (cu[r] <= t && t <= cu[r + 1]) {"),
+    "cache write ignores the skip marker": (
+        "if (s < 0) continue;", "if (s < -1) continue;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-std=c11", "-fPIC",
+                    "-shared", "-pthread", str(mut), "-o", str(lib), "-lm"], check=True)
+    env = dict(os.environ, PKV_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins accepted the mutant '{name}':\n{r.stdout[-2000:]}"

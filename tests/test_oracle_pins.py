@@ -1,0 +1,313 @@
+"""Pins of the fp64 CPU oracle to things other than itself (CPU only).
+
+Each test checks the oracle against a fact the pages or the mathematics fix:
+  * the worked examples of the transformers docs "paged_attention" page
+    (token -> request by cu_seq_lens; pages and new-token slots by block_table),
+    stored under tests/golden/ with their citation;
+  * a library routine: torch's scaled_dot_product_attention in fp64, for the
+    plain softmax (no sink), and for the sink read as one more softmax column
+    with a zero value row (sink_attention_reference.py, sink_softmax);
+  * closed forms: window_left = 0 leaves one key, o = v * sigmoid(s - sink);
+  * invariances: physical page relabelling, page size, window >= kv_len,
+    decode == last prefill row, chunk == suffix of a longer chunk;
+  * an independent dense brute force in numpy on tiny inputs.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._dense import brute_force, cu, paginate, random_dense
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# worked examples of the page (exact)
+# ---------------------------------------------------------------------------
+
+def test_varlen_example_token_to_request():
+    g = _golden("varlen_example.json")
+    assert list(np.cumsum([0] + g["q_lens"])) == g["cu_seq_lens_q"]
+    assert list(np.cumsum([0] + g["k_lens"])) == g["cu_seq_lens_k"]
+    assert max(g["q_lens"]) == g["max_length_q"] and max(g["k_lens"]) == g["max_length_k"]
+    q_map = oracle.token_to_request(g["cu_seq_lens_q"], g["total_q"])
+    k_map = oracle.token_to_request(g["cu_seq_lens_k"], g["total_k"])
+    assert q_map.tolist() == g["q_request_index"]
+    assert k_map.tolist() == g["k_request_index"]  # r0 has no key token
+
+
+def test_decode_example_pages_and_new_token_slots():
+    g = _golden("decode_example.json")
+    bt, bs = g["block_table"], g["block_size"]
+    for b, L in enumerate(g["cache_seqlens"]):
+        # positions 0..L (cached tokens and the new one) live in the blocks
+        # the page lists for the sequence
+        blocks = {oracle.slot(bt, b, p, bs) // bs for p in range(L + 1)}
+        assert blocks == set(g["blocks_listed_for_seq"][b])
+        assert not blocks & set(g["blocks_never_owned"])
+        # the new token (position L) lands where the page says
+        s = oracle.slot(bt, b, L, bs)
+        assert s // bs == g["new_token_block"][b]
+        assert s % bs == g["new_token_offset_in_block"][b]
+        assert s == g["new_token_slot"][b]
+
+
+def test_decode_example_unallocated_entry_is_not_a_slot():
+    g = _golden("decode_example.json")
+    # position 32 of sequence 0 would need block_table[0][1] == -1
+    assert oracle.slot(g["block_table"], 0, 32, g["block_size"]) == -1
+
+
+def test_decode_example_never_reads_unowned_pages():
+    """Pool blocks 4 and 7 (never owned in the example) hold NaN; the oracle's
+    outputs stay finite, so it never reads them or a -1 entry."""
+    from paged_kv_cache_attention_gb300 import workloads as W
+    case = W.config1_tiny()
+    out = oracle.paged_decode(W.to_oracle(case.q), W.to_oracle(case.k_cache),
+                              W.to_oracle(case.v_cache), case.block_table.numpy(),
+                              case.cache_seqlens.numpy(), sink=case.sink.numpy(),
+                              sm_scale=case.sm_scale)
+    assert np.isfinite(out).all()
+
+
+# ---------------------------------------------------------------------------
+# library routine: scaled_dot_product_attention in fp64
+# ---------------------------------------------------------------------------
+
+def _sdpa(q, k, v, scale, sink=None):
+    """Causal prefill (q_len == kv_len) through torch SDPA in fp64.  With a
+    sink, one extra key is appended whose value row is 0 and whose logit is
+    sink[h] (given as an additive mask column): the sink column joins the
+    softmax and contributes nothing to the output."""
+    qt = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)[None]  # [1,Hq,L,D]
+    G = q.shape[1] // k.shape[1]
+    kt = torch.from_numpy(k.astype(np.float64)).repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+    vt = torch.from_numpy(v.astype(np.float64)).repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+    if sink is None:
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True,
+                                                             scale=scale)
+    else:
+        L, Hq = q.shape[0], q.shape[1]
+        causal = torch.triu(torch.full((L, L), float("-inf"), dtype=torch.float64), 1)
+        bias = torch.cat([causal[None].expand(Hq, L, L),
+                          torch.from_numpy(sink.astype(np.float64))[:, None, None].expand(Hq, L, 1)],
+                         dim=-1)[None]
+        zk = torch.zeros(1, Hq, 1, q.shape[2], dtype=torch.float64)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt, torch.cat([kt, zk], 2), torch.cat([vt, zk], 2), attn_mask=bias, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs,lens", [
+    (4, 4, 16, 4, [5, 9]),
+    (4, 2, 32, 8, [17, 1, 33]),
+    (8, 2, 64, 16, [40, 7]),
+    (8, 1, 16, 16, [3, 50]),
+])
+@pytest.mark.parametrize("with_sink", [False, True])
+def test_prefill_matches_sdpa(Hq, Hkv, D, bs, lens, with_sink):
+    rng = np.random.default_rng(7 + Hq + D + len(lens))
+    qd, kd, vd = random_dense(rng, lens, lens, Hq, Hkv, D)
+    kp, vp, bt = paginate(kd, vd, bs, rng)
+    sink = rng.standard_normal(Hq).astype(np.float32) * 2 if with_sink else None
+    scale = 1.0 / math.sqrt(D)
+    out = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(lens), np.array(lens, np.int32),
+                           sink=sink, causal=True, sm_scale=scale)
+    ref = np.concatenate([_sdpa(qd[r], kd[r], vd[r], scale, sink) for r in range(len(lens))])
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_sink_only_rescales():
+    """With a sink the output is the plain output times one per-row factor in
+    (0, 1): the sink adds to the denominator only."""
+    rng = np.random.default_rng(3)
+    qd, kd, vd = random_dense(rng, [6], [6], 4, 2, 32)
+    kp, vp, bt = paginate(kd, vd, 8, rng)
+    sink = np.array([0.5, -1.0, 2.0, 3.0], np.float32)
+    args = (qd[0], kp, vp, bt, cu([6]), np.array([6], np.int32))
+    plain = oracle.attention(*args, sink=None, sm_scale=0.2)
+    with_s = oracle.attention(*args, sink=sink, sm_scale=0.2)
+    ratio = with_s / plain
+    assert np.all(ratio > 0) and np.all(ratio < 1)
+    np.testing.assert_allclose(ratio, ratio[..., :1].repeat(32, -1), rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# closed forms and invariances
+# ---------------------------------------------------------------------------
+
+def test_window_zero_keeps_only_own_key():
+    """window_left = 0: the query at position p keeps key p alone, so
+    o = v_p * e^{s_p} / (e^{s_p} + e^{sink}) = v_p * sigmoid(s_p - sink)."""
+    rng = np.random.default_rng(11)
+    q_lens, kv_lens = [3, 1], [7, 5]
+    qd, kd, vd = random_dense(rng, q_lens, kv_lens, 4, 2, 16)
+    kp, vp, bt = paginate(kd, vd, 4, rng)
+    sink = rng.standard_normal(4).astype(np.float32)
+    scale = 0.3
+    out = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(q_lens),
+                           np.array(kv_lens, np.int32), sink=sink, window_left=0,
+                           sm_scale=scale)
+    row = 0
+    for r in range(2):
+        for i in range(q_lens[r]):
+            p = kv_lens[r] - q_lens[r] + i
+            for h in range(4):
+                g = h // 2
+                s = scale * float(np.dot(qd[r][i, h].astype(np.float64),
+                                         kd[r][p, g].astype(np.float64)))
+                w = 1.0 / (1.0 + math.exp(float(sink[h]) - s))
+                np.testing.assert_allclose(out[row, h], w * vd[r][p, g].astype(np.float64),
+                                           rtol=1e-13, atol=1e-14)
+            row += 1
+
+
+def test_window_at_least_kv_len_is_no_window():
+    rng = np.random.default_rng(12)
+    lens = [9, 20]
+    qd, kd, vd = random_dense(rng, lens, lens, 4, 4, 16)
+    kp, vp, bt = paginate(kd, vd, 4, rng)
+    args = (np.concatenate(qd), kp, vp, bt, cu(lens), np.array(lens, np.int32))
+    a = oracle.attention(*args, window_left=-1, sm_scale=0.25)
+    b = oracle.attention(*args, window_left=20, sm_scale=0.25)
+    c = oracle.attention(*args, window_left=1000, sm_scale=0.25)
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+def test_physical_relabelling_is_invisible():
+    """Moving pages (and their block-table entries) leaves outputs bit-identical."""
+    rng = np.random.default_rng(13)
+    lens = [33, 17, 64]
+    qd, kd, vd = random_dense(rng, [4, 1, 5], lens, 8, 2, 32)
+    sink = rng.standard_normal(8).astype(np.float32)
+    outs = []
+    for seed in (1, 2, 3):
+        kp, vp, bt = paginate(kd, vd, 16, np.random.default_rng(seed), spare=5)
+        outs.append(oracle.attention(np.concatenate(qd), kp, vp, bt, cu([4, 1, 5]),
+                                     np.array(lens, np.int32), sink=sink, window_left=9,
+                                     sm_scale=0.17))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_page_size_is_invisible():
+    rng = np.random.default_rng(14)
+    lens = [70, 31]
+    qd, kd, vd = random_dense(rng, [2, 3], lens, 4, 2, 16)
+    res = []
+    for bs in (16, 32, 1, 7):
+        kp, vp, bt = paginate(kd, vd, bs, rng)
+        res.append(oracle.attention(np.concatenate(qd), kp, vp, bt, cu([2, 3]),
+                                    np.array(lens, np.int32), sm_scale=0.2))
+    for r in res[1:]:
+        assert np.array_equal(res[0], r)
+
+
+def test_decode_is_last_row_of_prefill():
+    rng = np.random.default_rng(15)
+    lens = [12, 30]
+    qd, kd, vd = random_dense(rng, lens, lens, 4, 2, 16)
+    kp, vp, bt = paginate(kd, vd, 8, rng)
+    sink = rng.standard_normal(4).astype(np.float32)
+    full = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(lens), np.array(lens, np.int32),
+                            sink=sink, window_left=5, sm_scale=0.3)
+    last_q = np.stack([qd[0][-1], qd[1][-1]])
+    dec = oracle.paged_decode(last_q, kp, vp, bt, np.array(lens, np.int32), sink=sink,
+                              window_left=5, sm_scale=0.3)
+    np.testing.assert_array_equal(dec[0], full[lens[0] - 1])
+    np.testing.assert_array_equal(dec[1], full[sum(lens) - 1])
+
+
+def test_chunk_is_suffix_of_longer_chunk():
+    """A chunk of the last c queries over kv_len keys equals the last c rows of
+    a longer chunk over the same keys (the causal mask is aligned to the end)."""
+    rng = np.random.default_rng(16)
+    kv = 40
+    qd, kd, vd = random_dense(rng, [25], [kv], 4, 1, 16)
+    kp, vp, bt = paginate(kd, vd, 16, rng)
+    long_ = oracle.attention(qd[0], kp, vp, bt, cu([25]), np.array([kv], np.int32),
+                             sm_scale=0.25, window_left=8)
+    short = oracle.attention(qd[0][-6:], kp, vp, bt, cu([6]), np.array([kv], np.int32),
+                             sm_scale=0.25, window_left=8)
+    np.testing.assert_array_equal(short, long_[-6:])
+
+
+# ---------------------------------------------------------------------------
+# independent brute force on tiny inputs
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(12))
+def test_matches_bruteforce(seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 5))
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4]))
+    D = int(rng.choice([8, 16, 64]))
+    bs = int(rng.choice([1, 4, 16, 32]))
+    kv_lens = [int(x) for x in rng.integers(0, 45, n)]
+    q_lens = [int(rng.integers(0, 8)) for _ in range(n)]
+    q_lens[0] = max(q_lens[0], 1)
+    causal = bool(seed % 3 != 2)
+    window = int(rng.choice([-1, 0, 3, 17]))
+    sink = None if seed % 4 == 0 else (rng.standard_normal(Hkv * G) * 3).astype(np.float32)
+    qd, kd, vd = random_dense(rng, q_lens, kv_lens, Hkv * G, Hkv, D)
+    kp, vp, bt = paginate(kd, vd, bs, rng)
+    out, lse = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(q_lens),
+                                np.array(kv_lens, np.int32), sink=sink, causal=causal,
+                                window_left=window, sm_scale=0.21, with_lse=True)
+    ref, ref_lse = brute_force(qd, kd, vd, sink, causal, window, 0.21)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(fin, np.isfinite(lse))
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=0, atol=1e-12)
+
+
+def test_rows_with_no_key_are_zero():
+    """kv_len = 0 (r0 of the varlen example), and rows whose position is
+    negative because q_len > kv_len, attend to nothing: output 0."""
+    rng = np.random.default_rng(17)
+    q_lens, kv_lens = [3, 4], [0, 2]
+    qd, kd, vd = random_dense(rng, q_lens, kv_lens, 2, 1, 8)
+    kp, vp, bt = paginate([np.zeros((1, 1, 8), np.float32) if k.shape[0] == 0 else k for k in kd],
+                          [np.zeros((1, 1, 8), np.float32) if v.shape[0] == 0 else v for v in vd],
+                          4, rng)
+    sink = np.array([0.3, -0.2], np.float32)
+    out, lse = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(q_lens),
+                                np.array(kv_lens, np.int32), sink=sink, sm_scale=0.5,
+                                with_lse=True)
+    assert np.all(out[:3] == 0)        # request 0: no keys at all
+    assert np.all(out[3:5] == 0)       # request 1 rows 0,1: positions -2, -1
+    assert np.all(out[5:] != 0)
+    np.testing.assert_array_equal(lse[:5], np.broadcast_to(sink.astype(np.float64), (5, 2)))
+
+
+# ---------------------------------------------------------------------------
+# the cache write
+# ---------------------------------------------------------------------------
+
+def test_reshape_and_cache_places_rows_bit_exactly():
+    g = _golden("decode_example.json")
+    rng = np.random.default_rng(18)
+    nb, bs, Hkv, D = 8, g["block_size"], 2, 64
+    kc = np.full((nb, bs, Hkv, D), np.nan, np.float32)
+    vc = np.full((nb, bs, Hkv, D), np.nan, np.float32)
+    key = rng.standard_normal((4, Hkv, D)).astype(np.float32)
+    val = rng.standard_normal((4, Hkv, D)).astype(np.float32)
+    slots = np.array(g["new_token_slot"] + [-1], np.int64)  # last token is not cached
+    oracle.reshape_and_cache(key, val, kc, vc, slots)
+    flat_k = kc.reshape(nb * bs, Hkv, D)
+    flat_v = vc.reshape(nb * bs, Hkv, D)
+    for t, s in enumerate(g["new_token_slot"]):
+        assert flat_k[s].tobytes() == key[t].tobytes()
+        assert flat_v[s].tobytes() == val[t].tobytes()
+    untouched = np.setdiff1d(np.arange(nb * bs), g["new_token_slot"])
+    assert np.isnan(flat_k[untouched]).all() and np.isnan(flat_v[untouched]).all()
