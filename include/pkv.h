@@ -1,0 +1,190 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * Three operations, each an asynchronous launch sequence on the caller's
+ * CUDA stream:
+ *
+ *   pkv_reshape_and_cache  write the new tokens' K/V rows into the paged pools
+ *                          at the flat slots slot_mapping names
+ *                          (vLLM attention.py, PagedAttention.forward: the
+ *                          cache_ops.reshape_and_cache step);
+ *   pkv_paged_decode       one query token per sequence, attending to positions
+ *                          0 .. cache_seqlens[b]-1 gathered through block_table
+ *                          (transformers docs "paged_attention", decode path;
+ *                          vLLM attention.py, single_query_cached_kv_attention
+ *                          with 512-token split-KV partitions);
+ *   pkv_varlen_prefill     causal varlen / chunk prefill: request r has
+ *                          q_len = cu_seq_lens_q[r+1]-cu_seq_lens_q[r] queries
+ *                          over kv_len = cu_seq_lens_k[r+1]-cu_seq_lens_k[r]
+ *                          keys read from the paged pools (transformers docs
+ *                          "paged_attention", varlen path; FlashInfer
+ *                          sink_attention_reference.py, varlen mode).
+ *
+ * What the attention computes (FlashInfer sink_attention_reference.py,
+ * sink_softmax and sink_attention_unified): for request r, query row i and
+ * query head h, with G = num_qo_heads / num_kv_heads and kv head g = h / G:
+ *   qpos  = kv_len - q_len + i               (decode: kv_len - 1)
+ *   keep key j iff j < kv_len, j <= qpos, and (window_left < 0 or
+ *                  j >= qpos - window_left)
+ *   s_j   = sm_scale * <q[i,h,:], k[j,g,:]>  (fp32)
+ *   o     = sum_j exp(s_j) v[j,g,:] / (sum_j exp(s_j) + exp(sink[h]))
+ *   lse   = log(sum_j exp(s_j) + exp(sink[h]))           (natural log)
+ * sink[h] is a logit, not scaled by sm_scale; sink == NULL means no sink.
+ * A row that keeps no key gets o = 0 and lse = sink[h] (or -inf).
+ *
+ * Paged pool layout ("NHD pages"): k_cache and v_cache are each a contiguous
+ *   [num_blocks, block_size, num_kv_heads, head_dim]
+ * array.  Logical position p of sequence b lives in page
+ * block_table[b * max_blocks_per_seq + p / block_size], row p % block_size;
+ * its flat slot is page * block_size + p % block_size.  block_table entries
+ * beyond a sequence's length may be -1 (unallocated) and are never read.
+ *
+ * Ownership: the caller allocates and owns every buffer; device pointers are
+ * device memory, host values are plain ints/floats.  The library allocates
+ * nothing and keeps no state between calls except a process-wide cache of
+ * the driver's tensor-map encoder and of per-device attributes.  Scratch
+ * space (split-KV partials) lives in the caller's workspace, whose size the
+ * *_workspace_size functions give.  The library never reads device memory
+ * from the host and never synchronises the stream.
+ *
+ * Errors: arguments are validated on the host before anything is launched;
+ * a non-zero pkv_status is returned and nothing runs.  Metadata that only the
+ * device sees (a block id outside the pool, a slot outside the pool, a
+ * sequence length larger than the declared maximum) is checked in the
+ * kernels: the offending page or row is skipped and a PKV_DEVERR_* bit is
+ * OR-ed into *dev_error (a device int32 the caller owns and zeroes; may be
+ * NULL).  No kernel traps.
+ *
+ * Supported in this version: head_dim 64 or 128; block_size 16 or 32;
+ * num_qo_heads % num_kv_heads == 0 with G <= 16; decode in fp32 or bf16,
+ * prefill in bf16 (causal only); the output has the dtype of the cache.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shape */
+    PKV_ERR_UNSUPPORTED = 2, /* a shape or dtype this version has no kernel for */
+    PKV_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+    PKV_ERR_CUDA = 4         /* a CUDA call failed (launch, tensor-map encode) */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Device-side error bits OR-ed into *dev_error. */
+#define PKV_DEVERR_BLOCK_ID 1u /* block_table entry of an attended position outside [0, num_blocks) */
+#define PKV_DEVERR_SLOT 2u     /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEVERR_SEQLEN 4u   /* a length above its declared maximum, negative, or
+                                  beyond max_blocks_per_seq * block_size */
+#define PKV_DEVERR_TIMEOUT 8u  /* a bounded pipeline wait gave up */
+
+/* Description of the two paged pools (same shape and dtype). */
+typedef struct pkv_cache_desc {
+    int64_t num_blocks;   /* pages in each pool */
+    int32_t block_size;   /* tokens per page: 16 or 32 */
+    int32_t num_kv_heads; /* Hkv */
+    int32_t head_dim;     /* D: 64 or 128 */
+    int32_t dtype;        /* pkv_dtype of the pools, q and out */
+} pkv_cache_desc;
+
+/* Human-readable name of a pkv_status. */
+PKV_API const char *pkv_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+PKV_API int pkv_version(void);
+
+/*
+ * reshape_and_cache: for every t in [0, num_tokens) with slot_mapping[t] >= 0,
+ * copy row t of key and of value ([num_tokens, Hkv, D], contiguous, dtype of
+ * the cache) into flat slot slot_mapping[t] of k_cache and v_cache.  The copy
+ * is bit-exact.  A negative slot skips the token (stands for vLLM's to_cache
+ * filter).  A slot >= num_blocks * block_size is skipped and sets
+ * PKV_DEVERR_SLOT.  Two tokens with the same slot race (caller error).
+ * All pointers must be 16-byte aligned.
+ */
+PKV_API pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                 void *v_cache, const int64_t *slot_mapping,
+                                 int64_t num_tokens, pkv_cache_desc cache, int32_t *dev_error,
+                                 void *stream);
+
+/*
+ * Workspace bytes pkv_paged_decode needs: split-KV partials for
+ * batch x num_qo_heads x P partitions, P = ceil(max_seqlen / partition_size)
+ * (fewer with a window).  partition_size 0 means 512.
+ */
+PKV_API size_t pkv_paged_decode_workspace_size(int batch, int num_qo_heads, int head_dim,
+                                       int max_seqlen, int partition_size, int window_left);
+
+/*
+ * paged_decode: out[b, h, :] for one query q[b, h, :] per sequence.
+ *   out, q        [batch, num_qo_heads, head_dim], contiguous, cache dtype
+ *   block_table   [batch, max_blocks_per_seq] int32 (device)
+ *   cache_seqlens [batch] int32 (device): attended length L_b; the query sits
+ *                 at position L_b - 1 (write the new token first, then pass
+ *                 the length including it)
+ *   max_seqlen    host int >= every cache_seqlens[b] (sizes the grid)
+ *   sink          [num_qo_heads] fp32 (device) or NULL
+ *   window_left   -1 for none, else keep keys j >= L_b - 1 - window_left
+ *   partition_size split-KV partition in tokens (0 = 512); a multiple of
+ *                 block_size, at most 16384; partitions start at multiples of
+ *                 it
+ *   lse_out       [batch, num_qo_heads] fp32 (device) or NULL
+ *   workspace     device scratch of at least pkv_paged_decode_workspace_size
+ *                 bytes, 256-byte aligned; contents need no initialisation
+ * Sequences longer than max_seqlen are clipped to it and set
+ * PKV_DEVERR_SEQLEN.
+ */
+PKV_API pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            pkv_cache_desc cache, const int32_t *block_table,
+                            int max_blocks_per_seq, const int32_t *cache_seqlens,
+                            int max_seqlen, const float *sink, int batch, int num_qo_heads,
+                            int window_left, float sm_scale, int partition_size,
+                            float *lse_out, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_error, void *stream);
+
+/* Workspace bytes pkv_varlen_prefill needs (its work-tile list). */
+PKV_API size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
+                                         int total_q, int max_seqlen_q);
+
+/*
+ * varlen_prefill: causal attention of every query row over its request's
+ * paged keys.
+ *   out, q         [total_q, num_qo_heads, head_dim] bf16, contiguous
+ *   cu_seq_lens_q  [batch+1] int32 (device), exclusive prefix sums of q_len
+ *   cu_seq_lens_k  [batch+1] int32 (device), exclusive prefix sums of kv_len;
+ *                  only the differences are used -- keys come from the pages
+ *   max_seqlen_q/k host ints >= every q_len / kv_len
+ *   total_q        host int == cu_seq_lens_q[batch]
+ *   causal         must be 1 in this version (mask aligned to the end of kv)
+ *   sink, window_left, sm_scale, lse_out ([total_q, num_qo_heads]) as in
+ *   paged_decode.  Rows whose position is negative (q_len > kv_len) keep no
+ *   key.
+ */
+PKV_API pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
+                              const void *v_cache, pkv_cache_desc cache,
+                              const int32_t *block_table, int max_blocks_per_seq,
+                              const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
+                              int max_seqlen_q, int max_seqlen_k, int total_q,
+                              const float *sink, int batch, int num_qo_heads, int causal,
+                              int window_left, float sm_scale, float *lse_out, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_error, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -137,7 +137,7 @@ typedef struct {
 } job_t;
 
 /* One (query row, query head) output: the definition written out. */
-static int attend_one(job_t *J, int out_row, int t, double *s_buf) {
+static int attend_one(job_t *J, int out_row, int t, int h, double *s_buf) {
     const int Hq = J->num_qo_heads, Hkv = J->num_kv_heads, D = J->head_dim;
     /* which request owns query row t */
     int r = -1;
@@ -150,7 +150,7 @@ static int attend_one(job_t *J, int out_row, int t, double *s_buf) {
     const int64_t qpos = (int64_t)kv_len - q_len + i_row; /* the query's position */
     const int group = Hq / Hkv;
 
-    for (int h = 0; h < Hq; ++h) {
+    {
         const int g = h / group;
         const double sink = J->sink ? (double)J->sink[h] : -INFINITY;
         double *o = J->out + ((int64_t)out_row * Hq + h) * D;
@@ -179,7 +179,7 @@ static int attend_one(job_t *J, int out_row, int t, double *s_buf) {
             /* nothing attended: the sink column (if any) takes all the mass
              * and is dropped, so the output is 0 */
             if (J->lse) J->lse[(int64_t)out_row * Hq + h] = sink;
-            continue;
+            return 0;
         }
         /* softmax over [s_0 .. s_{n-1}, sink], sink column dropped */
         double z = exp(sink - m); /* exp(-inf) = 0 when there is no sink */
@@ -213,9 +213,10 @@ static void *worker(void *arg) {
         pthread_mutex_lock(&J->lock);
         int64_t u = J->next_unit++;
         pthread_mutex_unlock(&J->lock);
-        if (u >= J->nrows) break;
-        int t = J->rows ? J->rows[u] : (int)u;
-        int st = attend_one(J, (int)u, t, s_buf);
+        if (u >= (int64_t)J->nrows * J->num_qo_heads) break;
+        const int row = (int)(u / J->num_qo_heads), h = (int)(u % J->num_qo_heads);
+        int t = J->rows ? J->rows[row] : row;
+        int st = attend_one(J, row, t, h, s_buf);
         if (st != 0) {
             pthread_mutex_lock(&J->lock);
             J->status = st;
@@ -259,7 +260,8 @@ int oracle_attention(double *out, double *lse, const void *q, int q_dtype, const
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;
-    if (nthreads > nrows && nrows > 0) nthreads = nrows;
+    if ((int64_t)nthreads > (int64_t)nrows * num_qo_heads && nrows > 0)
+        nthreads = nrows * num_qo_heads;
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
     if (!th) return -3;
     int started = 0;

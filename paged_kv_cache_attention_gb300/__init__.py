@@ -1,1 +1,296 @@
-"""Paged KV-cache attention for GB300 (sm_103a): binding to the C-ABI library."""
+"""Paged KV-cache attention for GB300 (sm_103a): Python binding of libpkv.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of ``libpkv.so`` (built from ``csrc/`` by ``build()``); this module
+checks shapes and dtypes, takes raw device pointers from torch tensors and
+the current torch stream, and calls the C ABI declared in ``include/pkv.h``.
+There is no CPU or PyTorch fallback: if the library is missing or a call
+fails, an exception is raised.
+
+Operations (same names as the C ABI):
+  * ``reshape_and_cache`` -- write new K/V rows into the paged pools at
+    ``slot_mapping`` (vLLM attention.py, PagedAttention.forward);
+  * ``paged_decode`` -- one query per sequence over its pages through
+    ``block_table`` / ``cache_seqlens`` (transformers docs "paged_attention",
+    decode path), split-KV with 512-token partitions;
+  * ``varlen_prefill`` -- causal varlen / chunk prefill addressed by
+    ``cu_seq_lens_q`` / ``cu_seq_lens_k`` (transformers docs "paged_attention",
+    varlen path), keys read from the pages.
+All three support GQA, ``window_left`` and the per-head attention sink of
+FlashInfer's sink_attention_reference.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from ._build import LIB_PATH, build as _build_lib
+
+__all__ = [
+    "build", "load_library", "PkvError", "reshape_and_cache", "paged_decode",
+    "varlen_prefill", "paged_decode_workspace_size", "varlen_prefill_workspace_size",
+    "DEVERR_BLOCK_ID", "DEVERR_SLOT", "DEVERR_SEQLEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
+]
+
+PKV_F32 = 0
+PKV_BF16 = 1
+DEVERR_BLOCK_ID = 1
+DEVERR_SLOT = 2
+DEVERR_SEQLEN = 4
+DEVERR_TIMEOUT = 8
+
+EXPORTED_SYMBOLS = (
+    "pkv_status_string", "pkv_version", "pkv_reshape_and_cache",
+    "pkv_paged_decode_workspace_size", "pkv_paged_decode",
+    "pkv_varlen_prefill_workspace_size", "pkv_varlen_prefill",
+)
+
+
+class PkvError(RuntimeError):
+    """A libpkv call returned a non-OK status."""
+
+    def __init__(self, fn: str, status: int, name: str):
+        super().__init__(f"{fn} failed: {name} ({status})")
+        self.status = status
+        self.status_name = name
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile libpkv.so for sm_103a (in-tree)."""
+    return _build_lib(force=force)
+
+
+def load_library(path: Optional[str] = None):
+    """Load libpkv.so (building it first if it is absent) and declare the ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            p = _build_lib()
+        lib = ctypes.CDLL(p)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        lib.pkv_status_string.argtypes = [i32]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_version.argtypes = []
+        lib.pkv_version.restype = i32
+        lib.pkv_reshape_and_cache.argtypes = [P, P, P, P, P, i64, CacheDesc, P, P]
+        lib.pkv_reshape_and_cache.restype = i32
+        lib.pkv_paged_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.pkv_paged_decode_workspace_size.restype = sz
+        lib.pkv_paged_decode.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, i32, i32, i32,
+                                         f32, i32, P, P, sz, P, P]
+        lib.pkv_paged_decode.restype = i32
+        lib.pkv_varlen_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.pkv_varlen_prefill_workspace_size.restype = sz
+        lib.pkv_varlen_prefill.argtypes = [P, P, P, P, CacheDesc, P, i32, P, P, i32, i32, i32, P,
+                                           i32, i32, i32, i32, f32, P, P, sz, P, P]
+        lib.pkv_varlen_prefill.restype = i32
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        name = load_library().pkv_status_string(status).decode()
+        raise PkvError(fn, status, name)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype_code(dtype) -> int:
+    torch = _torch()
+    if dtype == torch.float32:
+        return PKV_F32
+    if dtype == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError(f"unsupported dtype {dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _require(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(name, t, dtype=None, ndim=None):
+    _require(t.is_cuda, f"{name} must be a CUDA tensor")
+    _require(t.is_contiguous(), f"{name} must be contiguous")
+    if dtype is not None:
+        _require(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None:
+        _require(t.dim() == ndim, f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _cache_desc(k_cache, v_cache) -> CacheDesc:
+    _cuda_contig("k_cache", k_cache, ndim=4)
+    _cuda_contig("v_cache", v_cache, ndim=4)
+    _require(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype,
+             "k_cache and v_cache must have the same shape and dtype")
+    nb, bs, hkv, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache.dtype))
+
+
+def paged_decode_workspace_size(batch: int, num_qo_heads: int, head_dim: int, max_seqlen: int,
+                                partition_size: int = 512, window_left: int = -1) -> int:
+    return int(load_library().pkv_paged_decode_workspace_size(
+        batch, num_qo_heads, head_dim, max_seqlen, partition_size, window_left))
+
+
+def varlen_prefill_workspace_size(batch: int, num_qo_heads: int, num_kv_heads: int,
+                                  total_q: int, max_seqlen_q: int) -> int:
+    return int(load_library().pkv_varlen_prefill_workspace_size(
+        batch, num_qo_heads, num_kv_heads, total_q, max_seqlen_q))
+
+
+def _workspace(nbytes: int, device, workspace):
+    torch = _torch()
+    if workspace is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    _cuda_contig("workspace", workspace)
+    _require(workspace.numel() * workspace.element_size() >= nbytes,
+             f"workspace too small: need {nbytes} bytes")
+    return workspace
+
+
+# ---------------------------------------------------------------------------
+# public operations
+# ---------------------------------------------------------------------------
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, dev_error=None,
+                      stream=None) -> None:
+    """k_cache/v_cache flat slot slot_mapping[t] <- key/value[t] (in place).
+
+    key, value: [T, Hkv, D] contiguous, dtype of the cache; slot_mapping: [T]
+    int64, negative = skip.  dev_error: optional int32 device tensor that
+    receives PKV_DEVERR_SLOT for slots outside the pool.
+    """
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    _cuda_contig("key", key, k_cache.dtype, 3)
+    _cuda_contig("value", value, k_cache.dtype, 3)
+    _cuda_contig("slot_mapping", slot_mapping, torch.int64, 1)
+    _require(key.shape == value.shape and key.shape[1:] == k_cache.shape[2:],
+             "key/value must be [T, num_kv_heads, head_dim] matching the cache")
+    _require(slot_mapping.shape[0] == key.shape[0], "slot_mapping must have T entries")
+    st = load_library().pkv_reshape_and_cache(
+        _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+        key.shape[0], desc, _ptr(dev_error), _stream_handle(stream))
+    _check("pkv_reshape_and_cache", st)
+
+
+def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,
+                 sink=None, window_left: int = -1, sm_scale: Optional[float] = None,
+                 partition_size: int = 512, out=None, lse=None, workspace=None,
+                 dev_error=None, stream=None):
+    """Single-token decode over the paged pools; returns out [B, Hq, D].
+
+    q: [B, Hq, D] (dtype of the cache); block_table: [B, max_blocks] int32;
+    cache_seqlens: [B] int32, the attended length (query at position L-1);
+    max_seqlen: host int >= max(cache_seqlens); sink: [Hq] float32 or None;
+    lse: optional [B, Hq] float32 output (natural log, sink included).
+    """
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    _cuda_contig("q", q, k_cache.dtype, 3)
+    _cuda_contig("block_table", block_table, torch.int32, 2)
+    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32, 1)
+    B, Hq, D = q.shape
+    _require(D == k_cache.shape[3], "head_dim of q and cache differ")
+    _require(block_table.shape[0] == B and cache_seqlens.shape[0] == B,
+             "block_table / cache_seqlens batch mismatch")
+    if sink is not None:
+        _cuda_contig("sink", sink, torch.float32, 1)
+        _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_contig("out", out, q.dtype, 3)
+        _require(out.shape == q.shape, "out must be shaped like q")
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32, 2)
+        _require(tuple(lse.shape) == (B, Hq), "lse must be [B, Hq]")
+    scale = float(sm_scale) if sm_scale is not None else D ** -0.5
+    need = paged_decode_workspace_size(B, Hq, D, max_seqlen, partition_size, window_left)
+    ws = _workspace(need, q.device, workspace)
+    st = load_library().pkv_paged_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
+        block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink), B, Hq,
+        int(window_left), scale, int(partition_size), _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
+    _check("pkv_paged_decode", st)
+    return out
+
+
+def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_k,
+                   max_seqlen_q: int, max_seqlen_k: int, sink=None, causal: bool = True,
+                   window_left: int = -1, sm_scale: Optional[float] = None, out=None, lse=None,
+                   workspace=None, dev_error=None, stream=None):
+    """Causal varlen / chunk prefill over the paged pools; returns out [total_q, Hq, D].
+
+    q: [total_q, Hq, D] bf16; cu_seq_lens_q / cu_seq_lens_k: [B+1] int32;
+    max_seqlen_q / max_seqlen_k: host ints; request r's queries sit at the end
+    of its kv_len keys.
+    """
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    _cuda_contig("q", q, k_cache.dtype, 3)
+    _cuda_contig("block_table", block_table, torch.int32, 2)
+    _cuda_contig("cu_seq_lens_q", cu_seq_lens_q, torch.int32, 1)
+    _cuda_contig("cu_seq_lens_k", cu_seq_lens_k, torch.int32, 1)
+    total_q, Hq, D = q.shape
+    B = cu_seq_lens_q.shape[0] - 1
+    _require(cu_seq_lens_k.shape[0] == B + 1, "cu_seq_lens_q/k lengths differ")
+    _require(block_table.shape[0] == B, "block_table must have one row per request")
+    if sink is not None:
+        _cuda_contig("sink", sink, torch.float32, 1)
+        _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_contig("out", out, q.dtype, 3)
+        _require(out.shape == q.shape, "out must be shaped like q")
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32, 2)
+        _require(tuple(lse.shape) == (total_q, Hq), "lse must be [total_q, Hq]")
+    scale = float(sm_scale) if sm_scale is not None else D ** -0.5
+    need = varlen_prefill_workspace_size(B, Hq, k_cache.shape[2], total_q, max_seqlen_q)
+    ws = _workspace(need, q.device, workspace)
+    st = load_library().pkv_varlen_prefill(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
+        block_table.shape[1], _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), int(max_seqlen_q),
+        int(max_seqlen_k), int(total_q), _ptr(sink), B, Hq, int(bool(causal)),
+        int(window_left), scale, _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(dev_error), _stream_handle(stream))
+    _check("pkv_varlen_prefill", st)
+    return out

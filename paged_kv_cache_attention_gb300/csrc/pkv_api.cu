@@ -1,0 +1,312 @@
+// pkv_api.cu -- the C ABI of libpkv: host-side validation, workspace sizing,
+// TMA tensor-map encoding and kernel dispatch.  Nothing here touches device
+// memory from the host or synchronises a stream.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kDefaultPartition = 512;
+constexpr int kMaxPartition = 16384;
+constexpr int kMaxDevices = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// 3-D view of a pool or of q: {D elements, heads, rows}, bf16, 128-byte
+// swizzled boxes of {64, box_heads, box_rows}.
+pkv_status encode_rows_map(CUtensorMap *map, const void *base, int D, int heads, int64_t rows,
+                           int box_heads, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return PKV_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * heads};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status check_cache(const pkv_cache_desc &c) {
+    if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (c.dtype != PKV_F32 && c.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (c.head_dim != 64 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (c.block_size != 16 && c.block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (c.num_blocks * (int64_t)c.block_size >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+int decode_num_parts(int max_seqlen, int P, int window_left) {
+    int n = (max_seqlen + P - 1) / P;
+    if (window_left >= 0) {
+        const long long w = ((long long)window_left + 1 + P - 1) / P + 1;
+        if (w < n) n = (int)w;
+    }
+    return n < 1 ? 1 : n;
+}
+
+struct DecodeLayout {
+    size_t lse_off, o_off, total;
+};
+
+DecodeLayout decode_layout(int batch, int Hq, int D, int num_parts) {
+    DecodeLayout L;
+    const size_t units = (size_t)batch * Hq * num_parts;
+    L.lse_off = 0;
+    L.o_off = round_up(units * sizeof(float), 256);
+    L.total = L.o_off + round_up(units * D * sizeof(float), 256);
+    return L;
+}
+
+pkv_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return PKV_OK;
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    return PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < kMaxDevices) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 148;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        default: return "PKV_ERR_UNKNOWN";
+    }
+}
+
+int pkv_version(void) { return 100; }
+
+pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                 void *v_cache, const int64_t *slot_mapping, int64_t num_tokens,
+                                 pkv_cache_desc cache, int32_t *dev_error, void *stream) {
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0 ||
+        cache.head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (cache.dtype != PKV_F32 && cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    const int64_t row_bytes =
+        (int64_t)cache.num_kv_heads * cache.head_dim * elem_bytes(cache.dtype);
+    if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t capacity = cache.num_blocks * (int64_t)cache.block_size;
+    return from_cuda(launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping,
+                                              num_tokens, row_bytes, capacity, dev_error,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_paged_decode_workspace_size(int batch, int num_qo_heads, int head_dim,
+                                       int max_seqlen, int partition_size, int window_left) {
+    if (batch <= 0 || num_qo_heads <= 0 || head_dim <= 0 || max_seqlen < 0) return 256;
+    const int P = partition_size > 0 ? partition_size : kDefaultPartition;
+    const int np = decode_num_parts(max_seqlen, P, window_left);
+    return decode_layout(batch, num_qo_heads, head_dim, np).total;
+}
+
+pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            pkv_cache_desc cache, const int32_t *block_table,
+                            int max_blocks_per_seq, const int32_t *cache_seqlens,
+                            int max_seqlen, const float *sink, int batch, int num_qo_heads,
+                            int window_left, float sm_scale, int partition_size,
+                            float *lse_out, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_error, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || batch > 65535 || num_qo_heads <= 0 || max_seqlen < 0 ||
+        max_blocks_per_seq <= 0 || window_left < -1 || !std::isfinite(sm_scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_qo_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    const int G = num_qo_heads / cache.num_kv_heads;
+    if (G > 16) return PKV_ERR_UNSUPPORTED;
+    const int P = partition_size > 0 ? partition_size : kDefaultPartition;
+    if (partition_size < 0 || P % cache.block_size != 0 || P > kMaxPartition)
+        return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !cache_seqlens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_table, 4) || !aligned(cache_seqlens, 4))
+        return PKV_ERR_INVALID_ARG;
+    const int np = decode_num_parts(max_seqlen, P, window_left);
+    const DecodeLayout lay = decode_layout(batch, num_qo_heads, cache.head_dim, np);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.total)
+        return PKV_ERR_WORKSPACE;
+
+    DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.out = out;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_table = block_table;
+    p.seqlens = cache_seqlens;
+    p.sink = sink;
+    p.lse_out = lse_out;
+    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.lse_off);
+    p.part_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.o_off);
+    p.dev_error = dev_error;
+    p.num_blocks = cache.num_blocks;
+    p.batch = batch;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = cache.num_kv_heads;
+    p.group = G;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_seqlen = max_seqlen;
+    p.window_left = window_left;
+    p.partition_size = P;
+    p.num_parts = np;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+
+    alignas(64) CUtensorMap tk, tv;
+    std::memset(&tk, 0, sizeof tk);
+    std::memset(&tv, 0, sizeof tv);
+    if (cache.dtype == PKV_BF16) {
+        const int64_t rows = cache.num_blocks * cache.block_size;
+        if ((st = encode_rows_map(&tk, k_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
+                                  cache.block_size)) != PKV_OK)
+            return st;
+        if ((st = encode_rows_map(&tv, v_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
+                                  cache.block_size)) != PKV_OK)
+            return st;
+    }
+    return from_cuda(launch_decode(p, cache, &tk, &tv, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
+                                         int total_q, int max_seqlen_q) {
+    if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || total_q < 0) return 256;
+    const int G = num_kv_heads > 0 ? num_qo_heads / num_kv_heads : 1;
+    const int rows = G > 0 && G <= 128 ? 128 / G : 1;
+    (void)max_seqlen_q;
+    // one int4 work item per (128-row q tile, kv head) plus a counter
+    const size_t tiles = ((size_t)total_q / rows + batch + 1) * num_kv_heads;
+    return round_up(256 + tiles * 16, 256);
+}
+
+pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
+                              const void *v_cache, pkv_cache_desc cache,
+                              const int32_t *block_table, int max_blocks_per_seq,
+                              const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
+                              int max_seqlen_q, int max_seqlen_k, int total_q,
+                              const float *sink, int batch, int num_qo_heads, int causal,
+                              int window_left, float sm_scale, float *lse_out, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_error, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (!causal) return PKV_ERR_UNSUPPORTED;
+    if (batch < 0 || num_qo_heads <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+        total_q < 0 || max_blocks_per_seq <= 0 || window_left < -1 || !std::isfinite(sm_scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_qo_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    const int G = num_qo_heads / cache.num_kv_heads;
+    if (G > 16 || (G & (G - 1)) != 0) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0 || total_q == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !cu_seq_lens_q || !cu_seq_lens_k)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PKV_ERR_INVALID_ARG;
+    const size_t need = pkv_varlen_prefill_workspace_size(batch, num_qo_heads,
+                                                          cache.num_kv_heads, total_q,
+                                                          max_seqlen_q);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+        return PKV_ERR_WORKSPACE;
+
+    PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.out = out;
+    p.block_table = block_table;
+    p.cu_q = cu_seq_lens_q;
+    p.cu_k = cu_seq_lens_k;
+    p.sink = sink;
+    p.lse_out = lse_out;
+    p.tiles = static_cast<int32_t *>(workspace);
+    p.dev_error = dev_error;
+    p.num_blocks = cache.num_blocks;
+    p.batch = batch;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = cache.num_kv_heads;
+    p.group = G;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_seqlen_q = max_seqlen_q;
+    p.max_seqlen_k = max_seqlen_k;
+    p.total_q = total_q;
+    p.window_left = window_left;
+    p.rows_per_head = 128 / G;
+    p.max_tiles = (int)((need - 256) / 16);
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+
+    alignas(64) CUtensorMap tq, tk, tv;
+    const int64_t rows = cache.num_blocks * cache.block_size;
+    if ((st = encode_rows_map(&tq, q, cache.head_dim, num_qo_heads, total_q, G, 128 / G)) !=
+        PKV_OK)
+        return st;
+    if ((st = encode_rows_map(&tk, k_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
+                              cache.block_size)) != PKV_OK)
+        return st;
+    if ((st = encode_rows_map(&tv, v_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
+                              cache.block_size)) != PKV_OK)
+        return st;
+    return from_cuda(launch_prefill(p, cache, &tq, &tk, &tv, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

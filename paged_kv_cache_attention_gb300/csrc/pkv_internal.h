@@ -1,0 +1,73 @@
+// pkv_internal.h -- parameter blocks and launcher entry points shared by the
+// C-ABI layer (pkv_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// Split-KV decode: one CTA per (partition, kv head, sequence).
+struct DecodeParams {
+    const void *q;               // [B, Hq, D]
+    void *out;                   // [B, Hq, D]
+    const void *k_cache;         // pools (used by the kernels that do not use TMA)
+    const void *v_cache;
+    const int32_t *block_table;  // [B, max_blocks_per_seq]
+    const int32_t *seqlens;      // [B]
+    const float *sink;           // [Hq] or nullptr
+    float *lse_out;              // [B, Hq] or nullptr
+    float *part_lse;             // [B, Hq, num_parts] (log2 units)
+    float *part_o;               // [B, Hq, num_parts, D], normalised partial outputs
+    int32_t *dev_error;
+    int64_t num_blocks;
+    int batch, num_qo_heads, num_kv_heads, group;
+    int max_blocks_per_seq, max_seqlen;
+    int window_left;
+    int partition_size;
+    int num_parts;               // grid.x: partitions per sequence the grid covers
+    float scale_log2;            // sm_scale * log2(e)
+};
+
+// Varlen causal prefill on the paged pools.
+struct PrefillParams {
+    const void *q;                 // [total_q, Hq, D]
+    void *out;                     // [total_q, Hq, D]
+    const int32_t *block_table;    // [B, max_blocks_per_seq]
+    const int32_t *cu_q;           // [B+1]
+    const int32_t *cu_k;           // [B+1]
+    const float *sink;             // [Hq] or nullptr
+    float *lse_out;                // [total_q, Hq] or nullptr
+    int32_t *tiles;                // work list, built on the device
+    int32_t *dev_error;
+    int64_t num_blocks;
+    int batch, num_qo_heads, num_kv_heads, group;
+    int max_blocks_per_seq, max_seqlen_q, max_seqlen_k, total_q;
+    int window_left;
+    int rows_per_head;             // query tokens per 128-row tile (128 / group)
+    int max_tiles;                 // capacity of the work list
+    float scale_log2;
+};
+
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                     void *v_cache, const int64_t *slot_mapping,
+                                     int64_t num_tokens, int64_t row_bytes, int64_t capacity,
+                                     int32_t *dev_error, cudaStream_t stream);
+
+// Returns cudaErrorNotSupported when no kernel matches the shape.
+cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
+                          const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
+                          cudaStream_t stream);
+
+cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache,
+                           const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
+                           const CUtensorMap *tmap_v, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace pkv

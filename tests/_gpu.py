@@ -1,0 +1,89 @@
+"""Shared plumbing of the GPU parity tests: run a case through the C ABI
+(via the binding) and through the fp64 oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_attention_gb300 as pkv
+from paged_kv_cache_attention_gb300 import workloads as W
+
+# max-abs-error bars on attention outputs
+TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-5}
+# log-sum-exp (natural log) bars: fp32 logits of bf16 / fp32 inputs
+LSE_TOL = {torch.bfloat16: 2e-3, torch.float32: 1e-5}
+
+
+def dev():
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def to_dev(t):
+    return None if t is None else t.to(dev())
+
+
+def gpu_decode(case, partition_size=None, with_lse=False, err=None, max_seqlen=None):
+    d = dev()
+    lse = torch.empty(case.batch, case.num_qo_heads, dtype=torch.float32, device=d) \
+        if with_lse else None
+    out = pkv.paged_decode(to_dev(case.q), to_dev(case.k_cache), to_dev(case.v_cache),
+                           to_dev(case.block_table), to_dev(case.cache_seqlens),
+                           max_seqlen=case.max_seqlen if max_seqlen is None else max_seqlen,
+                           sink=to_dev(case.sink), window_left=case.window_left,
+                           sm_scale=case.sm_scale,
+                           partition_size=partition_size or case.partition_size, lse=lse,
+                           dev_error=err)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
+
+
+def oracle_decode(case, rows=None, with_lse=False):
+    return oracle.paged_decode(
+        W.to_oracle(case.q), W.to_oracle(case.k_cache), W.to_oracle(case.v_cache),
+        case.block_table.numpy(), case.cache_seqlens.numpy(),
+        sink=None if case.sink is None else case.sink.numpy(), window_left=case.window_left,
+        sm_scale=case.sm_scale, rows=rows, with_lse=with_lse)
+
+
+def gpu_prefill(case, with_lse=False, err=None):
+    d = dev()
+    lse = torch.empty(case.total_q, case.q.shape[1], dtype=torch.float32, device=d) \
+        if with_lse else None
+    out = pkv.varlen_prefill(to_dev(case.q), to_dev(case.k_cache), to_dev(case.v_cache),
+                             to_dev(case.block_table), to_dev(case.cu_seq_lens_q),
+                             to_dev(case.cu_seq_lens_k), case.max_seqlen_q, case.max_seqlen_k,
+                             sink=to_dev(case.sink), causal=case.causal,
+                             window_left=case.window_left, sm_scale=case.sm_scale, lse=lse,
+                             dev_error=err)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
+
+
+def oracle_prefill(case, rows=None, with_lse=False):
+    return oracle.attention(
+        W.to_oracle(case.q), W.to_oracle(case.k_cache), W.to_oracle(case.v_cache),
+        case.block_table.numpy(), case.cu_seq_lens_q.numpy(), case.kv_lens.numpy(),
+        sink=None if case.sink is None else case.sink.numpy(), causal=case.causal,
+        window_left=case.window_left, sm_scale=case.sm_scale, rows=rows, with_lse=with_lse)
+
+
+def max_abs(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    if a.size == 0:
+        return 0.0
+    assert np.isfinite(a).all(), "non-finite values in the GPU output"
+    return float(np.abs(a - b).max())
+
+
+def lse_err(a, b):
+    """max |a-b| over entries where both are finite; -inf must match -inf."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    fa, fb = np.isfinite(a), np.isfinite(b)
+    assert np.array_equal(fa, fb), "finite/-inf pattern of lse differs"
+    return float(np.abs(a[fa] - b[fb]).max()) if fa.any() else 0.0

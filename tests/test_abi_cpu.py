@@ -1,0 +1,141 @@
+"""The C-ABI library builds, loads and exports every symbol include/pkv.h
+declares; host-side sizing and validation behave as documented (CPU only: no
+kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import paged_kv_cache_attention_gb300 as pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def _declared_symbols():
+    names = []
+    for h in HEADERS:
+        src = open(h).read()
+        names += re.findall(r"PKV_API\s+[\w\s\*]*?\b(pkv_\w+)\s*\(", src)
+    return names
+
+
+def test_header_declares_the_three_operations():
+    names = _declared_symbols()
+    for op in ("pkv_reshape_and_cache", "pkv_paged_decode", "pkv_varlen_prefill"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = pkv.load_library()
+    declared = _declared_symbols()
+    assert declared, "no PKV_API declarations found"
+    for name in declared:
+        assert hasattr(lib, name), f"libpkv.so does not export {name}"
+    assert set(pkv.EXPORTED_SYMBOLS) <= set(declared)
+
+
+def test_status_strings_and_version():
+    lib = pkv.load_library()
+    assert lib.pkv_version() >= 100
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
+    assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
+
+
+def test_decode_workspace_size_grows_with_partitions():
+    a = pkv.paged_decode_workspace_size(64, 32, 128, 4096, 512)
+    b = pkv.paged_decode_workspace_size(64, 32, 128, 8192, 512)
+    assert b > a
+    # split-KV partials: B * Hq * P * (D + 1) floats, 256-byte rounded
+    assert a >= 64 * 32 * 8 * 129 * 4
+    # a window bounds the partitions a sequence can touch
+    w = pkv.paged_decode_workspace_size(8, 64, 64, 131072, 512, 127)
+    assert w <= 8 * 64 * 2 * 65 * 4 + 1024
+
+
+# ---------------------------------------------------------------------------
+# host validation: every case below is rejected before any CUDA call.  The
+# pointers are fake, so these run only where no GPU is present.
+# ---------------------------------------------------------------------------
+nogpu = pytest.mark.skipif(torch.cuda.is_available(),
+                           reason="fake-pointer validation tests run without a GPU only")
+FAKE = 0x10000  # 256-byte aligned, never dereferenced
+
+
+def _desc(nb=64, bs=16, hkv=8, d=128, dtype=1):
+    return pkv.CacheDesc(nb, bs, hkv, d, dtype)
+
+
+def _decode(lib, desc=None, batch=4, hq=32, window=-1, part=512, ws_bytes=1 << 30,
+            ws=FAKE, q=FAKE, max_blocks=8, max_seqlen=128, scale=0.1):
+    return lib.pkv_paged_decode(FAKE, q, FAKE, FAKE, desc or _desc(), FAKE, max_blocks, FAKE,
+                                max_seqlen, None, batch, hq, window, scale, part, None, ws,
+                                ws_bytes, None, None)
+
+
+@nogpu
+@pytest.mark.parametrize("kw,expected", [
+    (dict(desc=_desc(d=80)), 2),                 # head_dim without a kernel
+    (dict(desc=_desc(bs=8)), 2),                 # block size without a kernel
+    (dict(desc=_desc(dtype=7)), 2),              # unknown dtype
+    (dict(desc=_desc(nb=0)), 1),                 # empty pool
+    (dict(desc=_desc(nb=1 << 28)), 2),           # pool rows beyond int32
+    (dict(hq=30), 1),                            # Hq % Hkv != 0
+    (dict(hq=8 * 17), 2),                        # group of 17
+    (dict(part=500), 1),                         # partition not a multiple of the page
+    (dict(part=32768), 1),                       # partition above the maximum
+    (dict(window=-2), 1),                        # bad window
+    (dict(batch=-1), 1),
+    (dict(max_blocks=0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(ws=None), 3),                          # no workspace
+    (dict(ws=FAKE + 16), 3),                     # misaligned workspace
+    (dict(ws_bytes=1000), 3),                    # too small
+    (dict(q=FAKE + 2), 1),                       # misaligned q
+    (dict(batch=0), 0),                          # nothing to do
+])
+def test_decode_validation(kw, expected):
+    assert _decode(pkv.load_library(), **kw) == expected
+
+
+@nogpu
+def test_reshape_and_cache_validation():
+    lib = pkv.load_library()
+    f = lib.pkv_reshape_and_cache
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 0, _desc(), None, None) == 0
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, _desc(), None, None) == 1
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 3, _desc(), None, None) == 1
+    assert f(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 3, _desc(), None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, _desc(dtype=3), None, None) == 2
+    # fp32 rows of 3 heads x 4 dims = 48 bytes are fine; bf16 rows of 3 x 2 = 12 bytes are not
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, _desc(hkv=3, d=2, dtype=1), None, None) == 2
+
+
+@nogpu
+@pytest.mark.parametrize("change,expected", [
+    (dict(causal=0), 2),            # non-causal prefill not in this version
+    (dict(dtype=0), 2),             # fp32 prefill not in this version
+    (dict(hq=24), 2),               # group of 3 (not a power of two)
+    (dict(total_q=0), 0),
+    (dict(ws_bytes=16), 3),
+])
+def test_prefill_validation(change, expected):
+    lib = pkv.load_library()
+    a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30)
+    a.update(change)
+    st = lib.pkv_varlen_prefill(FAKE, FAKE, FAKE, FAKE, _desc(dtype=a["dtype"]), FAKE, 8, FAKE,
+                                FAKE, 64, 128, a["total_q"], None, 2, a["hq"], a["causal"], -1,
+                                0.1, None, FAKE, a["ws_bytes"], None, None)
+    assert st == expected
+
+
+def test_binding_rejects_cpu_tensors():
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkv.paged_decode(q, kc, kc, torch.zeros(2, 1, dtype=torch.int32),
+                         torch.zeros(2, dtype=torch.int32), max_seqlen=16)

@@ -1,0 +1,181 @@
+"""paged_decode on the GPU against the fp64 oracle on the same seeded inputs.
+
+Bars: max-abs error 1e-5 (fp32) / 2e-2 (bf16) on outputs; lse within 1e-5 /
+2e-3.  Pool pages no sequence owns hold NaN, so a stray read fails the test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_attention_gb300 as pkv
+from paged_kv_cache_attention_gb300 import workloads as W
+from tests._gpu import (LSE_TOL, TOL, dev, gpu_decode, lse_err, max_abs, oracle_decode,
+                        to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------------------
+# the tiny fp32 worked example
+# ---------------------------------------------------------------------------
+
+def test_tiny_fp32_example_attend():
+    case = W.config1_tiny()
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.float32]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.float32]
+
+
+def test_tiny_fp32_example_append_then_attend():
+    """Write each sequence's new token (slots 94, 32, 198) with
+    reshape_and_cache, then attend over [31, 33, 71]."""
+    case = W.config1_tiny()
+    d = dev()
+    kc, vc = case.k_cache.to(d), case.v_cache.to(d)
+    slots = torch.tensor([94, 32, 198], dtype=torch.int64, device=d)
+    pkv.reshape_and_cache(case.new_k.to(d), case.new_v.to(d), kc, vc, slots)
+    torch.cuda.synchronize()
+    case.k_cache, case.v_cache = kc.cpu(), vc.cpu()
+    case.cache_seqlens = case.cache_seqlens + 1
+    got = gpu_decode(case)
+    ref = oracle_decode(case)
+    assert max_abs(got, ref) <= TOL[torch.float32]
+
+
+# ---------------------------------------------------------------------------
+# bf16 tensor-core path: shapes, ragged tails, windows, sinks, partitions
+# ---------------------------------------------------------------------------
+
+SHAPES = [
+    # (Hq, Hkv, D, bs)
+    (32, 8, 128, 16),
+    (64, 8, 64, 16),
+    (8, 8, 128, 32),
+    (16, 2, 64, 32),
+    (32, 2, 128, 16),   # G = 16
+    (6, 2, 64, 16),     # G = 3
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs", SHAPES)
+@pytest.mark.parametrize("sink", ["none", "randn"])
+def test_bf16_shapes(Hq, Hkv, D, bs, sink):
+    lens = [1, 15, 16, 17, 511, 512, 513, 1500]
+    case = W.make_decode(lens, Hq, Hkv, D, bs, torch.bfloat16, seed=Hq * 7 + D + bs, sink=sink)
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("window", [0, 1, 5, 127, 511, 512, 1000, 5000])
+def test_bf16_windows(window):
+    lens = [1, 40, 512, 700, 2049, 3000]
+    case = W.make_decode(lens, 16, 4, 64, 16, torch.bfloat16, seed=window + 3, sink="randn",
+                         window_left=window)
+    got = gpu_decode(case)
+    ref = oracle_decode(case)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("part", [16, 32, 64, 512, 1024, 16384])
+def test_bf16_partition_sizes(part):
+    lens = [3, 100, 1000, 4000]
+    case = W.make_decode(lens, 32, 8, 128, 16, torch.bfloat16, seed=part, sink="randn")
+    got = gpu_decode(case, partition_size=part)
+    ref = oracle_decode(case)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+
+
+def test_partition_size_invariance():
+    """Split-KV is exact up to fp32 rounding: 512-token partitions and one
+    partition for the whole sequence agree far inside the bf16 bar."""
+    case = W.make_decode([5000, 333, 4096], 32, 8, 128, 16, torch.bfloat16, seed=9,
+                         sink="randn")
+    a = gpu_decode(case, partition_size=512)
+    b = gpu_decode(case, partition_size=16384)
+    assert np.abs(a - b).max() <= 1.6e-2  # at most a couple of bf16 ulps apart
+
+
+def test_block_relabelling_invariance():
+    case = W.make_decode([700, 33, 2000], 32, 8, 128, 16, torch.bfloat16, seed=10)
+    a = gpu_decode(case)
+    perm = torch.randperm(case.k_cache.shape[0], generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel())
+    case.k_cache = case.k_cache[perm].contiguous()
+    case.v_cache = case.v_cache[perm].contiguous()
+    bt = case.block_table.clone()
+    m = bt >= 0
+    bt[m] = inv[bt[m].long()].to(torch.int32)
+    case.block_table = bt
+    b = gpu_decode(case)
+    assert np.array_equal(a, b)  # same arithmetic in the same order
+
+
+def test_zero_length_sequences():
+    case = W.make_decode([0, 10, 0], 8, 2, 64, 16, torch.bfloat16, seed=11, sink="randn")
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    np.testing.assert_allclose(glse[0], case.sink.numpy(), rtol=0, atol=1e-6)
+
+
+def test_bad_block_id_is_flagged_not_read():
+    case = W.make_decode([64, 64], 8, 2, 64, 16, torch.bfloat16, seed=12)
+    case.block_table[1, 2] = case.k_cache.shape[0] + 5  # outside the pool
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    got = gpu_decode(case, err=err)
+    assert int(err.item()) & pkv.DEVERR_BLOCK_ID
+    assert np.isfinite(got).all()
+    ref = oracle_decode(case, rows=[0])
+    assert max_abs(got[:1], ref) <= TOL[torch.bfloat16]
+
+
+def test_seqlen_above_declared_max_is_flagged():
+    case = W.make_decode([100, 40], 8, 2, 64, 16, torch.bfloat16, seed=13)
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    gpu_decode(case, err=err, max_seqlen=64)
+    assert int(err.item()) & pkv.DEVERR_SEQLEN
+
+
+# ---------------------------------------------------------------------------
+# the serving configurations at full size
+# ---------------------------------------------------------------------------
+
+def test_config2_decode_full():
+    case = W.config2_decode()
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_config3_long_context(layer):
+    """Long-context split-KV decode: layer 0 (window 127) checked on every
+    sequence, layer 1 (full 32K-128K context) on two sampled sequences."""
+    case = W.config3_long(layer)
+    got = gpu_decode(case)
+    rows = None if layer == 0 else [0, 5]
+    ref = oracle_decode(case, rows=rows)
+    sel = got if rows is None else got[rows]
+    assert max_abs(sel, ref) <= TOL[torch.bfloat16]
+
+
+def test_config5_decode_half_after_cache_write():
+    """The decode half of the mixed step: write the new tokens, then attend
+    over cache length + 1 (sampled sequences)."""
+    case = W.config5_mixed()
+    d = dev()
+    kc, vc = case.k_cache.to(d), case.v_cache.to(d)
+    pkv.reshape_and_cache(case.key.to(d), case.value.to(d), kc, vc, case.slot_mapping.to(d))
+    torch.cuda.synchronize()
+    dec = case.decode
+    dec.k_cache, dec.v_cache = kc.cpu(), vc.cpu()
+    got = gpu_decode(dec)
+    rows = list(range(0, 256, 17))
+    ref = oracle_decode(dec, rows=rows)
+    assert max_abs(got[rows], ref) <= TOL[torch.bfloat16]
