@@ -88,6 +88,22 @@ DecodeLayout decode_layout(int batch, int Hq, int D, int num_parts) {
     return L;
 }
 
+// Work list of the prefill kernel: a 256-byte header (item count), one int4
+// per (query block, kv head) and the per-request block offsets.  A query
+// block holds 2 tiles of 128 / G tokens.
+struct PrefillLayout {
+    int64_t max_items;
+    size_t total;
+};
+
+PrefillLayout prefill_layout(int batch, int G, int num_kv_heads, int total_q) {
+    PrefillLayout L;
+    const int64_t tokens = G > 0 && G <= 128 ? 2 * (128 / G) : 1;
+    L.max_items = ((int64_t)total_q / tokens + batch) * num_kv_heads;
+    L.total = round_up(256 + (size_t)L.max_items * 16 + ((size_t)batch + 1) * 4, 256);
+    return L;
+}
+
 pkv_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return PKV_OK;
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
@@ -232,13 +248,12 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
 
 size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
                                          int total_q, int max_seqlen_q) {
-    if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || total_q < 0) return 256;
-    const int G = num_kv_heads > 0 ? num_qo_heads / num_kv_heads : 1;
-    const int rows = G > 0 && G <= 128 ? 128 / G : 1;
     (void)max_seqlen_q;
-    // one int4 work item per (128-row q tile, kv head) plus a counter
-    const size_t tiles = ((size_t)total_q / rows + batch + 1) * num_kv_heads;
-    return round_up(256 + tiles * 16, 256);
+    if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || total_q < 0 ||
+        num_qo_heads % num_kv_heads != 0)
+        return 256;
+    const int G = num_qo_heads / num_kv_heads;
+    return prefill_layout(batch, G, num_kv_heads, total_q).total;
 }
 
 pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
@@ -264,11 +279,10 @@ pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
         return PKV_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PKV_ERR_INVALID_ARG;
-    const size_t need = pkv_varlen_prefill_workspace_size(batch, num_qo_heads,
-                                                          cache.num_kv_heads, total_q,
-                                                          max_seqlen_q);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    const PrefillLayout lay = prefill_layout(batch, G, cache.num_kv_heads, total_q);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.total)
         return PKV_ERR_WORKSPACE;
+    if (lay.max_items > (int64_t)1 << 30) return PKV_ERR_UNSUPPORTED;
 
     PrefillParams p;
     std::memset(&p, 0, sizeof p);
@@ -292,7 +306,7 @@ pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
     p.total_q = total_q;
     p.window_left = window_left;
     p.rows_per_head = 128 / G;
-    p.max_tiles = (int)((need - 256) / 16);
+    p.max_tiles = (int)lay.max_items;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
 
     alignas(64) CUtensorMap tq, tk, tv;

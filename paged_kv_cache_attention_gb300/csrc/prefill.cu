@@ -1,14 +1,606 @@
-// prefill.cu -- varlen causal prefill on the paged pools (tcgen05 / TMEM).
+// prefill.cu -- causal varlen / chunk prefill on the paged pools, on the
+// 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// What it computes: for request r (q_len queries, kv_len keys addressed by
+// cu_seq_lens_q / cu_seq_lens_k, transformers docs "paged_attention", varlen
+// path) query row i sits at position kv_len - q_len + i and attends causally
+// (and within window_left) to its request's keys, read from the pages named by
+// block_table; the per-head sink joins the softmax denominator (FlashInfer
+// sink_attention_reference.py, varlen branch and sink_softmax).
+//
+// GB300 design.  One CTA takes NQ = 2 query tiles of 128 rows of one request
+// and one kv head.  The G query heads of the kv head are packed into the rows
+// (row = token * G + head), so every K/V byte staged in shared memory serves
+// 256 query rows.  Warp roles:
+//   warp 0      TMA producer: Q tiles once; per 128-key tile one 3-D box per
+//               (page, 64-dim half) of K and of V into a 2-stage ring
+//               (128-byte swizzle); pages past the end are fetched out of
+//               bounds, which fills zeros;
+//   warp 1      owns TMEM; one thread issues tcgen05.mma:
+//                 S_x = Q_x K^T   (A, B K-major in smem, fp32 in TMEM)
+//                 O_x += P_x V    (A = P in TMEM as bf16, B = V MN-major)
+//   warps 2..9  two softmax warpgroups, one per query tile; thread = row =
+//               TMEM lane.  Each reads its S row with tcgen05.ld, masks,
+//               updates the running max (O is rescaled in TMEM only when the
+//               max grows by more than 2^8), writes P back to TMEM in place of
+//               S, and finally normalises O (sink included) and stores it.
+// A small single-CTA kernel first builds the work list on the device
+// (counting sort by key-tile count, heaviest first).
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_tcgen05.cuh"
 
 namespace pkv {
+
+namespace {
+
+constexpr int kTileM = 128;   // query rows per tile
+constexpr int kTileN = 128;   // keys per tile
+constexpr int kHeadDim = 128;
+constexpr int kNQ = 2;        // query tiles per CTA
+constexpr int kStages = 2;    // K and V ring depth
+constexpr float kNegInf = -INFINITY;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct PfLayout {
+    static constexpr int Q_BYTES = kTileM * kHeadDim * 2;   // 32 KB
+    static constexpr int T_BYTES = kTileN * kHeadDim * 2;   // 32 KB per K or V tile
+    static constexpr int HALF = kTileN * 128;               // one 64-dim half: 16 KB
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + kNQ * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + kStages * T_BYTES;
+    static constexpr int OFF_BAR = OFF_V + kStages * T_BYTES;
+    // barriers
+    static constexpr int B_Q = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_KEMPTY = B_KFULL + kStages;
+    static constexpr int B_VFULL = B_KEMPTY + kStages;
+    static constexpr int B_VEMPTY = B_VFULL + kStages;
+    static constexpr int B_VFIX = B_VEMPTY + kStages;
+    static constexpr int B_SFULL = B_VFIX + 1;
+    static constexpr int B_PFULL = B_SFULL + kNQ;
+    static constexpr int B_ODONE = B_PFULL + kNQ;
+    static constexpr int NBARS = B_ODONE + kNQ;
+    static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM = 1024 + OFF_TMEM + 16;
+    static constexpr int THREADS = 64 + kNQ * 128;
+    static constexpr int TMEM_COLS = 512;  // O_0, O_1, S_0, S_1: 128 columns each
+};
+
+__host__ __device__ constexpr int o_col(int x) { return x * 128; }
+__host__ __device__ constexpr int s_col(int x) { return kNQ * 128 + x * 128; }
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023);
+    return reinterpret_cast<uint8_t *>(a);
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+}
+
+// Per-CTA geometry of one work item.
+struct Geo {
+    int r, t0, g;
+    int q_start, q_len, kv_len;
+    int kt_lo, ntiles;
+};
+
+__device__ __forceinline__ int clip_len(int v, int cap, int32_t *err, bool report) {
+    if (v < 0) {
+        if (report) flag_error(err, PKV_DEVERR_SEQLEN);
+        return 0;
+    }
+    if (v > cap) {
+        if (report) flag_error(err, PKV_DEVERR_SEQLEN);
+        return cap;
+    }
+    return v;
+}
+
+__device__ __forceinline__ Geo make_geo(const PrefillParams &p, int4 item, int block_size,
+                                        bool report) {
+    Geo G;
+    G.r = item.x;
+    G.t0 = item.y;
+    G.g = item.z;
+    G.q_start = p.cu_q[G.r];
+    G.q_len = clip_len(p.cu_q[G.r + 1] - G.q_start, p.max_seqlen_q, p.dev_error, report);
+    int cap_k = p.max_seqlen_k;
+    const long long cap_blocks = (long long)p.max_blocks_per_seq * block_size;
+    if (cap_blocks < cap_k) cap_k = (int)cap_blocks;
+    G.kv_len = clip_len(p.cu_k[G.r + 1] - p.cu_k[G.r], cap_k, p.dev_error, report);
+    const int tokens = kNQ * p.rows_per_head;
+    const int t_end = min(G.t0 + tokens, G.q_len);
+    const int qpos_min = G.kv_len - G.q_len + G.t0;
+    const int qpos_max = G.kv_len - G.q_len + t_end - 1;
+    const int hi = min(G.kv_len, qpos_max + 1);
+    int lo = 0;
+    if (p.window_left >= 0) lo = max(0, qpos_min - p.window_left);
+    if (hi <= lo || t_end <= G.t0) {
+        G.kt_lo = 0;
+        G.ntiles = 0;
+    } else {
+        G.kt_lo = lo / kTileN;
+        G.ntiles = (hi - 1) / kTileN - G.kt_lo + 1;
+    }
+    return G;
+}
+
+// ---------------------------------------------------------------------------
+// work list: items {request, first query token, kv head, cost} sorted by cost
+// (key tiles), heaviest first.  Single CTA.
+// ---------------------------------------------------------------------------
+constexpr int kSchedThreads = 1024;
+constexpr int kBuckets = 1024;
+
+__device__ __forceinline__ int item_cost(const PrefillParams &p, int q_len, int kv_len, int t0) {
+    const int tokens = kNQ * p.rows_per_head;
+    const int t_end = min(t0 + tokens, q_len);
+    const int qpos_min = kv_len - q_len + t0;
+    const int hi = min(kv_len, kv_len - q_len + t_end);
+    int lo = 0;
+    if (p.window_left >= 0) lo = max(0, qpos_min - p.window_left);
+    if (hi <= lo) return 0;
+    return (hi - 1) / kTileN - lo / kTileN + 1;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const PrefillParams p) {
+    __shared__ int hist[kBuckets];
+    __shared__ int wsum[kSchedThreads / 32];
+    __shared__ int total_pairs_s;
+    int *count = p.tiles;                                      // [0]: number of items
+    int4 *items = reinterpret_cast<int4 *>(p.tiles + 64);      // 256-byte header
+    int *offs = p.tiles + 64 + 4 * p.max_tiles;                // [batch + 1] pair offsets
+    const int tid = threadIdx.x;
+    const int tokens = kNQ * p.rows_per_head;
+
+    // 1. pairs (request, q block) per request, exclusive prefix sum
+    int carry = 0;
+    for (int base = 0; base < p.batch; base += kSchedThreads) {
+        const int r = base + tid;
+        int n = 0;
+        if (r < p.batch) {
+            int ql = p.cu_q[r + 1] - p.cu_q[r];
+            ql = ql < 0 ? 0 : min(ql, p.max_seqlen_q);
+            n = (ql + tokens - 1) / tokens;
+        }
+        // block scan
+        int v = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, v, off);
+            if ((tid & 31) >= off) v += o;
+        }
+        if ((tid & 31) == 31) wsum[tid >> 5] = v;
+        __syncthreads();
+        if (tid < 32) {
+            int w = tid < kSchedThreads / 32 ? wsum[tid] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, w, off);
+                if (tid >= off) w += o;
+            }
+            if (tid < kSchedThreads / 32) wsum[tid] = w;
+        }
+        __syncthreads();
+        const int excl = carry + v - n + ((tid >> 5) ? wsum[(tid >> 5) - 1] : 0);
+        if (r < p.batch) offs[r] = excl;
+        const int block_total = wsum[kSchedThreads / 32 - 1];
+        __syncthreads();
+        carry += block_total;
+    }
+    if (tid == 0) {
+        offs[p.batch] = carry;
+        total_pairs_s = carry;
+    }
+    for (int i = tid; i < kBuckets; i += kSchedThreads) hist[i] = 0;
+    __syncthreads();
+    const int total_pairs = total_pairs_s;
+    const int n_items = min(total_pairs * p.num_kv_heads, p.max_tiles);
+
+    // locate the request of pair i by binary search over offs
+    auto pair_of = [&](int i, int &r, int &t0, int &cost) {
+        int lo = 0, hi = p.batch;  // offs[lo] <= i < offs[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (offs[mid] <= i) lo = mid; else hi = mid;
+        }
+        r = lo;
+        t0 = (i - offs[r]) * tokens;
+        int ql = p.cu_q[r + 1] - p.cu_q[r];
+        ql = ql < 0 ? 0 : min(ql, p.max_seqlen_q);
+        int kl = p.cu_k[r + 1] - p.cu_k[r];
+        kl = kl < 0 ? 0 : min(kl, p.max_seqlen_k);
+        cost = min(item_cost(p, ql, kl, t0), kBuckets - 1);
+    };
+
+    // 2. histogram of costs (per pair; each pair yields num_kv_heads items)
+    for (int i = tid; i < total_pairs; i += kSchedThreads) {
+        int r, t0, c;
+        pair_of(i, r, t0, c);
+        atomicAdd(&hist[c], p.num_kv_heads);
+    }
+    __syncthreads();
+    // 3. exclusive scan from the heaviest bucket down (sequential: 1024 buckets)
+    if (tid == 0) {
+        int acc = 0;
+        for (int b = kBuckets - 1; b >= 0; --b) {
+            const int h = hist[b];
+            hist[b] = acc;
+            acc += h;
+        }
+    }
+    __syncthreads();
+    // 4. scatter
+    for (int i = tid; i < total_pairs; i += kSchedThreads) {
+        int r, t0, c;
+        pair_of(i, r, t0, c);
+        const int pos = atomicAdd(&hist[c], p.num_kv_heads);
+        for (int g = 0; g < p.num_kv_heads; ++g)
+            if (pos + g < p.max_tiles) items[pos + g] = make_int4(r, t0, g, c);
+    }
+    if (tid == 0) *count = n_items;
+}
+
+// ---------------------------------------------------------------------------
+// the attention kernel
+// ---------------------------------------------------------------------------
+template <int BS>
+__global__ void __launch_bounds__(PfLayout::THREADS, 1)
+prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
+                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    using Lay = PfLayout;
+    constexpr int NPG = kTileN / BS;  // pages per key tile
+
+    if ((int)blockIdx.x >= p.tiles[0]) return;  // beyond the work list
+    const int4 item = reinterpret_cast<const int4 *>(p.tiles + 64)[blockIdx.x];
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + Lay::OFF_Q, sK = sbase + Lay::OFF_K, sV = sbase + Lay::OFF_V;
+    const uint32_t bars = sbase + Lay::OFF_BAR;
+    auto bar = [&](int i) { return bars + 8u * i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo geo = make_geo(p, item, BS, threadIdx.x == 0);
+    const int G = p.group;
+    const int TPR = p.rows_per_head;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Lay::NBARS; ++i)
+            mbar_init(bar(i), (i >= Lay::B_PFULL && i < Lay::B_PFULL + kNQ) ? 128u : 1u);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int ntiles = geo.ntiles;
+    const int last_key_end = (geo.kt_lo + ntiles) * kTileN;
+    const bool tail = ntiles > 0 && last_key_end > geo.kv_len;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (ntiles > 0) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tmq);
+                tma_prefetch_desc(&tmk);
+                tma_prefetch_desc(&tmv);
+                mbar_arrive_expect_tx(bar(Lay::B_Q), kNQ * Lay::Q_BYTES);
+                for (int x = 0; x < kNQ; ++x)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(sQ + x * Lay::Q_BYTES + h * Lay::HALF, &tmq, bar(Lay::B_Q),
+                                    h * 64, geo.g * G, geo.q_start + geo.t0 + x * TPR);
+            }
+            const int32_t *bt = p.block_table + (int64_t)geo.r * p.max_blocks_per_seq;
+            const int oob_row = (int)(p.num_blocks * BS);
+            bool alive = true;
+            for (int j = 0; j < ntiles && alive; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                const int key0 = (geo.kt_lo + j) * kTileN;
+                int row = oob_row;
+                if (lane < NPG) {
+                    const int pos = key0 + lane * BS;
+                    if (pos < geo.kv_len) {
+                        const int blk = bt[pos / BS];
+                        if (blk < 0 || blk >= p.num_blocks)
+                            flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
+                        else
+                            row = blk * BS;
+                    }
+                }
+                // K
+                alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error);
+                if (!alive) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_KFULL + s), Lay::T_BYTES);
+                __syncwarp();
+                {
+                    const int pg = min(lane >> 1, NPG - 1), h = lane & 1;
+                    const int rw = __shfl_sync(0xffffffffu, row, pg);
+                    if (lane < 2 * NPG)
+                        tma_load_3d(sK + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmk,
+                                    bar(Lay::B_KFULL + s), h * 64, geo.g, rw);
+                }
+                // V
+                alive = mbar_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error);
+                if (!alive) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_VFULL + s), Lay::T_BYTES);
+                __syncwarp();
+                {
+                    const int pg = min(lane >> 1, NPG - 1), h = lane & 1;
+                    const int rw = __shfl_sync(0xffffffffu, row, pg);
+                    if (lane < 2 * NPG)
+                        tma_load_3d(sV + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmv,
+                                    bar(Lay::B_VFULL + s), h * 64, geo.g, rw);
+                }
+                if (j == ntiles - 1 && tail) {
+                    // rows at or past kv_len of the last value tile may hold any
+                    // bits: zero them so P = 0 never meets a non-finite value
+                    alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
+                    if (!alive) break;
+                    const int first = max(geo.kv_len - key0, 0);
+                    const uint32_t vb = sV + s * Lay::T_BYTES;
+                    for (int e = first * 16 + lane; e < kTileN * 16; e += 32) {
+                        const int rr = e >> 4, c = e & 15;
+                        st_shared_zero16(vb + (c >> 3) * Lay::HALF + sw128(rr, c & 7));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(Lay::B_VFIX));
+                }
+            }
+            // Let the MMA issuer's last "stage empty" arrivals land before the
+            // CTA can exit.
+            for (int j = max(0, ntiles - kStages); j < ntiles && alive; ++j) {
+                const uint32_t ph = (j >> 1) & 1;
+                alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + (j & 1)), ph, p.dev_error) &&
+                        mbar_wait_bounded(bar(Lay::B_VEMPTY + (j & 1)), ph, p.dev_error);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (ntiles > 0 && lane == 0) {
+            constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
+            constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
+            bool alive = mbar_wait_bounded(bar(Lay::B_Q), 0, p.dev_error);
+            for (int j = 0; j < ntiles && alive; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                alive = mbar_wait_bounded(bar(Lay::B_KFULL + s), ph, p.dev_error);
+                if (!alive) break;
+                tc::fence_after_sync();
+                for (int x = 0; x < kNQ; ++x) {
+                    if (j > 0) {
+                        // P_x(j-1) lives where S_x(j) goes: PV_x(j-1) must be done
+                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + x), (j - 1) & 1, p.dev_error);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * Lay::HALF + (kk & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(sQ + x * Lay::Q_BYTES + koff, 16, 1024);
+                        const uint64_t b = tc::smem_desc_sw128(sK + s * Lay::T_BYTES + koff, 16, 1024);
+                        tc::mma_ss(tmem + s_col(x), a, b, idS, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(bar(Lay::B_SFULL + x));
+                }
+                if (!alive) break;
+                tc::commit(bar(Lay::B_KEMPTY + s));
+                for (int x = 0; x < kNQ; ++x) {
+                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + x), j & 1, p.dev_error);
+                    if (!alive) break;
+                    tc::fence_after_sync();
+                    if (x == 0) {
+                        if (j == ntiles - 1 && tail)
+                            alive = mbar_wait_bounded(bar(Lay::B_VFIX), 0, p.dev_error);
+                        else
+                            alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk) {
+                        const uint64_t b =
+                            tc::smem_desc_sw128(sV + s * Lay::T_BYTES + kk * 2048, Lay::HALF, 1024);
+                        tc::mma_ts(tmem + o_col(x), tmem + s_col(x) + kk * 8, b, idO,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(bar(Lay::B_ODONE + x));
+                }
+                if (!alive) break;
+                tc::commit(bar(Lay::B_VEMPTY + s));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int x = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int tok_local = row / G;
+        const int h_local = row - tok_local * G;
+        const int tok = geo.t0 + x * TPR + tok_local;
+        const bool row_valid = tok < geo.q_len;
+        const int qpos = geo.kv_len - geo.q_len + tok;
+        const int head = geo.g * G + h_local;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + s_col(x);
+        const uint32_t tO = tmem + lane_off + o_col(x);
+        const float sl2 = p.scale_log2;
+        const int wl = p.window_left;
+
+        float m_run = kNegInf, l_run = 0.f;
+        bool alive = true;
+        for (int j = 0; j < ntiles; ++j) {
+            alive = __all_sync(0xffffffffu,
+                               mbar_wait_bounded(bar(Lay::B_SFULL + x), j & 1, p.dev_error));
+            if (!alive) break;
+            tc::fence_after_sync();
+            const int key0 = (geo.kt_lo + j) * kTileN;
+            const bool full = (key0 + kTileN - 1 <= qpos) && (key0 + kTileN <= geo.kv_len) &&
+                              (wl < 0 || key0 >= qpos - wl);
+            // keys this row keeps: [klo, khi] (inclusive), relative to key0
+            const int khi = min(qpos, geo.kv_len - 1) - key0;
+            const int klo = wl < 0 ? -1 : qpos - wl - key0;
+            // pass 1: row maximum over the tile, 32 columns at a time
+            float mx = kNegInf;
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c) {
+                uint32_t r32[32];
+                tc::ld_32x32b_x32(tS + c * 32, r32);
+                tc::wait_ld();
+                if (full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(r32[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int k = c * 32 + i;
+                        if (k <= khi && k >= klo) mx = fmaxf(mx, __uint_as_float(r32[i]));
+                    }
+                }
+            }
+            const float m_tile = mx * sl2;
+            const bool grow = m_tile > m_run + kRescaleThreshold;
+            // tcgen05.ld/st are warp-collective: the warp rescales together,
+            // lanes whose maximum did not grow enough multiply by 1
+            if (__any_sync(0xffffffffu, grow)) {
+                const float alpha = grow ? fast_exp2(m_run - m_tile) : 1.f;
+                l_run *= alpha;
+                if (j > 0) {
+#pragma unroll
+                    for (int c = 0; c < kHeadDim / 32; ++c) {
+                        uint32_t r32[32];
+                        tc::ld_32x32b_x32(tO + c * 32, r32);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r32[i] = __float_as_uint(__uint_as_float(r32[i]) * alpha);
+                        tc::st_32x32b_x32(tO + c * 32, r32);
+                    }
+                }
+                if (grow) m_run = m_tile;
+            }
+            // pass 2: P = 2^(s * scale - m) as bf16, written over S (64 columns)
+            const float msub = m_run == kNegInf ? 0.f : m_run;
+            float psum = 0.f;
+#pragma unroll
+            for (int c2 = 0; c2 < kTileN / 64; ++c2) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = 2 * c2 + h;
+                    uint32_t r32[32];
+                    tc::ld_32x32b_x32(tS + c * 32, r32);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int k = c * 32 + 2 * i;
+                        float p0 = fast_exp2(fmaf(__uint_as_float(r32[2 * i]), sl2, -msub));
+                        float p1 = fast_exp2(fmaf(__uint_as_float(r32[2 * i + 1]), sl2, -msub));
+                        if (!full) {
+                            p0 = (k <= khi && k >= klo) ? p0 : 0.f;
+                            p1 = (k + 1 <= khi && k + 1 >= klo) ? p1 : 0.f;
+                        }
+                        psum += p0 + p1;
+                        pk[h * 16 + i] = pack_bf16(p0, p1);
+                    }
+                }
+                tc::st_32x32b_x32(tS + c2 * 32, pk);
+            }
+            l_run += psum;
+            tc::wait_st();
+            tc::fence_before_sync();
+            mbar_arrive(bar(Lay::B_PFULL + x));
+        }
+        // epilogue: normalise (sink in the denominator) and store
+        bool have_o = ntiles > 0 && alive;
+        if (have_o) {
+            have_o = __all_sync(0xffffffffu, mbar_wait_bounded(bar(Lay::B_ODONE + x),
+                                                               (ntiles - 1) & 1, p.dev_error));
+            tc::fence_after_sync();
+        }
+        const float sink_l2 = p.sink ? p.sink[head] * kLog2e : kNegInf;
+        const float M = fmaxf(m_run, sink_l2);
+        float oscale = 0.f, lse = kNegInf;
+        if (M != kNegInf) {
+            const float f = fast_exp2(m_run - M);
+            const float Z = l_run * f + fast_exp2(sink_l2 - M);
+            oscale = f / Z;
+            lse = (M + log2f(Z)) * kLn2;
+        }
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) +
+                              ((int64_t)(geo.q_start + tok) * p.num_qo_heads + head) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < kHeadDim / 32; ++c) {
+            uint32_t r32[32];
+            if (have_o) {  // warp-uniform: every lane takes part in the load
+                tc::ld_32x32b_x32(tO + c * 32, r32);
+                tc::wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r32[i] = 0u;
+            }
+            if (row_valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = 8 * i;
+                    dst[i] = make_uint4(
+                        pack_bf16(__uint_as_float(r32[e + 0]) * oscale, __uint_as_float(r32[e + 1]) * oscale),
+                        pack_bf16(__uint_as_float(r32[e + 2]) * oscale, __uint_as_float(r32[e + 3]) * oscale),
+                        pack_bf16(__uint_as_float(r32[e + 4]) * oscale, __uint_as_float(r32[e + 5]) * oscale),
+                        pack_bf16(__uint_as_float(r32[e + 6]) * oscale, __uint_as_float(r32[e + 7]) * oscale));
+                }
+            }
+        }
+        if (row_valid && p.lse_out)
+            p.lse_out[(int64_t)(geo.q_start + tok) * p.num_qo_heads + head] = lse;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, Lay::TMEM_COLS);
+    }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
 
 cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache,
                            const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
                            const CUtensorMap *tmap_v, cudaStream_t stream) {
-    (void)p; (void)cache; (void)tmap_q; (void)tmap_k; (void)tmap_v; (void)stream;
-    return cudaErrorNotSupported;
+    if (cache.head_dim != kHeadDim || cache.dtype != PKV_BF16) return cudaErrorNotSupported;
+    prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int grid = p.max_tiles;
+    if (grid <= 0) return cudaSuccess;
+    if (cache.block_size == 16) {
+        auto k = prefill_tc_kernel<16>;
+        if ((e = set_smem(k, PfLayout::SMEM)) != cudaSuccess) return e;
+        k<<<grid, PfLayout::THREADS, PfLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k, *tmap_v);
+    } else if (cache.block_size == 32) {
+        auto k = prefill_tc_kernel<32>;
+        if ((e = set_smem(k, PfLayout::SMEM)) != cudaSuccess) return e;
+        k<<<grid, PfLayout::THREADS, PfLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k, *tmap_v);
+    } else {
+        return cudaErrorNotSupported;
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace pkv

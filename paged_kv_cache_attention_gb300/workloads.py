@@ -244,6 +244,24 @@ def make_varlen(q_lens, prefix_lens, num_qo_heads, num_kv_heads, head_dim, block
                       cumsum0(ql), cumsum0(kvl), sk, window_left, scale, causal)
 
 
+def make_varlen_kv(q_lens, kv_lens, num_qo_heads, num_kv_heads, head_dim, block_size, dtype,
+                   seed, sink: str = "randn", window_left: int = -1,
+                   sm_scale: Optional[float] = None, spare: int = 64, causal: bool = True,
+                   name: str = "varlen") -> VarlenCase:
+    """A varlen batch with explicit per-request kv lengths (q_len may exceed
+    kv_len; such rows sit at negative positions and attend to nothing)."""
+    gen = _gen(seed)
+    ql = torch.tensor([int(x) for x in q_lens], dtype=torch.int32)
+    kvl = torch.tensor([int(x) for x in kv_lens], dtype=torch.int32)
+    pc = [pages_for(int(L), block_size) for L in kvl]
+    pool = build_pool([pc], block_size, num_kv_heads, head_dim, dtype, gen, spare=spare)
+    q = randn((int(ql.sum()), num_qo_heads, head_dim), dtype, gen)
+    sk = _make_sink(sink, num_qo_heads, gen)
+    scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(head_dim)
+    return VarlenCase(name, q, pool.k_cache, pool.v_cache, pool.block_tables[0],
+                      cumsum0(ql), cumsum0(kvl), sk, window_left, scale, causal)
+
+
 # ---------------------------------------------------------------------------
 # the five serving configurations
 # ---------------------------------------------------------------------------

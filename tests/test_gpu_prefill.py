@@ -1,0 +1,150 @@
+"""varlen_prefill on the GPU against the fp64 oracle on the same seeded inputs.
+
+Bar: max-abs error 2e-2 on bf16 outputs (P is rounded to bf16 before the PV
+product, the oracle is exact), lse within 2e-3.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_attention_gb300 as pkv
+from paged_kv_cache_attention_gb300 import workloads as W
+from tests._gpu import (LSE_TOL, TOL, dev, gpu_decode, gpu_prefill, lse_err, max_abs,
+                        oracle_decode, oracle_prefill)
+
+pytestmark = pytest.mark.gpu
+BF16 = torch.bfloat16
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _check(case, rows=None, lse=True):
+    got, glse = gpu_prefill(case, with_lse=True)
+    ref, rlse = oracle_prefill(case, rows=rows, with_lse=True)
+    if rows is not None:
+        got, glse = got[rows], glse[rows]
+    assert max_abs(got, ref) <= TOL[BF16]
+    if lse:
+        assert lse_err(glse, rlse) <= LSE_TOL[BF16]
+    return got
+
+
+def test_varlen_example_of_the_page():
+    """cu_seq_lens_q [0,10,13,14], cu_seq_lens_k [0,0,1,8]: request 0 has no
+    key (10 zero rows), request 1 has 3 queries over 1 key (rows at positions
+    -2, -1 see nothing, the last sees key 0), request 2 one query over 7 keys."""
+    g = json.load(open(os.path.join(GOLDEN, "varlen_example.json")))
+    case = W.make_varlen_kv(g["q_lens"], g["k_lens"], 8, 2, 128, 16, BF16, seed=21,
+                            sink="randn")
+    assert case.cu_seq_lens_q.tolist() == g["cu_seq_lens_q"]
+    assert case.cu_seq_lens_k.tolist() == g["cu_seq_lens_k"]
+    got = _check(case)
+    assert np.all(got[:12] == 0) and np.all(got[12:] != 0)
+
+
+@pytest.mark.parametrize("G,Hkv", [(1, 4), (2, 4), (4, 8), (8, 2), (16, 1)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_group_sizes_and_pages(G, Hkv, bs):
+    q_lens = [1, 7, 33, 64, 129, 300]
+    prefix = [0, 100, 5, 128, 1000, 77]
+    case = W.make_varlen(q_lens, prefix, G * Hkv, Hkv, 128, bs, BF16, seed=G * 31 + bs,
+                         sink="randn")
+    _check(case)
+
+
+@pytest.mark.parametrize("sink", ["none", "randn"])
+@pytest.mark.parametrize("window", [-1, 0, 7, 127, 128, 1000])
+def test_windows_and_sinks(sink, window):
+    q_lens = [200, 1, 513, 64]
+    prefix = [300, 2000, 0, 64]
+    case = W.make_varlen(q_lens, prefix, 32, 8, 128, 16, BF16, seed=window + 50, sink=sink,
+                         window_left=window)
+    _check(case)
+
+
+def test_empty_requests_and_ragged_tails():
+    q_lens = [0, 5, 0, 127, 128, 129, 1]
+    kv_lens = [10, 5, 0, 127, 1000, 129, 0]
+    case = W.make_varlen_kv(q_lens, kv_lens, 16, 4, 128, 16, BF16, seed=22, sink="randn")
+    _check(case)
+
+
+def test_decode_equals_prefill_with_one_query():
+    """Cross-op: paged_decode == varlen_prefill with q_len = 1 per request."""
+    dec = W.make_decode([1, 300, 1024, 4097], 32, 8, 128, 16, BF16, seed=23, sink="randn",
+                        window_left=500)
+    B = dec.batch
+    var = W.VarlenCase("as-prefill", dec.q, dec.k_cache, dec.v_cache, dec.block_table,
+                       W.cumsum0(torch.ones(B, dtype=torch.int32)),
+                       W.cumsum0(dec.cache_seqlens), dec.sink, dec.window_left, dec.sm_scale)
+    a = gpu_decode(dec)
+    b = gpu_prefill(var)
+    assert np.abs(a - b).max() <= 2e-2
+    assert max_abs(b, oracle_decode(dec)) <= TOL[BF16]
+
+
+def test_chunk_is_suffix_of_longer_chunk():
+    """A chunk of the last 40 queries equals the last 40 rows of a 300-query
+    chunk over the same keys (mask aligned to the end of kv)."""
+    long_ = W.make_varlen([300], [700], 32, 8, 128, 16, BF16, seed=24, sink="randn")
+    short = W.VarlenCase("short", long_.q[-40:].contiguous(), long_.k_cache, long_.v_cache,
+                         long_.block_table, W.cumsum0(torch.tensor([40], dtype=torch.int32)),
+                         long_.cu_seq_lens_k, long_.sink, -1, long_.sm_scale)
+    a = gpu_prefill(long_)
+    b = gpu_prefill(short)
+    assert np.abs(a[-40:] - b).max() <= 2e-2
+
+
+def test_block_relabelling_invariance():
+    case = W.make_varlen([150, 40], [500, 9], 32, 8, 128, 16, BF16, seed=25)
+    a = gpu_prefill(case)
+    perm = torch.randperm(case.k_cache.shape[0], generator=torch.Generator().manual_seed(4))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel())
+    case.k_cache = case.k_cache[perm].contiguous()
+    case.v_cache = case.v_cache[perm].contiguous()
+    bt = case.block_table.clone()
+    m = bt >= 0
+    bt[m] = inv[bt[m].long()].to(torch.int32)
+    case.block_table = bt
+    b = gpu_prefill(case)
+    assert np.array_equal(a, b)
+
+
+def test_bad_block_id_is_flagged():
+    case = W.make_varlen([40, 40], [100, 100], 8, 2, 128, 16, BF16, seed=26)
+    case.block_table[1, 3] = -7
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    got = gpu_prefill(case, err=err)
+    assert int(err.item()) & pkv.DEVERR_BLOCK_ID
+    assert np.isfinite(got).all()
+    ref = oracle_prefill(case, rows=list(range(40)))
+    assert max_abs(got[:40], ref) <= TOL[BF16]
+
+
+def _sample_rows(case, n_per_req=4):
+    rows = []
+    cu = case.cu_seq_lens_q.tolist()
+    for r in range(case.batch):
+        a, b = cu[r], cu[r + 1]
+        if b > a:
+            rows += sorted({a, b - 1, (a + b) // 2, a + (b - a) // 3})[:n_per_req]
+    return rows
+
+
+def test_config4_prefill_full_size_sampled():
+    case = W.config4_prefill()
+    _check(case, rows=_sample_rows(case))
+
+
+def test_config5_prefill_half_after_cache_write():
+    case = W.config5_mixed()
+    d = dev()
+    kc, vc = case.k_cache.to(d), case.v_cache.to(d)
+    pkv.reshape_and_cache(case.key.to(d), case.value.to(d), kc, vc, case.slot_mapping.to(d))
+    torch.cuda.synchronize()
+    pre = case.prefill
+    pre.k_cache, pre.v_cache = kc.cpu(), vc.cpu()
+    _check(pre, rows=_sample_rows(pre, 3), lse=False)
