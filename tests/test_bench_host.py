@@ -1,0 +1,75 @@
+"""Host-side logic of bench.py on CPU: the work accounting, and the
+max-over-ranks timing of the replica run on 2 gloo ranks."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+from paged_kv_cache_attention_gb300 import workloads as W
+
+
+def test_attended_pairs_matches_a_mask_count():
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        q = int(rng.integers(0, 40))
+        k = int(rng.integers(0, 60))
+        w = int(rng.choice([-1, 0, 3, 10]))
+        pos = (k - q + np.arange(q))[:, None]
+        col = np.arange(k)[None, :]
+        m = col <= pos
+        if w >= 0:
+            m &= col >= pos - w
+        assert bench.attended_pairs(q, k, w) == int(m.sum())
+
+
+def test_prefill_flops_of_the_mixed_step():
+    case = W.make_mixed([100, 200], 64, 128, 2, 32, 8, 128, 16, torch.bfloat16, seed=1)
+    # each chunk: 64 queries over 128 + 64 keys, causal at the end
+    pairs = sum(128 + i + 1 for i in range(64))
+    assert bench.prefill_flops(case.prefill) == 4 * 32 * 128 * 2 * pairs
+
+
+def test_decode_bytes_count_window():
+    case = W.make_decode([10, 1000], 8, 2, 64, 16, torch.bfloat16, seed=2, window_left=99)
+    assert bench.kv_bytes_decode(case) == (10 + 100) * 2 * 64 * 2 * 2
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    d = bench.Dist()
+    try:
+        assert d.on and d.world == world and d.rank == rank
+        d.barrier()
+        m = d.max(1.5 + rank)  # per-rank step times: the slowest one wins
+        q.put((rank, m))
+    finally:
+        d.close()
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="gloo replica test runs on CPU hosts")
+def test_max_over_ranks_with_gloo():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(world))
+    assert got == {0: 2.5, 1: 2.5}
