@@ -183,6 +183,39 @@ PKV_API pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_ca
                               int window_left, float sm_scale, float *lse_out, void *workspace,
                               size_t workspace_bytes, int32_t *dev_error, void *stream);
 
+/*
+ * paged_decode_noalloc: paged_decode for callers that cannot allocate device
+ * memory at the call site -- for example a plug-in whose host framework owns
+ * all device memory and exposes no allocator to it, or a serving loop that
+ * must not allocate once it is running.  The pages have no counterpart: this
+ * entry point exists only for such callers.
+ *
+ * It takes the same arguments as pkv_paged_decode minus the workspace.  The
+ * split-KV scratch is instead a fixed device array inside the library of
+ * PKV_NOALLOC_DECODE_SCRATCH_BYTES bytes; every GPU that loads the library
+ * holds that array until the process exits.  A problem whose scratch need
+ * (pkv_paged_decode_workspace_size) exceeds it is rejected with
+ * PKV_ERR_WORKSPACE before anything is launched.  The caller still provides
+ * out, q, the pools and the metadata; nothing is allocated.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents: nothing in it needs to start at zero, because every call writes
+ * each partial it later reads.  Calls that can overlap on the GPU (concurrent
+ * streams, or several host threads) race on the array: serialise them.
+ */
+#define PKV_NOALLOC_DECODE_SCRATCH_BYTES ((size_t)32 << 20)
+
+PKV_API pkv_status pkv_paged_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                            const void *v_cache, pkv_cache_desc cache,
+                                            const int32_t *block_table, int max_blocks_per_seq,
+                                            const int32_t *cache_seqlens, int max_seqlen,
+                                            const float *sink, int batch, int num_qo_heads,
+                                            int window_left, float sm_scale,
+                                            int partition_size, float *lse_out,
+                                            int32_t *dev_error, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

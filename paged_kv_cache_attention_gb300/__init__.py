@@ -294,3 +294,41 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
         _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill", st)
     return out
+
+
+def paged_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,
+                         sink=None, window_left: int = -1, sm_scale: Optional[float] = None,
+                         partition_size: int = 512, out=None, lse=None, dev_error=None,
+                         stream=None):
+    """paged_decode without a caller workspace, for callers that cannot
+    allocate device memory at the call site.  The library's fixed device
+    scratch array (PKV_NOALLOC_DECODE_SCRATCH_BYTES, 32 MiB) replaces the
+    workspace; problems that need more are rejected (PkvError
+    PKV_ERR_WORKSPACE).  Calls share the array: do not overlap them on the
+    GPU.  The first call on a device should come before any stream capture.
+    ``out`` (and ``lse``) should be preallocated when the caller must not
+    allocate at all."""
+    torch = _torch()
+    lib = load_library()
+    fn = lib.pkv_paged_decode_noalloc
+    if fn.argtypes is None:
+        P, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, i32, i32, i32, f32, i32, P, P,
+                       P]
+        fn.restype = i32
+    desc = _cache_desc(k_cache, v_cache)
+    _cuda_contig("q", q, k_cache.dtype, 3)
+    _cuda_contig("block_table", block_table, torch.int32, 2)
+    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32, 1)
+    B, Hq, D = q.shape
+    if sink is not None:
+        _cuda_contig("sink", sink, torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    scale = float(sm_scale) if sm_scale is not None else D ** -0.5
+    st = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
+            block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink), B, Hq,
+            int(window_left), scale, int(partition_size), _ptr(lse), _ptr(dev_error),
+            _stream_handle(stream))
+    _check("pkv_paged_decode_noalloc", st)
+    return out
