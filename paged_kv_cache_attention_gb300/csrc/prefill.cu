@@ -301,45 +301,47 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             }
             const int32_t *bt = p.block_table + (int64_t)geo.r * p.max_blocks_per_seq;
             const int oob_row = (int)(p.num_blocks * BS);
+            const int pg0 = geo.kt_lo * NPG;       // first page of the CTA's key range
+            const int npages_kv = (geo.kv_len + BS - 1) / BS;
+            int ids_batch = -1, ids_row = oob_row;  // lane l: pool row of page pg0 + 32*batch + l
             bool alive = true;
             for (int j = 0; j < ntiles && alive; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = (j >> 1) & 1;
                 const int key0 = (geo.kt_lo + j) * kTileN;
-                int row = oob_row;
-                if (lane < NPG) {
-                    const int pos = key0 + lane * BS;
-                    if (pos < geo.kv_len) {
-                        const int blk = bt[pos / BS];
+                const int rel = j * NPG;
+                if ((rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
+                    ids_batch = rel >> 5;
+                    const int pg = pg0 + ids_batch * 32 + lane;
+                    ids_row = oob_row;
+                    if (pg < npages_kv) {
+                        const int blk = bt[pg];
                         if (blk < 0 || blk >= p.num_blocks)
                             flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
                         else
-                            row = blk * BS;
+                            ids_row = blk * BS;
                     }
                 }
+                const int row = __shfl_sync(0xffffffffu, ids_row, ((rel & 31) + min(lane >> 1, NPG - 1)) & 31);
                 // K
                 alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error);
                 if (!alive) break;
                 if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_KFULL + s), Lay::T_BYTES);
                 __syncwarp();
-                {
-                    const int pg = min(lane >> 1, NPG - 1), h = lane & 1;
-                    const int rw = __shfl_sync(0xffffffffu, row, pg);
-                    if (lane < 2 * NPG)
-                        tma_load_3d(sK + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmk,
-                                    bar(Lay::B_KFULL + s), h * 64, geo.g, rw);
+                if (lane < 2 * NPG) {
+                    const int pg = lane >> 1, h = lane & 1;
+                    tma_load_3d(sK + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmk,
+                                bar(Lay::B_KFULL + s), h * 64, geo.g, row);
                 }
                 // V
                 alive = mbar_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error);
                 if (!alive) break;
                 if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_VFULL + s), Lay::T_BYTES);
                 __syncwarp();
-                {
-                    const int pg = min(lane >> 1, NPG - 1), h = lane & 1;
-                    const int rw = __shfl_sync(0xffffffffu, row, pg);
-                    if (lane < 2 * NPG)
-                        tma_load_3d(sV + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmv,
-                                    bar(Lay::B_VFULL + s), h * 64, geo.g, rw);
+                if (lane < 2 * NPG) {
+                    const int pg = lane >> 1, h = lane & 1;
+                    tma_load_3d(sV + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmv,
+                                bar(Lay::B_VFULL + s), h * 64, geo.g, row);
                 }
                 if (j == ntiles - 1 && tail) {
                     // rows at or past kv_len of the last value tile may hold any
@@ -367,35 +369,36 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Order per key tile j:  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): the next
+        // S of a query tile only waits for that tile's own PV (S_x(j+1) is
+        // written where P_x(j) lives), not for the other tile's softmax.
         if (ntiles > 0 && lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
-            bool alive = mbar_wait_bounded(bar(Lay::B_Q), 0, p.dev_error);
+            auto issue_s = [&](int x, int s) {
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * Lay::HALF + (kk & 3) * 32;
+                    const uint64_t a = tc::smem_desc_sw128(sQ + x * Lay::Q_BYTES + koff, 16, 1024);
+                    const uint64_t b = tc::smem_desc_sw128(sK + s * Lay::T_BYTES + koff, 16, 1024);
+                    tc::mma_ss(tmem + s_col(x), a, b, idS, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(bar(Lay::B_SFULL + x));
+            };
+            bool alive = mbar_wait_bounded(bar(Lay::B_Q), 0, p.dev_error) &&
+                         mbar_wait_bounded(bar(Lay::B_KFULL + 0), 0, p.dev_error);
+            if (alive) {
+                tc::fence_after_sync();
+                for (int x = 0; x < kNQ; ++x) issue_s(x, 0);
+                tc::commit(bar(Lay::B_KEMPTY + 0));
+            }
             for (int j = 0; j < ntiles && alive; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = (j >> 1) & 1;
-                alive = mbar_wait_bounded(bar(Lay::B_KFULL + s), ph, p.dev_error);
-                if (!alive) break;
-                tc::fence_after_sync();
-                for (int x = 0; x < kNQ; ++x) {
-                    if (j > 0) {
-                        // P_x(j-1) lives where S_x(j) goes: PV_x(j-1) must be done
-                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + x), (j - 1) & 1, p.dev_error);
-                        if (!alive) break;
-                        tc::fence_after_sync();
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * Lay::HALF + (kk & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(sQ + x * Lay::Q_BYTES + koff, 16, 1024);
-                        const uint64_t b = tc::smem_desc_sw128(sK + s * Lay::T_BYTES + koff, 16, 1024);
-                        tc::mma_ss(tmem + s_col(x), a, b, idS, kk > 0 ? 1u : 0u);
-                    }
-                    tc::commit(bar(Lay::B_SFULL + x));
-                }
-                if (!alive) break;
-                tc::commit(bar(Lay::B_KEMPTY + s));
-                for (int x = 0; x < kNQ; ++x) {
+                const int sn = (j + 1) & 1;
+                const uint32_t phn = ((j + 1) >> 1) & 1;
+                const bool more = j + 1 < ntiles;
+                for (int x = 0; x < kNQ && alive; ++x) {
                     alive = mbar_wait_bounded(bar(Lay::B_PFULL + x), j & 1, p.dev_error);
                     if (!alive) break;
                     tc::fence_after_sync();
@@ -415,6 +418,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                                    (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::commit(bar(Lay::B_ODONE + x));
+                    if (more) {
+                        if (x == 0) {
+                            alive = mbar_wait_bounded(bar(Lay::B_KFULL + sn), phn, p.dev_error);
+                            if (!alive) break;
+                        }
+                        // P_x(j) lives where S_x(j+1) goes: PV_x(j) must be done
+                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + x), j & 1, p.dev_error);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                        issue_s(x, sn);
+                        if (x == kNQ - 1) tc::commit(bar(Lay::B_KEMPTY + sn));
+                    }
                 }
                 if (!alive) break;
                 tc::commit(bar(Lay::B_VEMPTY + s));
@@ -450,24 +465,36 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             // keys this row keeps: [klo, khi] (inclusive), relative to key0
             const int khi = min(qpos, geo.kv_len - 1) - key0;
             const int klo = wl < 0 ? -1 : qpos - wl - key0;
-            // pass 1: row maximum over the tile, 32 columns at a time
-            float mx = kNegInf;
+            // pass 1: row maximum over the tile, 64 columns per TMEM round trip,
+            // eight independent partial maxima
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) {
-                uint32_t r32[32];
-                tc::ld_32x32b_x32(tS + c * 32, r32);
+            for (int i = 0; i < 8; ++i) mx8[i] = kNegInf;
+#pragma unroll
+            for (int cc = 0; cc < kTileN / 64; ++cc) {
+                uint32_t ra[32], rb[32];
+                tc::ld_32x32b_x32(tS + cc * 64, ra);
+                tc::ld_32x32b_x32(tS + cc * 64 + 32, rb);
                 tc::wait_ld();
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(r32[i]));
+                    for (int i = 0; i < 32; ++i) {
+                        mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(ra[i]));
+                        mx8[(i + 4) & 7] = fmaxf(mx8[(i + 4) & 7], __uint_as_float(rb[i]));
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int k = c * 32 + i;
-                        if (k <= khi && k >= klo) mx = fmaxf(mx, __uint_as_float(r32[i]));
+                        const int ka = cc * 64 + i, kb = ka + 32;
+                        if (ka <= khi && ka >= klo)
+                            mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(ra[i]));
+                        if (kb <= khi && kb >= klo)
+                            mx8[(i + 4) & 7] = fmaxf(mx8[(i + 4) & 7], __uint_as_float(rb[i]));
                     }
                 }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_tile = mx * sl2;
             const bool grow = m_tile > m_run + kRescaleThreshold;
             // tcgen05.ld/st are warp-collective: the warp rescales together,
@@ -491,31 +518,32 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             }
             // pass 2: P = 2^(s * scale - m) as bf16, written over S (64 columns)
             const float msub = m_run == kNegInf ? 0.f : m_run;
-            float psum = 0.f;
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c2 = 0; c2 < kTileN / 64; ++c2) {
-                uint32_t pk[32];
+                uint32_t ra[32], rb[32];
+                tc::ld_32x32b_x32(tS + c2 * 64, ra);
+                tc::ld_32x32b_x32(tS + c2 * 64 + 32, rb);
+                tc::wait_ld();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int c = 2 * c2 + h;
-                    uint32_t r32[32];
-                    tc::ld_32x32b_x32(tS + c * 32, r32);
-                    tc::wait_ld();
+                    uint32_t *src = h ? rb : ra;  // packed in place: pair i -> word i
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int k = c * 32 + 2 * i;
-                        float p0 = fast_exp2(fmaf(__uint_as_float(r32[2 * i]), sl2, -msub));
-                        float p1 = fast_exp2(fmaf(__uint_as_float(r32[2 * i + 1]), sl2, -msub));
+                        const int k = c2 * 64 + h * 32 + 2 * i;
+                        float p0 = fast_exp2(fmaf(__uint_as_float(src[2 * i]), sl2, -msub));
+                        float p1 = fast_exp2(fmaf(__uint_as_float(src[2 * i + 1]), sl2, -msub));
                         if (!full) {
                             p0 = (k <= khi && k >= klo) ? p0 : 0.f;
                             p1 = (k + 1 <= khi && k + 1 >= klo) ? p1 : 0.f;
                         }
-                        psum += p0 + p1;
-                        pk[h * 16 + i] = pack_bf16(p0, p1);
+                        ps4[i & 3] += p0 + p1;
+                        src[i] = pack_bf16(p0, p1);
                     }
+                    tc::st_32x32b_x16(tS + c2 * 32 + h * 16, src);
                 }
-                tc::st_32x32b_x32(tS + c2 * 32, pk);
             }
+            const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             l_run += psum;
             tc::wait_st();
             tc::fence_before_sync();
