@@ -57,7 +57,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-configuration decode / prefill lines")
-    ap.add_argument("--profile", choices=["decode", "prefill", "write"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "write"],
+                    default=None,
                     help="run a few launches of one call on a mid-size case (for ncu)")
     return ap.parse_args()
 
@@ -555,15 +556,18 @@ def run_profile(which: str):
     from paged_kv_cache_attention_gb300 import workloads as W
     dev = torch.device("cuda", torch.cuda.current_device())
     pkv.load_library()
-    if which == "decode":
-        c = W.config2_decode()
+    if which in ("decode", "decode_long"):
+        c = W.config2_decode() if which == "decode" else W.config3_long(1)
         q, kc, vc = c.q.to(dev), c.k_cache.to(dev), c.v_cache.to(dev)
         bt, sl = c.block_table.to(dev), c.cache_seqlens.to(dev)
         ws = torch.empty(pkv.paged_decode_workspace_size(c.batch, c.num_qo_heads, q.shape[2],
-                                                         c.max_seqlen), dtype=torch.uint8,
+                                                         c.max_seqlen, c.partition_size,
+                                                         c.window_left), dtype=torch.uint8,
                          device=dev)
-        go = lambda: pkv.paged_decode(q, kc, vc, bt, sl, c.max_seqlen, sm_scale=c.sm_scale,
-                                      workspace=ws)
+        sink = None if c.sink is None else c.sink.to(dev)
+        go = lambda: pkv.paged_decode(q, kc, vc, bt, sl, c.max_seqlen, sink=sink,
+                                      window_left=c.window_left, sm_scale=c.sm_scale,
+                                      partition_size=c.partition_size, workspace=ws)
     elif which == "prefill":
         c = W.config4_prefill()
         q, kc, vc = c.q.to(dev), c.k_cache.to(dev), c.v_cache.to(dev)

@@ -10,10 +10,11 @@
 // sink_attention_reference.py, sink_softmax: the sink is one extra softmax
 // column whose value row is zero).
 //
-// GB300 design (bf16): one CTA per (partition, kv head, sequence), so the G
-// query heads of a kv head share every K/V byte fetched from HBM.  Each of the
-// 4 warps owns every 4th page of the partition and streams it through a
-// private ring of shared-memory stages filled by TMA (one 3-D tiled box per
+// GB300 design (bf16): one CTA per (kv head, partition, sequence), heads
+// fastest in launch order so the CTAs reading one page run side by side; the
+// G query heads of a kv head share every K/V byte fetched from HBM.  Each of
+// the 2 warps owns every other page of the partition and streams it through a
+// private 2-stage ring of shared-memory stages filled by TMA (one 3-D tiled box per
 // 64-dim half of a page, 128-byte swizzle, evict-first L2 policy).  The dot
 // products run on the tensor cores with mma.sync m16n8k16 (bf16 in, fp32
 // accumulate): S = Q K^T with the (zero-padded) query heads as the 16 rows,
@@ -30,7 +31,11 @@ namespace pkv {
 
 namespace {
 
-constexpr int kDecWarps = 4;
+// Small CTAs (2 warps, 2 stages of K+V per warp, ~38 KB of shared memory)
+// let 5-6 CTAs share an SM, so one CTA's start-up latency is covered by the
+// others' streaming; measured on GB300 this beat 4- and 8-warp CTAs and deeper
+// per-warp rings.
+constexpr int kDecWarps = 2;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kMaxGroup = 16;
 constexpr int kMaxPartition = 16384;
@@ -76,8 +81,8 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
 // Combine the per-warp softmax states of one CTA and write the partition's
 // normalised output and log-sum-exp (log2 units).  s_o holds the warps'
 // O accumulators already rescaled to the common maximum.
-__device__ __forceinline__ void write_partition(const DecodeParams &p, int b, int g, int D,
-                                                const float *s_m, const float *s_l,
+__device__ __forceinline__ void write_partition(const DecodeParams &p, int b, int g, int pidx,
+                                                int D, const float *s_m, const float *s_l,
                                                 const float *s_o) {
     const int G = p.group;
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
@@ -92,7 +97,7 @@ __device__ __forceinline__ void write_partition(const DecodeParams &p, int b, in
                 Ls += exp2f(s_m[w * kMaxGroup + h] - M) * s_l[w * kMaxGroup + h];
         }
         const int hq = g * G + h;
-        const int64_t idx = ((int64_t)b * p.num_qo_heads + hq) * p.num_parts + blockIdx.x;
+        const int64_t idx = ((int64_t)b * p.num_qo_heads + hq) * p.num_parts + pidx;
         p.part_o[idx * D + d] = Ls > 0.f ? s_o[h * D + d] / Ls : 0.f;
         if (d == 0) p.part_lse[idx] = Ls > 0.f ? M + log2f(Ls) : kNegInf;
     }
@@ -132,12 +137,14 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
     float *s_m = reinterpret_cast<float *>(smem + C::M_OFF);
     float *s_l = reinterpret_cast<float *>(smem + C::L_OFF);
 
-    const int b = blockIdx.z, g = blockIdx.y;
+    // grid: x = kv head (fastest, so the heads reading one page run together),
+    // y = partition index, z = sequence
+    const int b = blockIdx.z, g = blockIdx.x, pidx = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = clipped_seqlen(p, b, BS, blockIdx.x == 0 && g == 0 && threadIdx.x == 0);
+    const int L = clipped_seqlen(p, b, BS, pidx == 0 && g == 0 && threadIdx.x == 0);
     const int start = window_start(L, p.window_left);
     const int P = p.partition_size;
-    const int part = start / P + blockIdx.x;
+    const int part = start / P + pidx;
     const int tok_lo = max(part * P, start);
     const int tok_hi = min((part + 1) * P, L);
     if (tok_lo >= tok_hi) return;  // this partition holds no attended key
@@ -390,7 +397,7 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
         }
     }
     __syncthreads();
-    write_partition(p, b, g, D, s_m, s_l, s_o);
+    write_partition(p, b, g, pidx, D, s_m, s_l, s_o);
 }
 
 // ---------------------------------------------------------------------------
@@ -403,12 +410,12 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
     __shared__ float s_m[kDecWarps * kMaxGroup], s_l[kDecWarps * kMaxGroup];
     __shared__ float s_o[kMaxGroup * D];
 
-    const int b = blockIdx.z, g = blockIdx.y;
+    const int b = blockIdx.z, g = blockIdx.x, pidx = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = clipped_seqlen(p, b, block_size, blockIdx.x == 0 && g == 0 && threadIdx.x == 0);
+    const int L = clipped_seqlen(p, b, block_size, pidx == 0 && g == 0 && threadIdx.x == 0);
     const int start = window_start(L, p.window_left);
     const int P = p.partition_size;
-    const int part = start / P + blockIdx.x;
+    const int part = start / P + pidx;
     const int tok_lo = max(part * P, start);
     const int tok_hi = min((part + 1) * P, L);
     if (tok_lo >= tok_hi) return;
@@ -487,7 +494,7 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
         }
     }
     __syncthreads();
-    write_partition(p, b, g, D, s_m, s_l, s_o);
+    write_partition(p, b, g, pidx, D, s_m, s_l, s_o);
 }
 
 // ---------------------------------------------------------------------------
@@ -569,7 +576,7 @@ decode_merge_kernel(const DecodeParams p, int D, int block_size) {
 
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), bytes);
 }
 
 template <int D, int BS, int NHT, int NST>
@@ -579,7 +586,7 @@ cudaError_t launch_tc(const DecodeParams &p, const CUtensorMap *tk, const CUtens
     auto kern = decode_bf16_tc_kernel<D, BS, NHT, NST>;
     cudaError_t e = set_smem(kern, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_parts, p.num_kv_heads, p.batch);
+    dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
     kern<<<grid, kDecThreads, C::SMEM, stream>>>(p, *tk, *tv);
     return cudaGetLastError();
 }
@@ -587,7 +594,7 @@ cudaError_t launch_tc(const DecodeParams &p, const CUtensorMap *tk, const CUtens
 template <int D, int BS>
 cudaError_t launch_tc_g(const DecodeParams &p, const CUtensorMap *tk, const CUtensorMap *tv,
                         cudaStream_t stream) {
-    constexpr int NST = (D * BS >= 128 * 16) ? 2 : 4;
+    constexpr int NST = 2;
     if (p.group <= 8) return launch_tc<D, BS, 1, NST>(p, tk, tv, stream);
     return launch_tc<D, BS, 2, NST>(p, tk, tv, stream);
 }
@@ -601,7 +608,7 @@ cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
     cudaError_t e = cudaSuccess;
     if (p.group > kMaxGroup || p.partition_size > kMaxPartition) return cudaErrorNotSupported;
     if (cache.dtype == PKV_F32) {
-        dim3 grid(p.num_parts, p.num_kv_heads, p.batch);
+        dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
         if (D == 64)
             decode_f32_kernel<64><<<grid, kDecThreads, 0, stream>>>(p, BS);
         else if (D == 128)

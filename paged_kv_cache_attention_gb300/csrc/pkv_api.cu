@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "pkv_internal.h"
 
@@ -128,6 +129,25 @@ int device_sm_count() {
     return sms;
 }
 
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes) {
+    struct Entry {
+        const void *kernel;
+        int device;
+        int bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &x : done)
+        if (x.kernel == kernel && x.device == dev && x.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.push_back({kernel, dev, bytes});
+    return e;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -202,6 +222,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
         !aligned(block_table, 4) || !aligned(cache_seqlens, 4))
         return PKV_ERR_INVALID_ARG;
     const int np = decode_num_parts(max_seqlen, P, window_left);
+    if (np > 65535) return PKV_ERR_UNSUPPORTED;  // grid.y limit
     const DecodeLayout lay = decode_layout(batch, num_qo_heads, cache.head_dim, np);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.total)
         return PKV_ERR_WORKSPACE;

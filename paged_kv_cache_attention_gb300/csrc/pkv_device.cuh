@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 
 namespace pkv {
 

@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 
 namespace pkv {
 
@@ -69,5 +69,9 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache,
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `kernel` on the
+// current device, done once per (kernel, device, size) and remembered.
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
 
 }  // namespace pkv

@@ -603,7 +603,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
 
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), bytes);
 }
 
 }  // namespace
