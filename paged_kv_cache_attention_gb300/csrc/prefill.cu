@@ -476,25 +476,24 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 tc::ld_32x32b_x32(tS + cc * 64, ra);
                 tc::ld_32x32b_x32(tS + cc * 64 + 32, rb);
                 tc::wait_ld();
-                if (full) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(ra[i]));
-                        mx8[(i + 4) & 7] = fmaxf(mx8[(i + 4) & 7], __uint_as_float(rb[i]));
-                    }
-                } else {
+                if (!full) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int ka = cc * 64 + i, kb = ka + 32;
-                        if (ka <= khi && ka >= klo)
-                            mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(ra[i]));
-                        if (kb <= khi && kb >= klo)
-                            mx8[(i + 4) & 7] = fmaxf(mx8[(i + 4) & 7], __uint_as_float(rb[i]));
+                        if (!(ka <= khi && ka >= klo)) ra[i] = __float_as_uint(kNegInf);
+                        if (!(kb <= khi && kb >= klo)) rb[i] = __float_as_uint(kNegInf);
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    mx8[i & 3] = fmax3(mx8[i & 3], __uint_as_float(ra[2 * i]),
+                                       __uint_as_float(ra[2 * i + 1]));
+                    mx8[4 + (i & 3)] = fmax3(mx8[4 + (i & 3)], __uint_as_float(rb[2 * i]),
+                                             __uint_as_float(rb[2 * i + 1]));
+                }
             }
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                                   fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7])));
             const float m_tile = mx * sl2;
             const bool grow = m_tile > m_run + kRescaleThreshold;
             // tcgen05.ld/st are warp-collective: the warp rescales together,
@@ -518,7 +517,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             }
             // pass 2: P = 2^(s * scale - m) as bf16, written over S (64 columns)
             const float msub = m_run == kNegInf ? 0.f : m_run;
-            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-msub, -msub);
+            uint64_t ps2[2] = {0ull, 0ull};
 #pragma unroll
             for (int c2 = 0; c2 < kTileN / 64; ++c2) {
                 uint32_t ra[32], rb[32];
@@ -531,19 +531,26 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int k = c2 * 64 + h * 32 + 2 * i;
-                        float p0 = fast_exp2(fmaf(__uint_as_float(src[2 * i]), sl2, -msub));
-                        float p1 = fast_exp2(fmaf(__uint_as_float(src[2 * i + 1]), sl2, -msub));
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * i]),
+                                                 __uint_as_float(src[2 * i + 1])),
+                                         scale2, neg2),
+                                  t0, t1);
+                        float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
                         if (!full) {
                             p0 = (k <= khi && k >= klo) ? p0 : 0.f;
                             p1 = (k + 1 <= khi && k + 1 >= klo) ? p1 : 0.f;
                         }
-                        ps4[i & 3] += p0 + p1;
+                        ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
                         src[i] = pack_bf16(p0, p1);
                     }
                     tc::st_32x32b_x16(tS + c2 * 32 + h * 16, src);
                 }
             }
-            const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+            float s0, s1, s2, s3;
+            f2_unpack(ps2[0], s0, s1);
+            f2_unpack(ps2[1], s2, s3);
+            const float psum = (s0 + s1) + (s2 + s3);
             l_run += psum;
             tc::wait_st();
             tc::fence_before_sync();
