@@ -62,8 +62,14 @@ struct PfLayout {
     static constexpr int B_ODONE = B_PFULL + kNQ;
     static constexpr int NBARS = B_ODONE + kNQ;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
-    static constexpr int SMEM = 1024 + OFF_TMEM + 16;
-    static constexpr int THREADS = 64 + kNQ * 128;
+    // row-max exchange between the two warps sharing a row ([2][kNQ][128][2]
+    // floats, double-buffered by tile parity) and the row-sum exchange
+    // ([kNQ][128][2])
+    static constexpr int OFF_XMAX = OFF_TMEM + 16;
+    static constexpr int OFF_XL = OFF_XMAX + 2 * kNQ * 128 * 2 * 4;
+    static constexpr int SMEM = 1024 + OFF_XL + kNQ * 128 * 2 * 4;
+    static constexpr int SOFT_WARPS = 8;  // per query tile: 2 per TMEM lane quarter
+    static constexpr int THREADS = 64 + kNQ * SOFT_WARPS * 32;
     static constexpr int TMEM_COLS = 512;  // O_0, O_1, S_0, S_1: 128 columns each
 };
 
@@ -271,7 +277,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lay::NBARS; ++i)
-            mbar_init(bar(i), (i >= Lay::B_PFULL && i < Lay::B_PFULL + kNQ) ? 128u : 1u);
+            mbar_init(bar(i), (i >= Lay::B_PFULL && i < Lay::B_PFULL + kNQ)
+                                  ? (uint32_t)(Lay::SOFT_WARPS * 32)
+                                  : 1u);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -437,8 +445,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int x = (warp - 2) >> 2;
+        // Eight warps per query tile.  A warp may only touch the TMEM lane
+        // quarter (warp % 4), so each quarter has two warps, and they split
+        // every row's 128 key columns: warp half hc owns columns
+        // [64 hc, 64 hc + 64) of S, [32 hc, 32 hc + 32) of the packed P and
+        // [64 hc, 64 hc + 64) of O.  The two halves of a row exchange their
+        // partial maxima (and, at the end, row sums) through shared memory
+        // under a 64-thread named barrier.
+        const int w = warp - 2;
+        const int x = w / Lay::SOFT_WARPS;
         const int quarter = warp & 3;
+        const int hc = (w % Lay::SOFT_WARPS) >> 2;
         const int row = quarter * 32 + lane;
         const int tok_local = row / G;
         const int h_local = row - tok_local * G;
@@ -447,8 +464,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         const int qpos = geo.kv_len - geo.q_len + tok;
         const int head = geo.g * G + h_local;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + s_col(x);
-        const uint32_t tO = tmem + lane_off + o_col(x);
+        const uint32_t tS = tmem + lane_off + s_col(x) + hc * 64;
+        const uint32_t tP = tmem + lane_off + s_col(x) + hc * 32;
+        const uint32_t tO = tmem + lane_off + o_col(x) + hc * 64;
+        const uint32_t pair_bar = 1 + x * 4 + quarter;
+        float *xmax = reinterpret_cast<float *>(smem + Lay::OFF_XMAX);
+        float *xl = reinterpret_cast<float *>(smem + Lay::OFF_XL);
         const float sl2 = p.scale_log2;
         const int wl = p.window_left;
 
@@ -459,41 +480,36 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                                mbar_wait_bounded(bar(Lay::B_SFULL + x), j & 1, p.dev_error));
             if (!alive) break;
             tc::fence_after_sync();
-            const int key0 = (geo.kt_lo + j) * kTileN;
-            const bool full = (key0 + kTileN - 1 <= qpos) && (key0 + kTileN <= geo.kv_len) &&
+            const int key0 = (geo.kt_lo + j) * kTileN + hc * 64;  // first key of this half
+            const bool full = (key0 + 63 <= qpos) && (key0 + 64 <= geo.kv_len) &&
                               (wl < 0 || key0 >= qpos - wl);
             // keys this row keeps: [klo, khi] (inclusive), relative to key0
             const int khi = min(qpos, geo.kv_len - 1) - key0;
             const int klo = wl < 0 ? -1 : qpos - wl - key0;
-            // pass 1: row maximum over the tile, 64 columns per TMEM round trip,
-            // eight independent partial maxima
-            float mx8[8];
+            uint32_t ra[32], rb[32];
+            tc::ld_32x32b_x32(tS, ra);
+            tc::ld_32x32b_x32(tS + 32, rb);
+            tc::wait_ld();
+            if (!full) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = kNegInf;
-#pragma unroll
-            for (int cc = 0; cc < kTileN / 64; ++cc) {
-                uint32_t ra[32], rb[32];
-                tc::ld_32x32b_x32(tS + cc * 64, ra);
-                tc::ld_32x32b_x32(tS + cc * 64 + 32, rb);
-                tc::wait_ld();
-                if (!full) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int ka = cc * 64 + i, kb = ka + 32;
-                        if (!(ka <= khi && ka >= klo)) ra[i] = __float_as_uint(kNegInf);
-                        if (!(kb <= khi && kb >= klo)) rb[i] = __float_as_uint(kNegInf);
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    mx8[i & 3] = fmax3(mx8[i & 3], __uint_as_float(ra[2 * i]),
-                                       __uint_as_float(ra[2 * i + 1]));
-                    mx8[4 + (i & 3)] = fmax3(mx8[4 + (i & 3)], __uint_as_float(rb[2 * i]),
-                                             __uint_as_float(rb[2 * i + 1]));
+                for (int i = 0; i < 32; ++i) {
+                    if (!(i <= khi && i >= klo)) ra[i] = __float_as_uint(kNegInf);
+                    if (!(i + 32 <= khi && i + 32 >= klo)) rb[i] = __float_as_uint(kNegInf);
                 }
             }
-            const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
-                                   fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7])));
+            float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                mx4[i & 1] = fmax3(mx4[i & 1], __uint_as_float(ra[2 * i]),
+                                   __uint_as_float(ra[2 * i + 1]));
+                mx4[2 + (i & 1)] = fmax3(mx4[2 + (i & 1)], __uint_as_float(rb[2 * i]),
+                                         __uint_as_float(rb[2 * i + 1]));
+            }
+            const float mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
+            float *slot = xmax + (((j & 1) * kNQ + x) * 128 + row) * 2;
+            slot[hc] = mine;
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            const float mx = fmaxf(mine, slot[hc ^ 1]);
             const float m_tile = mx * sl2;
             const bool grow = m_tile > m_run + kRescaleThreshold;
             // tcgen05.ld/st are warp-collective: the warp rescales together,
@@ -503,79 +519,72 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 l_run *= alpha;
                 if (j > 0) {
 #pragma unroll
-                    for (int c = 0; c < kHeadDim / 32; ++c) {
-                        uint32_t r32[32];
-                        tc::ld_32x32b_x32(tO + c * 32, r32);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r16[16];
+                        tc::ld_32x32b_x16(tO + c * 16, r16);
                         tc::wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r32[i] = __float_as_uint(__uint_as_float(r32[i]) * alpha);
-                        tc::st_32x32b_x32(tO + c * 32, r32);
+                        for (int i = 0; i < 16; ++i)
+                            r16[i] = __float_as_uint(__uint_as_float(r16[i]) * alpha);
+                        tc::st_32x32b_x16(tO + c * 16, r16);
                     }
                 }
                 if (grow) m_run = m_tile;
             }
-            // pass 2: P = 2^(s * scale - m) as bf16, written over S (64 columns)
+            // P = 2^(s * scale - m) as bf16 (masked keys hold -inf: 2^-inf = 0)
             const float msub = m_run == kNegInf ? 0.f : m_run;
             const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-msub, -msub);
             uint64_t ps2[2] = {0ull, 0ull};
 #pragma unroll
-            for (int c2 = 0; c2 < kTileN / 64; ++c2) {
-                uint32_t ra[32], rb[32];
-                tc::ld_32x32b_x32(tS + c2 * 64, ra);
-                tc::ld_32x32b_x32(tS + c2 * 64 + 32, rb);
-                tc::wait_ld();
+            for (int h = 0; h < 2; ++h) {
+                uint32_t *src = h ? rb : ra;  // packed in place: pair i -> word i
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t *src = h ? rb : ra;  // packed in place: pair i -> word i
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int k = c2 * 64 + h * 32 + 2 * i;
-                        float t0, t1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * i]),
-                                                 __uint_as_float(src[2 * i + 1])),
-                                         scale2, neg2),
-                                  t0, t1);
-                        float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-                        if (!full) {
-                            p0 = (k <= khi && k >= klo) ? p0 : 0.f;
-                            p1 = (k + 1 <= khi && k + 1 >= klo) ? p1 : 0.f;
-                        }
-                        ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
-                        src[i] = pack_bf16(p0, p1);
-                    }
-                    tc::st_32x32b_x16(tS + c2 * 32 + h * 16, src);
+                for (int i = 0; i < 16; ++i) {
+                    float t0, t1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * i]),
+                                             __uint_as_float(src[2 * i + 1])),
+                                     scale2, neg2),
+                              t0, t1);
+                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                    ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
+                    src[i] = pack_bf16(p0, p1);
                 }
+                tc::st_32x32b_x16(tP + h * 16, src);
             }
             float s0, s1, s2, s3;
             f2_unpack(ps2[0], s0, s1);
             f2_unpack(ps2[1], s2, s3);
-            const float psum = (s0 + s1) + (s2 + s3);
-            l_run += psum;
+            l_run += (s0 + s1) + (s2 + s3);
             tc::wait_st();
             tc::fence_before_sync();
             mbar_arrive(bar(Lay::B_PFULL + x));
         }
-        // epilogue: normalise (sink in the denominator) and store
+        // epilogue: combine the two halves' sums, normalise (sink in the
+        // denominator) and store this warp's 64 output columns
         bool have_o = ntiles > 0 && alive;
         if (have_o) {
             have_o = __all_sync(0xffffffffu, mbar_wait_bounded(bar(Lay::B_ODONE + x),
                                                                (ntiles - 1) & 1, p.dev_error));
             tc::fence_after_sync();
         }
+        float *lslot = xl + (x * 128 + row) * 2;
+        lslot[hc] = l_run;
+        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+        const float l_tot = l_run + lslot[hc ^ 1];
         const float sink_l2 = p.sink ? p.sink[head] * kLog2e : kNegInf;
         const float M = fmaxf(m_run, sink_l2);
         float oscale = 0.f, lse = kNegInf;
         if (M != kNegInf) {
             const float f = fast_exp2(m_run - M);
-            const float Z = l_run * f + fast_exp2(sink_l2 - M);
+            const float Z = l_tot * f + fast_exp2(sink_l2 - M);
             oscale = f / Z;
             lse = (M + log2f(Z)) * kLn2;
         }
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) +
-                              ((int64_t)(geo.q_start + tok) * p.num_qo_heads + head) * kHeadDim;
+                              ((int64_t)(geo.q_start + tok) * p.num_qo_heads + head) * kHeadDim +
+                              hc * 64;
 #pragma unroll
-        for (int c = 0; c < kHeadDim / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
             uint32_t r32[32];
             if (have_o) {  // warp-uniform: every lane takes part in the load
                 tc::ld_32x32b_x32(tO + c * 32, r32);
@@ -597,7 +606,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 }
             }
         }
-        if (row_valid && p.lse_out)
+        if (row_valid && hc == 0 && p.lse_out)
             p.lse_out[(int64_t)(geo.q_start + tok) * p.num_qo_heads + head] = lse;
     }
     tc::fence_before_sync();
