@@ -511,7 +511,7 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
 }
 
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float *scratch) {
 #pragma unroll
@@ -554,15 +554,54 @@ decode_merge_kernel(const DecodeParams p, int D, int block_size) {
     sum = block_reduce(sum, false, scratch);
     const float lam = sum + (M == kNegInf ? 0.f : exp2f(sink_l2 - M));
     __syncthreads();
+    // Weighted sum over the partitions: thread (r, c) accumulates a 4-wide
+    // column slice c of partition rows r, r + R, r + 2R, ... (coalesced 16-byte
+    // loads, R partition rows in flight per pass); the R partial rows are
+    // then added in shared memory.
     OutT *out = static_cast<OutT *>(p.out) + ((int64_t)b * p.num_qo_heads + h) * D;
     const float *po = p.part_o + base * D;
-    for (int d = threadIdx.x; d < D; d += kMergeThreads) {
-        float acc = 0.f;
-        for (int i = 0; i < n; ++i) {
-            const float w = s_w[i];
-            if (w != 0.f) acc = fmaf(w, po[(int64_t)i * D + d], acc);
+    const int cols = D / 4;                  // float4 slices per row
+    const int R = kMergeThreads / cols;      // partition rows per pass
+    const int c = threadIdx.x % cols, r = threadIdx.x / cols;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lam > 0.f) {
+        int i = r;
+        for (; i + R < n; i += 2 * R) {  // two rows in flight per thread
+            const float w0 = s_w[i], w1 = s_w[i + R];
+            const float4 v0 = *reinterpret_cast<const float4 *>(po + (int64_t)i * D + 4 * c);
+            const float4 v1 = *reinterpret_cast<const float4 *>(po + (int64_t)(i + R) * D + 4 * c);
+            if (w0 != 0.f) {
+                acc.x = fmaf(w0, v0.x, acc.x); acc.y = fmaf(w0, v0.y, acc.y);
+                acc.z = fmaf(w0, v0.z, acc.z); acc.w = fmaf(w0, v0.w, acc.w);
+            }
+            if (w1 != 0.f) {
+                acc.x = fmaf(w1, v1.x, acc.x); acc.y = fmaf(w1, v1.y, acc.y);
+                acc.z = fmaf(w1, v1.z, acc.z); acc.w = fmaf(w1, v1.w, acc.w);
+            }
         }
-        out[d] = from_f32<OutT>(lam > 0.f ? acc / lam : 0.f);
+        if (i < n) {
+            const float w0 = s_w[i];
+            const float4 v0 = *reinterpret_cast<const float4 *>(po + (int64_t)i * D + 4 * c);
+            if (w0 != 0.f) {
+                acc.x = fmaf(w0, v0.x, acc.x); acc.y = fmaf(w0, v0.y, acc.y);
+                acc.z = fmaf(w0, v0.z, acc.z); acc.w = fmaf(w0, v0.w, acc.w);
+            }
+        }
+    }
+    __shared__ float4 s_acc[kMergeThreads];
+    s_acc[threadIdx.x] = acc;
+    __syncthreads();
+    if (threadIdx.x < cols) {
+        float4 t = s_acc[threadIdx.x];
+        for (int k = 1; k < R; ++k) {
+            const float4 u = s_acc[k * cols + threadIdx.x];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        const float inv = lam > 0.f ? 1.f / lam : 0.f;
+        out[4 * threadIdx.x + 0] = from_f32<OutT>(t.x * inv);
+        out[4 * threadIdx.x + 1] = from_f32<OutT>(t.y * inv);
+        out[4 * threadIdx.x + 2] = from_f32<OutT>(t.z * inv);
+        out[4 * threadIdx.x + 3] = from_f32<OutT>(t.w * inv);
     }
     if (p.lse_out && threadIdx.x == 0) {
         float lse;
