@@ -57,7 +57,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-configuration decode / prefill lines")
-    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "write"],
+    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_mixed",
+                                          "write"],
                     default=None,
                     help="run a few launches of one call on a mid-size case (for ncu)")
     return ap.parse_args()
@@ -568,11 +569,14 @@ def run_profile(which: str):
         go = lambda: pkv.paged_decode(q, kc, vc, bt, sl, c.max_seqlen, sink=sink,
                                       window_left=c.window_left, sm_scale=c.sm_scale,
                                       partition_size=c.partition_size, workspace=ws)
-    elif which == "prefill":
-        c = W.config4_prefill()
+    elif which in ("prefill", "prefill_mixed"):
+        # prefill_mixed: the prefill launch of the mixed step (4 chunks of 2048
+        # over 4096-token prefixes), on a pool holding only those pages
+        c = W.config4_prefill() if which == "prefill" else W.make_mixed(
+            [], 2048, 4096, 4, 32, 8, 128, 16, torch.bfloat16, seed=W.seed_for(5) + 100).prefill
         q, kc, vc = c.q.to(dev), c.k_cache.to(dev), c.v_cache.to(dev)
         bt, cq, ck = c.block_table.to(dev), c.cu_seq_lens_q.to(dev), c.cu_seq_lens_k.to(dev)
-        sink = c.sink.to(dev)
+        sink = None if c.sink is None else c.sink.to(dev)
         go = lambda: pkv.varlen_prefill(q, kc, vc, bt, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
                                         sink=sink, sm_scale=c.sm_scale)
     else:

@@ -613,6 +613,93 @@ decode_merge_kernel(const DecodeParams p, int D, int block_size) {
     }
 }
 
+// Merge with one warp per (sequence, query head), for batches with many
+// heads and few partitions each (short sequences): no block-wide barriers.
+// Lane l owns the columns [l * D/32, (l+1) * D/32); partition weights are
+// computed 32 at a time, one per lane, and broadcast with shuffles.
+template <typename OutT, int D>
+__global__ void __launch_bounds__(kMergeThreads)
+decode_merge_warp_kernel(const DecodeParams p, int block_size) {
+    constexpr int VEC = D / 32;  // columns per lane: 2 or 4
+    const int lane = threadIdx.x & 31;
+    const int64_t unit = (int64_t)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
+    if (unit >= (int64_t)p.batch * p.num_qo_heads) return;
+    const int b = (int)(unit / p.num_qo_heads), h = (int)(unit % p.num_qo_heads);
+    const int L = clipped_seqlen(p, b, block_size, false);
+    const int start = window_start(L, p.window_left);
+    const int P = p.partition_size;
+    const int n = L > 0 ? (L - 1) / P - start / P + 1 : 0;
+    const int64_t base = ((int64_t)b * p.num_qo_heads + h) * p.num_parts;
+    const float *lp = p.part_lse + base;
+    const float sink_l2 = p.sink ? p.sink[h] * kLog2e : kNegInf;
+
+    float M = sink_l2;
+    for (int i = lane; i < n; i += 32) M = fmaxf(M, lp[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float sum = 0.f;
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+    const float *po = p.part_o + base * D + lane * VEC;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const float w_mine = (M == kNegInf || c0 + lane >= n) ? 0.f : exp2f(lp[c0 + lane] - M);
+        sum += w_mine;
+        const int cnt = min(32, n - c0);
+        for (int k = 0; k < cnt; ++k) {
+            const float w = __shfl_sync(0xffffffffu, w_mine, k);
+            const float *row = po + (int64_t)(c0 + k) * D;
+            if constexpr (VEC == 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(row);
+                acc[0] = fmaf(w, v4.x, acc[0]);
+                acc[1] = fmaf(w, v4.y, acc[1]);
+                acc[2] = fmaf(w, v4.z, acc[2]);
+                acc[3] = fmaf(w, v4.w, acc[3]);
+            } else {
+                const float2 v2 = *reinterpret_cast<const float2 *>(row);
+                acc[0] = fmaf(w, v2.x, acc[0]);
+                acc[1] = fmaf(w, v2.y, acc[1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float lam = sum + (M == kNegInf ? 0.f : exp2f(sink_l2 - M));
+    const float inv = lam > 0.f ? 1.f / lam : 0.f;
+    OutT *out = static_cast<OutT *>(p.out) + ((int64_t)b * p.num_qo_heads + h) * D + lane * VEC;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) out[v] = from_f32<OutT>(acc[v] * inv);
+    if (p.lse_out && lane == 0) {
+        float lse;
+        if (lam > 0.f)
+            lse = (M + log2f(lam)) * kLn2;
+        else
+            lse = p.sink ? p.sink[h] : kNegInf;
+        p.lse_out[(int64_t)b * p.num_qo_heads + h] = lse;
+    }
+}
+
+template <typename OutT>
+cudaError_t launch_merge(const DecodeParams &p, int D, int BS, cudaStream_t stream) {
+    // many heads with few partitions: warp per head; otherwise CTA per head
+    const int64_t units = (int64_t)p.batch * p.num_qo_heads;
+    if (p.num_parts <= 64 && units >= 8LL * device_sm_count()) {
+        const unsigned blocks = (unsigned)((units + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
+        if (D == 64)
+            decode_merge_warp_kernel<OutT, 64><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
+        else
+            decode_merge_warp_kernel<OutT, 128><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
+        return cudaGetLastError();
+    }
+    const int merge_smem = p.num_parts * (int)sizeof(float);
+    auto k = decode_merge_kernel<OutT>;
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(k), merge_smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid2(p.num_qo_heads, p.batch);
+    k<<<grid2, kMergeThreads, merge_smem, stream>>>(p, D, BS);
+    return cudaGetLastError();
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
     return ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), bytes);
@@ -668,18 +755,8 @@ cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
             return cudaErrorNotSupported;
     }
     if (e != cudaSuccess) return e;
-    const int merge_smem = p.num_parts * (int)sizeof(float);
-    dim3 grid2(p.num_qo_heads, p.batch);
-    if (cache.dtype == PKV_F32) {
-        auto k = decode_merge_kernel<float>;
-        if ((e = set_smem(k, merge_smem)) != cudaSuccess) return e;
-        k<<<grid2, kMergeThreads, merge_smem, stream>>>(p, D, BS);
-    } else {
-        auto k = decode_merge_kernel<__nv_bfloat16>;
-        if ((e = set_smem(k, merge_smem)) != cudaSuccess) return e;
-        k<<<grid2, kMergeThreads, merge_smem, stream>>>(p, D, BS);
-    }
-    return cudaGetLastError();
+    if (cache.dtype == PKV_F32) return launch_merge<float>(p, D, BS, stream);
+    return launch_merge<__nv_bfloat16>(p, D, BS, stream);
 }
 
 }  // namespace pkv

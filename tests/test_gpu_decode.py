@@ -88,6 +88,23 @@ def test_bf16_partition_sizes(part):
     assert max_abs(got, ref) <= TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("D,window,sink", [(128, -1, "randn"), (64, 300, "randn"), (128, 0, "none")])
+def test_many_heads_batch(D, window, sink):
+    """A batch with many (sequence, head) pairs and few partitions each takes
+    the warp-per-head merge; it must agree with the oracle like the
+    CTA-per-head merge, including empty and one-token sequences."""
+    gen = torch.Generator().manual_seed(D + window)
+    lens = torch.randint(0, 3000, (64,), generator=gen).tolist()
+    lens[:4] = [0, 1, 512, 513]
+    case = W.make_decode(lens, 32, 8, D, 16, torch.bfloat16, seed=D * 3 + window, sink=sink,
+                         window_left=window)
+    got, glse = gpu_decode(case, with_lse=True)
+    rows = list(range(0, 64, 3)) + [0, 1, 2, 3]
+    ref, rlse = oracle_decode(case, rows=rows, with_lse=True)
+    assert max_abs(got[rows], ref) <= TOL[torch.bfloat16]
+    assert lse_err(glse[rows], rlse) <= LSE_TOL[torch.bfloat16]
+
+
 def test_partition_size_invariance():
     """Split-KV is exact up to fp32 rounding: 512-token partitions and one
     partition for the whole sequence agree far inside the bf16 bar."""
