@@ -408,7 +408,7 @@ def extra_configs(dev, K, peaks):
     return out
 
 
-def cpu_baseline(case, n_dec_every=8, n_pre_every=8, threads=0):
+def cpu_baseline(case, n_dec_every=2, n_pre_every=2, threads=0):
     """The fp64 oracle, as it stands, on a bounded sample of the mixed step:
     the full cache write, every n-th decode sequence and every n-th prefill
     row.  Returns (tokens/s on the sample, threads, description)."""
@@ -530,13 +530,13 @@ def run_reference(args, dist):
     case = W.config5_mixed()
     K, Wm = args.steps, max(args.warmup, 3)
     for _ in range(Wm):
-        cpu_baseline(case, n_dec_every=64, n_pre_every=512)
+        cpu_baseline(case, n_dec_every=64, n_pre_every=64)
     t0 = time.perf_counter()
     toks = 0
     desc = cores = None
     for _ in range(K):
-        _, cores, desc, dt = cpu_baseline(case, n_dec_every=64, n_pre_every=512)
-        toks += len(range(0, case.decode.batch, 64)) + len(range(0, case.prefill.total_q, 512))
+        _, cores, desc, dt = cpu_baseline(case, n_dec_every=64, n_pre_every=64)
+        toks += len(range(0, case.decode.batch, 64)) + len(range(0, case.prefill.total_q, 64))
     secs = time.perf_counter() - t0
     value = toks / secs
     return {
