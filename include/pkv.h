@@ -13,19 +13,25 @@
  *                          (transformers docs "paged_attention", decode path;
  *                          vLLM attention.py, single_query_cached_kv_attention
  *                          with 512-token split-KV partitions);
- *   pkv_varlen_prefill     causal varlen / chunk prefill: request r has
- *                          q_len = cu_seq_lens_q[r+1]-cu_seq_lens_q[r] queries
- *                          over kv_len = cu_seq_lens_k[r+1]-cu_seq_lens_k[r]
- *                          keys read from the paged pools (transformers docs
- *                          "paged_attention", varlen path; FlashInfer
- *                          sink_attention_reference.py, varlen mode).
+ *   pkv_varlen_prefill     varlen / chunk prefill, causal or not: request r
+ *                          has q_len = cu_seq_lens_q[r+1]-cu_seq_lens_q[r]
+ *                          queries over kv_len = cu_seq_lens_k[r+1]-
+ *                          cu_seq_lens_k[r] keys read from the paged pools
+ *                          (transformers docs "paged_attention", varlen path;
+ *                          FlashInfer sink_attention_reference.py, varlen
+ *                          mode);
+ *   pkv_varlen_prefill_contiguous  the same attention with request r's keys in
+ *                          rows cu_seq_lens_k[r] .. cu_seq_lens_k[r+1]-1 of
+ *                          contiguous [total_k, num_kv_heads, head_dim] K and
+ *                          V arrays (the docs' varlen path before the keys are
+ *                          paged).
  *
  * What the attention computes (FlashInfer sink_attention_reference.py,
  * sink_softmax and sink_attention_unified): for request r, query row i and
  * query head h, with G = num_qo_heads / num_kv_heads and kv head g = h / G:
  *   qpos  = kv_len - q_len + i               (decode: kv_len - 1)
- *   keep key j iff j < kv_len, j <= qpos, and (window_left < 0 or
- *                  j >= qpos - window_left)
+ *   keep key j iff j < kv_len, j <= qpos (causal only), and
+ *                  (window_left < 0 or j >= qpos - window_left)
  *   s_j   = sm_scale * <q[i,h,:], k[j,g,:]>  (fp32)
  *   o     = sum_j exp(s_j) v[j,g,:] / (sum_j exp(s_j) + exp(sink[h]))
  *   lse   = log(sum_j exp(s_j) + exp(sink[h]))           (natural log)
@@ -161,18 +167,22 @@ PKV_API size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, in
                                          int total_q, int max_seqlen_q);
 
 /*
- * varlen_prefill: causal attention of every query row over its request's
- * paged keys.
+ * varlen_prefill: attention of every query row over its request's paged keys.
  *   out, q         [total_q, num_qo_heads, head_dim] bf16, contiguous
  *   cu_seq_lens_q  [batch+1] int32 (device), exclusive prefix sums of q_len
  *   cu_seq_lens_k  [batch+1] int32 (device), exclusive prefix sums of kv_len;
  *                  only the differences are used -- keys come from the pages
  *   max_seqlen_q/k host ints >= every q_len / kv_len
  *   total_q        host int == cu_seq_lens_q[batch]
- *   causal         must be 1 in this version (mask aligned to the end of kv)
+ *   causal         1: key j <= qpos (the mask aligned to the end of kv);
+ *                  0: no upper bound, window_left >= 0 still drops keys
+ *                  before qpos - window_left (FlashInfer
+ *                  sink_attention_reference.py, non-causal varlen mask)
  *   sink, window_left, sm_scale, lse_out ([total_q, num_qo_heads]) as in
- *   paged_decode.  Rows whose position is negative (q_len > kv_len) keep no
- *   key.
+ *   paged_decode.  Causal rows whose position is negative (q_len > kv_len)
+ *   keep no key.  Supported: bf16 pools, head_dim 128, block_size 16 or 32,
+ *   G = num_qo_heads / num_kv_heads a power of two <= 16; anything else
+ *   returns PKV_ERR_UNSUPPORTED.
  */
 PKV_API pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
                               const void *v_cache, pkv_cache_desc cache,
@@ -182,6 +192,31 @@ PKV_API pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_ca
                               const float *sink, int batch, int num_qo_heads, int causal,
                               int window_left, float sm_scale, float *lse_out, void *workspace,
                               size_t workspace_bytes, int32_t *dev_error, void *stream);
+
+/*
+ * varlen_prefill_contiguous: varlen_prefill with the keys and values of all
+ * requests packed, not paged.
+ *   k, v           [total_k, num_kv_heads, head_dim] (dtype: PKV_BF16),
+ *                  contiguous, 16-byte aligned device memory owned by the
+ *                  caller; may be NULL when total_k == 0
+ *   total_k        host int, rows of k and v (normally cu_seq_lens_k[batch])
+ *   cu_seq_lens_k  [batch+1] int32 (device): request r's keys are rows
+ *                  cu_seq_lens_k[r] .. cu_seq_lens_k[r+1]-1
+ * Every other argument as in pkv_varlen_prefill, and the same workspace
+ * (pkv_varlen_prefill_workspace_size).  A request whose rows run past total_k
+ * is clipped to the rows that exist and PKV_DEVERR_SEQLEN is raised in
+ * dev_error; nothing outside k and v is read.
+ */
+PKV_API pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k,
+                                                 const void *v, int total_k, int num_kv_heads,
+                                                 int head_dim, int dtype,
+                                                 const int32_t *cu_seq_lens_q,
+                                                 const int32_t *cu_seq_lens_k, int max_seqlen_q,
+                                                 int max_seqlen_k, int total_q, const float *sink,
+                                                 int batch, int num_qo_heads, int causal,
+                                                 int window_left, float sm_scale, float *lse_out,
+                                                 void *workspace, size_t workspace_bytes,
+                                                 int32_t *dev_error, void *stream);
 
 /*
  * paged_decode_noalloc: paged_decode for callers that cannot allocate device

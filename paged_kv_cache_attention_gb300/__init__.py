@@ -30,7 +30,8 @@ from ._build import LIB_PATH, build as _build_lib
 
 __all__ = [
     "build", "load_library", "PkvError", "reshape_and_cache", "paged_decode",
-    "varlen_prefill", "paged_decode_workspace_size", "varlen_prefill_workspace_size",
+    "varlen_prefill", "varlen_prefill_contiguous", "paged_decode_noalloc",
+    "paged_decode_workspace_size", "varlen_prefill_workspace_size",
     "DEVERR_BLOCK_ID", "DEVERR_SLOT", "DEVERR_SEQLEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
 ]
 
@@ -45,6 +46,7 @@ EXPORTED_SYMBOLS = (
     "pkv_status_string", "pkv_version", "pkv_reshape_and_cache",
     "pkv_paged_decode_workspace_size", "pkv_paged_decode",
     "pkv_varlen_prefill_workspace_size", "pkv_varlen_prefill",
+    "pkv_varlen_prefill_contiguous",
 )
 
 
@@ -100,6 +102,10 @@ def load_library(path: Optional[str] = None):
         lib.pkv_varlen_prefill.argtypes = [P, P, P, P, CacheDesc, P, i32, P, P, i32, i32, i32, P,
                                            i32, i32, i32, i32, f32, P, P, sz, P, P]
         lib.pkv_varlen_prefill.restype = i32
+        lib.pkv_varlen_prefill_contiguous.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, i32,
+                                                      i32, i32, P, i32, i32, i32, i32, f32, P,
+                                                      P, sz, P, P]
+        lib.pkv_varlen_prefill_contiguous.restype = i32
         _lib = lib
         return lib
 
@@ -256,11 +262,12 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
                    max_seqlen_q: int, max_seqlen_k: int, sink=None, causal: bool = True,
                    window_left: int = -1, sm_scale: Optional[float] = None, out=None, lse=None,
                    workspace=None, dev_error=None, stream=None):
-    """Causal varlen / chunk prefill over the paged pools; returns out [total_q, Hq, D].
+    """Varlen / chunk prefill over the paged pools; returns out [total_q, Hq, D].
 
     q: [total_q, Hq, D] bf16; cu_seq_lens_q / cu_seq_lens_k: [B+1] int32;
     max_seqlen_q / max_seqlen_k: host ints; request r's queries sit at the end
-    of its kv_len keys.
+    of its kv_len keys.  causal=False drops the j <= position bound (a window
+    still bounds keys from below).
     """
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
@@ -293,6 +300,49 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
         int(window_left), scale, _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
         _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill", st)
+    return out
+
+
+def varlen_prefill_contiguous(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_seqlen_q: int,
+                              max_seqlen_k: int, sink=None, causal: bool = True,
+                              window_left: int = -1, sm_scale: Optional[float] = None, out=None,
+                              lse=None, workspace=None, dev_error=None, stream=None):
+    """Varlen prefill with contiguous keys: request r's keys and values are
+    rows cu_seq_lens_k[r] .. cu_seq_lens_k[r+1]-1 of k and v ([total_k, Hkv, D]
+    bf16).  Otherwise as varlen_prefill; returns out [total_q, Hq, D]."""
+    torch = _torch()
+    _cuda_contig("q", q, ndim=3)
+    _cuda_contig("k", k, q.dtype, 3)
+    _cuda_contig("v", v, q.dtype, 3)
+    _cuda_contig("cu_seq_lens_q", cu_seq_lens_q, torch.int32, 1)
+    _cuda_contig("cu_seq_lens_k", cu_seq_lens_k, torch.int32, 1)
+    _require(k.shape == v.shape, "k and v must have the same shape")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    _require(Dk == D, "head_dim of q and k differ")
+    B = cu_seq_lens_q.shape[0] - 1
+    _require(cu_seq_lens_k.shape[0] == B + 1, "cu_seq_lens_q/k lengths differ")
+    if sink is not None:
+        _cuda_contig("sink", sink, torch.float32, 1)
+        _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_contig("out", out, q.dtype, 3)
+        _require(out.shape == q.shape, "out must be shaped like q")
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32, 2)
+        _require(tuple(lse.shape) == (total_q, Hq), "lse must be [total_q, Hq]")
+    scale = float(sm_scale) if sm_scale is not None else D ** -0.5
+    need = varlen_prefill_workspace_size(B, Hq, Hkv, total_q, max_seqlen_q)
+    ws = _workspace(need, q.device, workspace)
+    st = load_library().pkv_varlen_prefill_contiguous(
+        _ptr(out), _ptr(q), _ptr(k) if total_k else None, _ptr(v) if total_k else None,
+        int(total_k), Hkv, D, _dtype_code(q.dtype), _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k),
+        int(max_seqlen_q), int(max_seqlen_k), int(total_q), _ptr(sink), B, Hq,
+        int(bool(causal)), int(window_left), scale, _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
+    _check("pkv_varlen_prefill_contiguous", st)
     return out
 
 

@@ -277,18 +277,23 @@ size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, int num_kv
     return prefill_layout(batch, G, num_kv_heads, total_q).total;
 }
 
-pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
-                              const void *v_cache, pkv_cache_desc cache,
-                              const int32_t *block_table, int max_blocks_per_seq,
-                              const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
-                              int max_seqlen_q, int max_seqlen_k, int total_q,
-                              const float *sink, int batch, int num_qo_heads, int causal,
-                              int window_left, float sm_scale, float *lse_out, void *workspace,
-                              size_t workspace_bytes, int32_t *dev_error, void *stream) {
-    pkv_status st = check_cache(cache);
-    if (st != PKV_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// Shared by the paged and the contiguous prefill entry points.  kv_rows: the
+// rows of the K/V views the tensor maps cover; kv_box_rows: rows per box (the
+// page size, or 128 for contiguous rows).
+pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
+                       const pkv_cache_desc &cache, bool contiguous, int64_t kv_rows,
+                       const int32_t *block_table, int max_blocks_per_seq,
+                       const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
+                       int max_seqlen_q, int max_seqlen_k, int total_q, const float *sink,
+                       int batch, int num_qo_heads, int causal, int window_left, float sm_scale,
+                       float *lse_out, void *workspace, size_t workspace_bytes,
+                       int32_t *dev_error, void *stream) {
     if (cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (!causal) return PKV_ERR_UNSUPPORTED;
+    if (cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (batch < 0 || num_qo_heads <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         total_q < 0 || max_blocks_per_seq <= 0 || window_left < -1 || !std::isfinite(sm_scale))
         return PKV_ERR_INVALID_ARG;
@@ -296,10 +301,13 @@ pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
     const int G = num_qo_heads / cache.num_kv_heads;
     if (G > 16 || (G & (G - 1)) != 0) return PKV_ERR_UNSUPPORTED;
     if (batch == 0 || total_q == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_table || !cu_seq_lens_q || !cu_seq_lens_k)
+    if (!out || !q || (kv_rows > 0 && (!k || !v)) || (!contiguous && !block_table) ||
+        !cu_seq_lens_q || !cu_seq_lens_k)
         return PKV_ERR_INVALID_ARG;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    if (!aligned(out, 16) || !aligned(q, 16) ||
+        (kv_rows > 0 && (!aligned(k, 16) || !aligned(v, 16))))
         return PKV_ERR_INVALID_ARG;
+    if (kv_rows >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
     const PrefillLayout lay = prefill_layout(batch, G, cache.num_kv_heads, total_q);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.total)
         return PKV_ERR_WORKSPACE;
@@ -326,22 +334,78 @@ pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
     p.max_seqlen_k = max_seqlen_k;
     p.total_q = total_q;
     p.window_left = window_left;
+    p.causal = causal ? 1 : 0;
+    p.total_k = contiguous ? (int)kv_rows : 0;
     p.rows_per_head = 128 / G;
     p.max_tiles = (int)lay.max_items;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
 
+    // With no contiguous keys at all every request clips to kv_len 0 and no
+    // K/V tile is ever loaded; the K/V maps then cover one row of q only so
+    // that they can be encoded.
+    if (contiguous && kv_rows == 0) {
+        k = v = q;
+        kv_rows = 1;
+    }
     alignas(64) CUtensorMap tq, tk, tv;
-    const int64_t rows = cache.num_blocks * cache.block_size;
+    const int box_rows = contiguous ? 128 : cache.block_size;
+    pkv_status st;
     if ((st = encode_rows_map(&tq, q, cache.head_dim, num_qo_heads, total_q, G, 128 / G)) !=
         PKV_OK)
         return st;
-    if ((st = encode_rows_map(&tk, k_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
-                              cache.block_size)) != PKV_OK)
+    if ((st = encode_rows_map(&tk, k, cache.head_dim, cache.num_kv_heads, kv_rows, 1,
+                              box_rows)) != PKV_OK)
         return st;
-    if ((st = encode_rows_map(&tv, v_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
-                              cache.block_size)) != PKV_OK)
+    if ((st = encode_rows_map(&tv, v, cache.head_dim, cache.num_kv_heads, kv_rows, 1,
+                              box_rows)) != PKV_OK)
         return st;
-    return from_cuda(launch_prefill(p, cache, &tq, &tk, &tv, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_prefill(p, cache, contiguous, &tq, &tk, &tv,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
+                              const void *v_cache, pkv_cache_desc cache,
+                              const int32_t *block_table, int max_blocks_per_seq,
+                              const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
+                              int max_seqlen_q, int max_seqlen_k, int total_q,
+                              const float *sink, int batch, int num_qo_heads, int causal,
+                              int window_left, float sm_scale, float *lse_out, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_error, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    return prefill_run(out, q, k_cache, v_cache, cache, false,
+                       cache.num_blocks * cache.block_size, block_table, max_blocks_per_seq,
+                       cu_seq_lens_q, cu_seq_lens_k, max_seqlen_q, max_seqlen_k, total_q, sink,
+                       batch, num_qo_heads, causal, window_left, sm_scale, lse_out, workspace,
+                       workspace_bytes, dev_error, stream);
+}
+
+pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k, const void *v,
+                                         int total_k, int num_kv_heads, int head_dim, int dtype,
+                                         const int32_t *cu_seq_lens_q,
+                                         const int32_t *cu_seq_lens_k, int max_seqlen_q,
+                                         int max_seqlen_k, int total_q, const float *sink,
+                                         int batch, int num_qo_heads, int causal,
+                                         int window_left, float sm_scale, float *lse_out,
+                                         void *workspace, size_t workspace_bytes,
+                                         int32_t *dev_error, void *stream) {
+    if (total_k < 0 || num_kv_heads <= 0 || head_dim <= 0) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    pkv_cache_desc cache;
+    cache.num_blocks = 1;
+    cache.block_size = 128;
+    cache.num_kv_heads = num_kv_heads;
+    cache.head_dim = head_dim;
+    cache.dtype = dtype;
+    return prefill_run(out, q, k, v, cache, true, total_k,
+                       nullptr, max_seqlen_k / 128 + 2, cu_seq_lens_q, cu_seq_lens_k,
+                       max_seqlen_q, max_seqlen_k, total_q, sink, batch, num_qo_heads, causal,
+                       window_left, sm_scale, lse_out, workspace, workspace_bytes, dev_error,
+                       stream);
 }
 
 }  // extern "C"

@@ -33,7 +33,8 @@ struct DecodeParams {
     float scale_log2;            // sm_scale * log2(e)
 };
 
-// Varlen causal prefill on the paged pools.
+// Varlen prefill on the paged pools, or on contiguous K/V ([total_k, Hkv, D]
+// addressed by cu_k).
 struct PrefillParams {
     const void *q;                 // [total_q, Hq, D]
     void *out;                     // [total_q, Hq, D]
@@ -48,6 +49,8 @@ struct PrefillParams {
     int batch, num_qo_heads, num_kv_heads, group;
     int max_blocks_per_seq, max_seqlen_q, max_seqlen_k, total_q;
     int window_left;
+    int causal;                    // 1: keys j <= query position; 0: no upper bound
+    int total_k;                   // contiguous K/V: rows in the arrays (unused when paged)
     int rows_per_head;             // query tokens per 128-row tile (128 / group)
     int max_tiles;                 // capacity of the work list
     float scale_log2;
@@ -63,7 +66,9 @@ cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
                           const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                           cudaStream_t stream);
 
-cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache,
+// contiguous: K/V are [total_k, Hkv, D] rows addressed by cu_k (the tensor
+// maps use 128-row boxes); otherwise paged pools of cache.block_size rows.
+cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, bool contiguous,
                            const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
                            const CUtensorMap *tmap_v, cudaStream_t stream);
 

@@ -1,12 +1,16 @@
-// prefill.cu -- causal varlen / chunk prefill on the paged pools, on the
-// 5th-generation tensor cores (tcgen05 + TMEM).
+// prefill.cu -- varlen / chunk prefill on the paged pools (or on contiguous
+// K/V rows), on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
 // What it computes: for request r (q_len queries, kv_len keys addressed by
 // cu_seq_lens_q / cu_seq_lens_k, transformers docs "paged_attention", varlen
 // path) query row i sits at position kv_len - q_len + i and attends causally
 // (and within window_left) to its request's keys, read from the pages named by
 // block_table; the per-head sink joins the softmax denominator (FlashInfer
-// sink_attention_reference.py, varlen branch and sink_softmax).
+// sink_attention_reference.py, varlen branch and sink_softmax).  Without the
+// causal bound a row keeps every key at or after position - window_left (the
+// same reference's non-causal varlen mask).  The contiguous form reads request
+// r's keys from rows cu_k[r] .. cu_k[r+1]-1 of [total_k, Hkv, D] arrays, as in
+// the docs' varlen path.
 //
 // GB300 design.  One CTA takes NQ = 2 query tiles of 128 rows of one request
 // and one kv head.  The G query heads of the kv head are packed into the rows
@@ -105,7 +109,7 @@ __device__ __forceinline__ int clip_len(int v, int cap, int32_t *err, bool repor
 }
 
 __device__ __forceinline__ Geo make_geo(const PrefillParams &p, int4 item, int block_size,
-                                        bool report) {
+                                        bool contiguous, bool report) {
     Geo G;
     G.r = item.x;
     G.t0 = item.y;
@@ -115,12 +119,16 @@ __device__ __forceinline__ Geo make_geo(const PrefillParams &p, int4 item, int b
     int cap_k = p.max_seqlen_k;
     const long long cap_blocks = (long long)p.max_blocks_per_seq * block_size;
     if (cap_blocks < cap_k) cap_k = (int)cap_blocks;
+    if (contiguous) {  // request r's key rows must lie inside the arrays
+        const int room = p.total_k - p.cu_k[G.r];
+        if (room < cap_k) cap_k = max(room, 0);
+    }
     G.kv_len = clip_len(p.cu_k[G.r + 1] - p.cu_k[G.r], cap_k, p.dev_error, report);
     const int tokens = kNQ * p.rows_per_head;
     const int t_end = min(G.t0 + tokens, G.q_len);
     const int qpos_min = G.kv_len - G.q_len + G.t0;
     const int qpos_max = G.kv_len - G.q_len + t_end - 1;
-    const int hi = min(G.kv_len, qpos_max + 1);
+    const int hi = p.causal ? min(G.kv_len, qpos_max + 1) : G.kv_len;
     int lo = 0;
     if (p.window_left >= 0) lo = max(0, qpos_min - p.window_left);
     if (hi <= lo || t_end <= G.t0) {
@@ -144,7 +152,7 @@ __device__ __forceinline__ int item_cost(const PrefillParams &p, int q_len, int 
     const int tokens = kNQ * p.rows_per_head;
     const int t_end = min(t0 + tokens, q_len);
     const int qpos_min = kv_len - q_len + t0;
-    const int hi = min(kv_len, kv_len - q_len + t_end);
+    const int hi = p.causal ? min(kv_len, kv_len - q_len + t_end) : kv_len;
     int lo = 0;
     if (p.window_left >= 0) lo = max(0, qpos_min - p.window_left);
     if (hi <= lo) return 0;
@@ -252,7 +260,9 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
 // ---------------------------------------------------------------------------
 // the attention kernel
 // ---------------------------------------------------------------------------
-template <int BS>
+// BS: rows per page of the paged pools; CONTIG: K/V are contiguous rows
+// addressed by cu_k (then BS = 128, one box per 64-dim half per tile).
+template <int BS, bool CONTIG>
 __global__ void __launch_bounds__(PfLayout::THREADS, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -271,7 +281,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Geo geo = make_geo(p, item, BS, threadIdx.x == 0);
+    const Geo geo = make_geo(p, item, BS, CONTIG, threadIdx.x == 0);
     const int G = p.group;
     const int TPR = p.rows_per_head;
 
@@ -318,7 +328,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 const uint32_t ph = (j >> 1) & 1;
                 const int key0 = (geo.kt_lo + j) * kTileN;
                 const int rel = j * NPG;
-                if ((rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
+                if (!CONTIG && (rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
                     ids_batch = rel >> 5;
                     const int pg = pg0 + ids_batch * 32 + lane;
                     ids_row = oob_row;
@@ -330,7 +340,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                             ids_row = blk * BS;
                     }
                 }
-                const int row = __shfl_sync(0xffffffffu, ids_row, ((rel & 31) + min(lane >> 1, NPG - 1)) & 31);
+                int row = __shfl_sync(0xffffffffu, ids_row, ((rel & 31) + min(lane >> 1, NPG - 1)) & 31);
+                if constexpr (CONTIG) row = p.cu_k[geo.r] + key0;  // rows past kv_len are masked
                 // K
                 alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error);
                 if (!alive) break;
@@ -462,6 +473,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         const int tok = geo.t0 + x * TPR + tok_local;
         const bool row_valid = tok < geo.q_len;
         const int qpos = geo.kv_len - geo.q_len + tok;
+        const int cpos = p.causal ? qpos : (1 << 30);  // causal upper bound on keys
         const int head = geo.g * G + h_local;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + s_col(x) + hc * 64;
@@ -481,10 +493,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             if (!alive) break;
             tc::fence_after_sync();
             const int key0 = (geo.kt_lo + j) * kTileN + hc * 64;  // first key of this half
-            const bool full = (key0 + 63 <= qpos) && (key0 + 64 <= geo.kv_len) &&
+            const bool full = (key0 + 63 <= cpos) && (key0 + 64 <= geo.kv_len) &&
                               (wl < 0 || key0 >= qpos - wl);
             // keys this row keeps: [klo, khi] (inclusive), relative to key0
-            const int khi = min(qpos, geo.kv_len - 1) - key0;
+            const int khi = min(cpos, geo.kv_len - 1) - key0;
             const int klo = wl < 0 ? -1 : qpos - wl - key0;
             uint32_t ra[32], rb[32];
             tc::ld_32x32b_x32(tS, ra);
@@ -624,7 +636,7 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache,
+cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, bool contiguous,
                            const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
                            const CUtensorMap *tmap_v, cudaStream_t stream) {
     if (cache.head_dim != kHeadDim || cache.dtype != PKV_BF16) return cudaErrorNotSupported;
@@ -633,18 +645,16 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache,
     if (e != cudaSuccess) return e;
     const int grid = p.max_tiles;
     if (grid <= 0) return cudaSuccess;
-    if (cache.block_size == 16) {
-        auto k = prefill_tc_kernel<16>;
-        if ((e = set_smem(k, PfLayout::SMEM)) != cudaSuccess) return e;
-        k<<<grid, PfLayout::THREADS, PfLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k, *tmap_v);
-    } else if (cache.block_size == 32) {
-        auto k = prefill_tc_kernel<32>;
-        if ((e = set_smem(k, PfLayout::SMEM)) != cudaSuccess) return e;
-        k<<<grid, PfLayout::THREADS, PfLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k, *tmap_v);
-    } else {
-        return cudaErrorNotSupported;
-    }
-    return cudaGetLastError();
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e2 = set_smem(kern, PfLayout::SMEM);
+        if (e2 != cudaSuccess) return e2;
+        kern<<<grid, PfLayout::THREADS, PfLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k, *tmap_v);
+        return cudaGetLastError();
+    };
+    if (contiguous) return go(prefill_tc_kernel<kTileN, true>);
+    if (cache.block_size == 16) return go(prefill_tc_kernel<16, false>);
+    if (cache.block_size == 32) return go(prefill_tc_kernel<32, false>);
+    return cudaErrorNotSupported;
 }
 
 }  // namespace pkv

@@ -62,6 +62,36 @@ def gpu_prefill(case, with_lse=False, err=None):
     return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
 
 
+def contiguous_kv(case, pad_rows=0):
+    """The case's keys and values packed request after request ([total_k, Hkv,
+    D], the layout cu_seq_lens_k addresses), gathered from the pool by plain
+    indexing; pad_rows NaN rows follow the last request."""
+    bs = case.k_cache.shape[1]
+    ks, vs = [], []
+    for r, L in enumerate(case.kv_lens.tolist()):
+        pos = torch.arange(L)
+        pages = case.block_table[r, (pos // bs)].long()
+        ks.append(case.k_cache[pages, pos % bs])
+        vs.append(case.v_cache[pages, pos % bs])
+    tail = torch.full((pad_rows,) + tuple(case.k_cache.shape[2:]), float("nan"),
+                      dtype=case.k_cache.dtype)
+    return torch.cat(ks + [tail]), torch.cat(vs + [tail])
+
+
+def gpu_prefill_contiguous(case, k, v, with_lse=False, err=None):
+    d = dev()
+    lse = torch.empty(case.total_q, case.q.shape[1], dtype=torch.float32, device=d) \
+        if with_lse else None
+    out = pkv.varlen_prefill_contiguous(
+        to_dev(case.q), to_dev(k), to_dev(v), to_dev(case.cu_seq_lens_q),
+        to_dev(case.cu_seq_lens_k), case.max_seqlen_q, case.max_seqlen_k,
+        sink=to_dev(case.sink), causal=case.causal, window_left=case.window_left,
+        sm_scale=case.sm_scale, lse=lse, dev_error=err)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
+
+
 def oracle_prefill(case, rows=None, with_lse=False):
     return oracle.attention(
         W.to_oracle(case.q), W.to_oracle(case.k_cache), W.to_oracle(case.v_cache),

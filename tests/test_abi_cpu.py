@@ -117,7 +117,7 @@ def test_reshape_and_cache_validation():
 
 @nogpu
 @pytest.mark.parametrize("change,expected", [
-    (dict(causal=0), 2),            # non-causal prefill not in this version
+    (dict(window=-2), 1),
     (dict(dtype=0), 2),             # fp32 prefill not in this version
     (dict(hq=24), 2),               # group of 3 (not a power of two)
     (dict(total_q=0), 0),
@@ -125,11 +125,35 @@ def test_reshape_and_cache_validation():
 ])
 def test_prefill_validation(change, expected):
     lib = pkv.load_library()
-    a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30)
+    a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30, window=-1)
     a.update(change)
     st = lib.pkv_varlen_prefill(FAKE, FAKE, FAKE, FAKE, _desc(dtype=a["dtype"]), FAKE, 8, FAKE,
-                                FAKE, 64, 128, a["total_q"], None, 2, a["hq"], a["causal"], -1,
-                                0.1, None, FAKE, a["ws_bytes"], None, None)
+                                FAKE, 64, 128, a["total_q"], None, 2, a["hq"], a["causal"],
+                                a["window"], 0.1, None, FAKE, a["ws_bytes"], None, None)
+    assert st == expected
+
+
+@nogpu
+@pytest.mark.parametrize("change,expected", [
+    (dict(total_k=-1), 1),
+    (dict(hkv=0), 1),
+    (dict(dtype=3), 2),
+    (dict(dtype=0), 2),             # fp32 prefill not in this version
+    (dict(d=64), 2),                # head_dim 128 only
+    (dict(hq=24), 2),               # group of 3 (not a power of two)
+    (dict(hq=12), 1),               # not a multiple of num_kv_heads
+    (dict(k=None), 1),              # keys missing although total_k > 0
+    (dict(k=FAKE + 8), 1),          # not 16-byte aligned
+    (dict(total_q=0), 0),
+    (dict(ws_bytes=16), 3),
+])
+def test_prefill_contiguous_validation(change, expected):
+    lib = pkv.load_library()
+    a = dict(total_k=500, hkv=8, d=128, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30, k=FAKE)
+    a.update(change)
+    st = lib.pkv_varlen_prefill_contiguous(
+        FAKE, FAKE, a["k"], FAKE, a["total_k"], a["hkv"], a["d"], a["dtype"], FAKE, FAKE, 64,
+        128, a["total_q"], None, 2, a["hq"], 1, -1, 0.1, None, FAKE, a["ws_bytes"], None, None)
     assert st == expected
 
 

@@ -12,8 +12,8 @@ import torch
 
 import paged_kv_cache_attention_gb300 as pkv
 from paged_kv_cache_attention_gb300 import workloads as W
-from tests._gpu import (LSE_TOL, TOL, dev, gpu_decode, gpu_prefill, lse_err, max_abs,
-                        oracle_decode, oracle_prefill)
+from tests._gpu import (LSE_TOL, TOL, contiguous_kv, dev, gpu_decode, gpu_prefill,
+                        gpu_prefill_contiguous, lse_err, max_abs, oracle_decode, oracle_prefill)
 
 pytestmark = pytest.mark.gpu
 BF16 = torch.bfloat16
@@ -69,6 +69,106 @@ def test_empty_requests_and_ragged_tails():
     kv_lens = [10, 5, 0, 127, 1000, 129, 0]
     case = W.make_varlen_kv(q_lens, kv_lens, 16, 4, 128, 16, BF16, seed=22, sink="randn")
     _check(case)
+
+
+# ---------------------------------------------------------------------------
+# non-causal varlen (no upper bound on keys; a window still bounds them below)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("sink", ["none", "randn"])
+@pytest.mark.parametrize("window", [-1, 0, 7, 128, 1000])
+def test_non_causal_windows_and_sinks(sink, window):
+    q_lens = [200, 1, 513, 64, 300, 9]
+    kv_lens = [500, 2001, 513, 64, 40, 0]   # q_len > kv_len in request 4
+    case = W.make_varlen_kv(q_lens, kv_lens, 32, 8, 128, 16, BF16, seed=window + 70,
+                            sink=sink, window_left=window, causal=False)
+    _check(case)
+
+
+@pytest.mark.parametrize("G,Hkv,bs", [(1, 4, 32), (4, 4, 16), (16, 1, 16)])
+def test_non_causal_group_sizes(G, Hkv, bs):
+    case = W.make_varlen_kv([1, 33, 129, 250], [1, 300, 129, 1000], G * Hkv, Hkv, 128, bs, BF16,
+                            seed=G * 13 + bs, sink="randn", causal=False)
+    _check(case)
+
+
+def test_non_causal_rows_see_the_same_keys():
+    """Without the causal bound and window every row of a request attends to
+    the same key set: permuting the queries of a request permutes the outputs."""
+    case = W.make_varlen_kv([100], [700], 16, 4, 128, 16, BF16, seed=27, causal=False)
+    a = gpu_prefill(case)
+    perm = torch.randperm(100, generator=torch.Generator().manual_seed(5))
+    case.q = case.q[perm].contiguous()
+    b = gpu_prefill(case)
+    assert np.array_equal(a[perm.numpy()], b)
+
+
+# ---------------------------------------------------------------------------
+# contiguous (unpaged) keys and values addressed by cu_seq_lens_k
+# ---------------------------------------------------------------------------
+
+def _check_contig(case, pad_rows=0, rows=None):
+    k, v = contiguous_kv(case, pad_rows)
+    got, glse = gpu_prefill_contiguous(case, k, v, with_lse=True)
+    ref, rlse = oracle_prefill(case, rows=rows, with_lse=True)
+    if rows is not None:
+        got, glse = got[rows], glse[rows]
+    assert max_abs(got, ref) <= TOL[BF16]
+    assert lse_err(glse, rlse) <= LSE_TOL[BF16]
+    return got
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("window,sink", [(-1, "randn"), (0, "none"), (100, "randn")])
+def test_contiguous_matches_oracle(causal, window, sink):
+    """NaN rows after the last request: a tile that runs past a request's keys
+    must mask them (keys) and zero them (values)."""
+    q_lens = [0, 5, 127, 128, 300, 1, 64]
+    kv_lens = [10, 5, 127, 1000, 300, 0, 129]
+    case = W.make_varlen_kv(q_lens, kv_lens, 32, 8, 128, 16, BF16, seed=window + 90,
+                            sink=sink, window_left=window, causal=causal)
+    _check_contig(case, pad_rows=200)
+
+
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (2, 4), (8, 2), (16, 1)])
+def test_contiguous_group_sizes(G, Hkv):
+    case = W.make_varlen([1, 70, 129, 256], [0, 100, 1000, 3], G * Hkv, Hkv, 128, 16, BF16,
+                         seed=G + 40, sink="randn")
+    _check_contig(case)
+
+
+def test_contiguous_equals_paged():
+    """Same tiles, same arithmetic order: the contiguous and paged forms give
+    identical bits."""
+    case = W.make_varlen([150, 40, 300], [500, 9, 0], 32, 8, 128, 16, BF16, seed=28,
+                         sink="randn", window_left=200)
+    a = gpu_prefill(case)
+    k, v = contiguous_kv(case)
+    b = gpu_prefill_contiguous(case, k, v)
+    assert np.array_equal(a, b)
+
+
+def test_contiguous_without_keys():
+    case = W.make_varlen_kv([3, 4], [0, 0], 8, 2, 128, 16, BF16, seed=29, sink="randn")
+    k, v = contiguous_kv(case)
+    assert k.shape[0] == 0
+    got, glse = gpu_prefill_contiguous(case, k, v, with_lse=True)
+    assert np.all(got == 0)
+    np.testing.assert_allclose(glse, np.broadcast_to(case.sink.numpy(), glse.shape), atol=1e-6)
+
+
+def test_contiguous_rows_past_the_arrays_are_flagged():
+    """cu_seq_lens_k running past total_k: the request is clipped to the rows
+    that exist, PKV_DEVERR_SEQLEN is raised and the other requests are exact."""
+    case = W.make_varlen_kv([40, 40], [100, 100], 8, 2, 128, 16, BF16, seed=30, sink="randn")
+    k, v = contiguous_kv(case)
+    k, v = k[:150].contiguous(), v[:150].contiguous()
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    got = gpu_prefill_contiguous(case, k, v, err=err)
+    assert int(err.item()) & pkv.DEVERR_SEQLEN
+    assert np.isfinite(got).all()
+    ref = oracle_prefill(case, rows=list(range(40)))
+    assert max_abs(got[:40], ref) <= TOL[BF16]
 
 
 def test_decode_equals_prefill_with_one_query():

@@ -24,6 +24,9 @@ MUTATIONS = {
         "qpos - J->window_left <= (int64_t)j", "qpos - J->window_left < (int64_t)j"),
     "causal bound off by one": (
         "(int64_t)j <= qpos", "(int64_t)j < qpos"),
+    "causal flag ignored": (
+        "if (J->causal && !((int64_t)j <= qpos)) allowed = 0;",
+        "if (!((int64_t)j <= qpos)) allowed = 0;"),
     "GQA head mapping modulo": (
         "const int g = h / group;", "const int g = h % Hkv;"),
     "causal mask aligned to the start": (

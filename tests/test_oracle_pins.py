@@ -127,6 +127,32 @@ def test_prefill_matches_sdpa(Hq, Hkv, D, bs, lens, with_sink):
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,bs,q_lens,kv_lens", [
+    (4, 4, 16, 4, [5, 9], [12, 3]),
+    (8, 2, 64, 16, [40, 1], [7, 70]),
+    (8, 1, 32, 8, [3, 20], [50, 20]),
+])
+def test_non_causal_prefill_matches_sdpa(Hq, Hkv, D, bs, q_lens, kv_lens):
+    """Non-causal, no window: every query row attends to all of its request's
+    keys whatever its position, which is SDPA with no mask (q_len may exceed
+    kv_len or fall short of it)."""
+    rng = np.random.default_rng(11 + Hq + D)
+    qd, kd, vd = random_dense(rng, q_lens, kv_lens, Hq, Hkv, D)
+    kp, vp, bt = paginate(kd, vd, bs, rng)
+    scale = 1.0 / math.sqrt(D)
+    out = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(q_lens),
+                           np.array(kv_lens, np.int32), causal=False, sm_scale=scale)
+    G = Hq // Hkv
+    ref = []
+    for r in range(len(q_lens)):
+        qt = torch.from_numpy(qd[r].astype(np.float64)).permute(1, 0, 2)[None]
+        kt = torch.from_numpy(kd[r].astype(np.float64)).repeat_interleave(G, 1).permute(1, 0, 2)[None]
+        vt = torch.from_numpy(vd[r].astype(np.float64)).repeat_interleave(G, 1).permute(1, 0, 2)[None]
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+        ref.append(o[0].permute(1, 0, 2).numpy())
+    np.testing.assert_allclose(out, np.concatenate(ref), rtol=0, atol=1e-12)
+
+
 def test_sink_only_rescales():
     """With a sink the output is the plain output times one per-row factor in
     (0, 1): the sink adds to the denominator only."""
