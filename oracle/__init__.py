@@ -73,6 +73,10 @@ def _load():
                 ctypes.c_int, P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, P,
                 ctypes.c_int, ctypes.c_int, ctypes.c_double, P, ctypes.c_int, ctypes.c_int]
             lib.oracle_attention.restype = ctypes.c_int
+            lib.oracle_rope.argtypes = [P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, P,
+                                        ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                        ctypes.c_int]
+            lib.oracle_rope.restype = None
             lib.oracle_online_cores.argtypes = []
             lib.oracle_online_cores.restype = ctypes.c_int
             _ = i32
@@ -171,6 +175,22 @@ def attention(q, k_cache, v_cache, block_table, cu_seq_lens_q, kv_lens, sink=Non
     if rc != 0:
         raise ValueError(f"oracle_attention failed with code {rc}")
     return (out, lse) if with_lse else out
+
+
+def rope(x, positions, rotary_dim: int, base: float = 10000.0, position_scale: float = 1.0,
+         neox: bool = True) -> np.ndarray:
+    """Rotary position embedding of x [T, H, D] (float32, or uint16 bf16 bits)
+    at positions [T]; returns float64 [T, H, D].  Dimensions past rotary_dim
+    are copied.  position_scale divides the positions (linear scaling)."""
+    x = np.ascontiguousarray(x)
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    T, H, D = x.shape
+    if pos.shape != (T,) or rotary_dim % 2 or not 0 < rotary_dim <= D:
+        raise ValueError("rope: positions must be [T]; rotary_dim even, 0 < rotary_dim <= D")
+    out = np.empty((T, H, D), dtype=np.float64)
+    _load().oracle_rope(_ptr(out), _ptr(x), _dtype_code(x), T, H, D, _ptr(pos), int(rotary_dim),
+                        float(base), float(position_scale), int(bool(neox)))
+    return out
 
 
 def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, sink=None,

@@ -275,3 +275,44 @@ int oracle_attention(double *out, double *lse, const void *q, int q_dtype, const
 }
 
 int oracle_online_cores(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }
+
+/* ------------------------------------------------------------------------ */
+/* rotary position embedding                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* The rotary step that precedes the cache write (vLLM attention.py,
+ * PagedAttentionWithRoPE.forward: rotary_emb(positions, query, key) with
+ * head_size, rotary_dim, base, is_neox_style and a rope_scaling factor).
+ * The page names those parameters but does not spell the rotation out; it is
+ * the rotary position embedding of RoFormer (Su et al., 2021):
+ *   - frequency i in [0, rotary_dim/2):  theta_i = base^(-2i / rotary_dim);
+ *   - a token at position m turns the pair (x_a, x_b) of frequency i by the
+ *     angle m' * theta_i, where m' = m / position_scale (linear position
+ *     scaling; 1 means none):
+ *         x_a' = x_a cos - x_b sin,   x_b' = x_b cos + x_a sin;
+ *   - the pairs: neox style (a, b) = (i, i + rotary_dim/2), the two halves
+ *     of the rotated part; otherwise (GPT-J style) (a, b) = (2i, 2i + 1);
+ *   - dimensions rotary_dim .. head_dim-1 are not rotated.
+ * x: [num_tokens, num_heads, head_dim] in dtype; out: the same shape, fp64,
+ * every value exact up to the rounding of double arithmetic. */
+void oracle_rope(double *out, const void *x, int dtype, int64_t num_tokens, int num_heads,
+                 int head_dim, const int64_t *positions, int rotary_dim, double base,
+                 double position_scale, int neox) {
+    const int half = rotary_dim / 2;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const double m = (double)positions[t] / position_scale;
+        for (int h = 0; h < num_heads; ++h) {
+            const int64_t row = (t * num_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) out[row + d] = widen(x, dtype, row + d);
+            for (int i = 0; i < half; ++i) {
+                const double theta = pow(base, -2.0 * i / rotary_dim);
+                const double c = cos(m * theta), s = sin(m * theta);
+                const int a = neox ? i : 2 * i;
+                const int b = neox ? i + half : 2 * i + 1;
+                const double xa = widen(x, dtype, row + a), xb = widen(x, dtype, row + b);
+                out[row + a] = xa * c - xb * s;
+                out[row + b] = xb * c + xa * s;
+            }
+        }
+    }
+}

@@ -42,6 +42,18 @@ MUTATIONS = {
         "s_buf[j] = J->sm_scale * dot;", "s_buf[j] = dot;"),
     "request bound inclusive": (
         "if (cu[r] <= t && t < cu[r + 1]) {", "if (cu[r] <= t && t <= cu[r + 1]) {"),
+    "rope: sine term with the wrong sign": (
+        "out[row + a] = xa * c - xb * s;", "out[row + a] = xa * c + xb * s;"),
+    "rope: frequency exponent without the 2": (
+        "pow(base, -2.0 * i / rotary_dim)", "pow(base, -1.0 * i / rotary_dim)"),
+    "rope: neox pairs off by one": (
+        "const int b = neox ? i + half : 2 * i + 1;",
+        "const int b = neox ? i + half - 1 : 2 * i + 1;"),
+    "rope: position scale multiplies": (
+        "(double)positions[t] / position_scale", "(double)positions[t] * position_scale"),
+    "rope: unrotated tail dropped": (
+        "for (int d = 0; d < head_dim; ++d) out[row + d] = widen(x, dtype, row + d);",
+        "for (int d = 0; d < head_dim; ++d) out[row + d] = 0.0;"),
     "cache write ignores the skip marker": (
         "if (s < 0) continue;", "if (s < -1) continue;"),
 }

@@ -10,7 +10,11 @@ Each test checks the oracle against a fact the pages or the mathematics fix:
   * closed forms: window_left = 0 leaves one key, o = v * sigmoid(s - sink);
   * invariances: physical page relabelling, page size, window >= kv_len,
     decode == last prefill row, chunk == suffix of a longer chunk;
-  * an independent dense brute force in numpy on tiny inputs.
+  * an independent dense brute force in numpy on tiny inputs;
+  * the rotary step: RoFormer's complex-multiplication statement of the
+    rotation, composition of rotations, relative-position invariance of the
+    rotated dot product, linear position scaling and the neox / GPT-J pairing
+    relation.
 """
 import json
 import math
@@ -337,3 +341,88 @@ def test_reshape_and_cache_places_rows_bit_exactly():
         assert flat_v[s].tobytes() == val[t].tobytes()
     untouched = np.setdiff1d(np.arange(nb * bs), g["new_token_slot"])
     assert np.isnan(flat_k[untouched]).all() and np.isnan(flat_v[untouched]).all()
+
+
+# ---------------------------------------------------------------------------
+# rotary position embedding
+# ---------------------------------------------------------------------------
+
+def _rope_complex(x, pos, rd, base, scale, neox):
+    """RoFormer's statement: the pair of frequency i, read as the complex
+    number x_a + i x_b, is multiplied by exp(i * (m / scale) * base^(-2i/rd))."""
+    x = x.astype(np.float64)
+    out = x.copy()
+    half = rd // 2
+    idx = np.arange(half)
+    a, b = (idx, idx + half) if neox else (2 * idx, 2 * idx + 1)
+    z = x[..., a] + 1j * x[..., b]
+    freq = np.power(float(base), -(2.0 * idx) / rd)
+    rot = np.exp(1j * (np.asarray(pos, np.float64)[:, None] / scale) * freq[None, :])
+    z = z * rot[:, None, :]
+    out[..., a], out[..., b] = z.real, z.imag
+    return out
+
+
+@pytest.mark.parametrize("neox", [True, False])
+@pytest.mark.parametrize("D,rd,base,scale", [(64, 64, 10000.0, 1.0), (128, 64, 10000.0, 1.0),
+                                             (80, 80, 500000.0, 4.0), (16, 8, 10.0, 2.0)])
+def test_rope_matches_complex_rotation(neox, D, rd, base, scale):
+    rng = np.random.default_rng(D + rd)
+    x = rng.standard_normal((7, 3, D)).astype(np.float32)
+    pos = np.array([0, 1, 2, 17, 1000, 32767, 131071], np.int64)
+    got = oracle.rope(x, pos, rd, base=base, position_scale=scale, neox=neox)
+    np.testing.assert_allclose(got, _rope_complex(x, pos, rd, base, scale, neox), rtol=0,
+                               atol=1e-9)
+    np.testing.assert_array_equal(got[..., rd:], x[..., rd:].astype(np.float64))
+    np.testing.assert_array_equal(got[0], x[0].astype(np.float64))  # position 0: identity
+
+
+def test_rope_bf16_input_widened_exactly():
+    rng = np.random.default_rng(3)
+    xf = rng.standard_normal((4, 2, 32)).astype(np.float32)
+    bits = (xf.view(np.uint32) >> 16).astype(np.uint16)           # truncate to bf16
+    widened = (bits.astype(np.uint32) << 16).view(np.float32)
+    pos = np.array([3, 9, 27, 81])
+    np.testing.assert_array_equal(oracle.rope(bits, pos, 32), oracle.rope(widened, pos, 32))
+
+
+@pytest.mark.parametrize("neox", [True, False])
+def test_rope_composes_and_is_relative(neox):
+    """Rotations compose (rotating by a then by b is rotating by a+b) and the
+    rotated dot product depends only on the distance of the two positions."""
+    rng = np.random.default_rng(4)
+    D = 32
+    q32 = rng.standard_normal((1, 1, D)).astype(np.float32)
+    k32 = rng.standard_normal((1, 1, D)).astype(np.float32)
+    once = oracle.rope(oracle.rope(q32, [300], D, neox=neox).astype(np.float32), [45], D,
+                       neox=neox)
+    np.testing.assert_allclose(once, oracle.rope(q32, [345], D, neox=neox),
+                               atol=1e-6)  # the intermediate was rounded to fp32
+    dots = [float(np.sum(oracle.rope(q32, [m], D, neox=neox) *
+                         oracle.rope(k32, [m - 13], D, neox=neox))) for m in (13, 50, 4000)]
+    np.testing.assert_allclose(dots, dots[0], rtol=0, atol=1e-9)
+    norms = np.linalg.norm(oracle.rope(q32, [777], D, neox=neox))
+    assert abs(norms - np.linalg.norm(q32.astype(np.float64))) < 1e-12
+
+
+def test_rope_linear_scaling_divides_the_position():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 2, 64)).astype(np.float32)
+    a = oracle.rope(x, [10, 400, 9000], 64, position_scale=2.0)
+    b = oracle.rope(x, [5, 200, 4500], 64, position_scale=1.0)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_rope_neox_is_gptj_on_interleaved_dims():
+    """neox pairs (i, i + rd/2); GPT-J pairs (2i, 2i+1): moving dim i to 2i and
+    dim i + rd/2 to 2i + 1 turns one into the other."""
+    rng = np.random.default_rng(6)
+    D, rd = 48, 32
+    x = rng.standard_normal((5, 2, D)).astype(np.float32)
+    perm = np.arange(D)
+    perm[:rd:2] = np.arange(rd // 2)
+    perm[1:rd:2] = np.arange(rd // 2) + rd // 2
+    pos = [1, 2, 3, 100, 12345]
+    neox = oracle.rope(x, pos, rd, neox=True)
+    gptj = oracle.rope(np.ascontiguousarray(x[..., perm]), pos, rd, neox=False)
+    np.testing.assert_allclose(gptj, neox[..., perm], rtol=0, atol=1e-12)
