@@ -62,7 +62,7 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-configuration decode / prefill lines")
     ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_mixed",
-                                          "write"],
+                                          "write", "rope"],
                     default=None,
                     help="run a few launches of one call on a mid-size case (for ncu)")
     return ap.parse_args()
@@ -198,6 +198,37 @@ def prefill_flops(case):
     pairs = sum(attended_pairs(int(q), int(k), case.window_left)
                 for q, k in zip(case.q_lens.tolist(), case.kv_lens.tolist()))
     return 4 * Hq * D * pairs
+
+
+def rope_bytes(num_tokens, Hq, Hkv, D, rotary_dim, elem_bytes):
+    """Algorithmic HBM bytes of rope_reshape_and_cache: per token the rotated
+    part of every q head is read and written back; every k head is read,
+    its rotated part written back and the whole row written to the cache;
+    every v head is read and written to the cache; plus the int64 position
+    and slot.  The cos/sin table (L2 resident, shared by tokens at one
+    position) is not counted."""
+    per_token = elem_bytes * (2 * Hq * rotary_dim + Hkv * (2 * D + rotary_dim) + 2 * Hkv * D)
+    return num_tokens * (per_token + 16)
+
+
+def time_flushed(fn, K, flush):
+    """Mean device time of fn over K launches, each timed alone with CUDA
+    events after a write of a buffer larger than L2 (so no launch reads what
+    the previous one left in L2)."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(K):
+        flush.add_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
 def source_sha(*names):
@@ -405,6 +436,26 @@ def extra_configs(dev, K, peaks):
     tf = fl / (ms * 1e-3) / 1e12
     out["config4_prefill_B16"] = {"ms": round(ms, 4), "flops": fl, "TFLOP/s": round(tf, 1),
                                   "frac_bf16_measured_burst": round(tf / peaks["bf16_tflops"], 3)}
+    del q, kc, vc, outp, ws
+    torch.cuda.empty_cache()
+
+    # rotary embedding fused with the cache write, on the mixed step's 8448 new
+    # tokens (their queries are the decode and prefill queries of the step)
+    c5 = W.config5_mixed()
+    qr = torch.cat([c5.decode.q, c5.prefill.q]).to(dev)
+    kr, vr = c5.key.to(dev), c5.value.to(dev)
+    kc5, vc5 = c5.k_cache.to(dev), c5.v_cache.to(dev)
+    pos, sm = c5.positions.to(dev), c5.slot_mapping.to(dev)
+    tab = pkv.rope_cos_sin_table(32768, 128)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ms = time_flushed(lambda: pkv.rope_reshape_and_cache(qr, kr, vr, kc5, vc5, pos, sm, tab),
+                      K, flush)
+    byts = rope_bytes(c5.num_new_tokens, qr.shape[1], kr.shape[1], kr.shape[2], 128, 2)
+    gbs = byts / (ms * 1e-3) / 1e9
+    out["rope_reshape_and_cache_mixed_8448tok"] = {
+        "ms": round(ms, 4), "bytes": byts, "GB/s": round(gbs, 1),
+        "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 3),
+        "l2": "256 MB buffer written before each timed launch"}
     return out
 
 
@@ -555,7 +606,8 @@ def run_reference(args, dist):
 def run_profile(which: str):
     """A few launches of one call on a case larger than L2 but a few GB at
     most: decode = the B64 / L512-4096 decode batch (~0.6 GB of KV), prefill =
-    the B16 varlen prefill batch, write = the mixed step's cache write."""
+    the B16 varlen prefill batch, write = the mixed step's cache write, rope =
+    the rotary step fused with the write for 8448 tokens."""
     import torch
     import paged_kv_cache_attention_gb300 as pkv
     from paged_kv_cache_attention_gb300 import workloads as W
@@ -583,6 +635,16 @@ def run_profile(which: str):
         sink = None if c.sink is None else c.sink.to(dev)
         go = lambda: pkv.varlen_prefill(q, kc, vc, bt, cq, ck, c.max_seqlen_q, c.max_seqlen_k,
                                         sink=sink, sm_scale=c.sm_scale)
+    elif which == "rope":
+        # 8448 tokens shaped like the mixed step's new tokens, on a pool just
+        # large enough for them (~0.2 GB on the device in all)
+        c = W.make_rope(8448, 32, 8, 128, 128, 16, torch.bfloat16, seed=W.seed_for(5) + 7,
+                        max_position=32768, skip_every=0)
+        qr, key, val = c.query.to(dev), c.key.to(dev), c.value.to(dev)
+        kc, vc = c.k_cache.to(dev), c.v_cache.to(dev)
+        pos, sm = c.positions.to(dev), c.slot_mapping.to(dev)
+        tab = pkv.rope_cos_sin_table(c.max_position, 128)
+        go = lambda: pkv.rope_reshape_and_cache(qr, key, val, kc, vc, pos, sm, tab)
     else:
         c = W.config5_mixed()
         kc, vc = c.k_cache.to(dev), c.v_cache.to(dev)

@@ -1,13 +1,16 @@
 /*
  * pkv.h -- C ABI of libpkv: attention over a paged KV cache on GB300 (sm_103a).
  *
- * Three operations, each an asynchronous launch sequence on the caller's
+ * The operations, each an asynchronous launch sequence on the caller's
  * CUDA stream:
  *
  *   pkv_reshape_and_cache  write the new tokens' K/V rows into the paged pools
  *                          at the flat slots slot_mapping names
  *                          (vLLM attention.py, PagedAttention.forward: the
  *                          cache_ops.reshape_and_cache step);
+ *   pkv_rope_reshape_and_cache  the same write preceded by the rotary
+ *                          position embedding of query and key
+ *                          (vLLM attention.py, PagedAttentionWithRoPE);
  *   pkv_paged_decode       one query token per sequence, attending to positions
  *                          0 .. cache_seqlens[b]-1 gathered through block_table
  *                          (transformers docs "paged_attention", decode path;
@@ -97,6 +100,7 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEVERR_SEQLEN 4u   /* a length above its declared maximum, negative, or
                                   beyond max_blocks_per_seq * block_size */
 #define PKV_DEVERR_TIMEOUT 8u  /* a bounded pipeline wait gave up */
+#define PKV_DEVERR_POSITION 16u /* a rotary position outside [0, max_position) */
 
 /* Description of the two paged pools (same shape and dtype). */
 typedef struct pkv_cache_desc {
@@ -126,6 +130,53 @@ PKV_API pkv_status pkv_reshape_and_cache(const void *key, const void *value, voi
                                  void *v_cache, const int64_t *slot_mapping,
                                  int64_t num_tokens, pkv_cache_desc cache, int32_t *dev_error,
                                  void *stream);
+
+/*
+ * Rotary position embedding (vLLM attention.py, PagedAttentionWithRoPE:
+ * rotary_dim, base, is_neox_style, rope_scaling), in two calls.
+ *
+ * rope_cos_sin_table: fill cos_sin ([max_position, rotary_dim / 2] pairs of
+ * float32 (cos, sin), device memory owned by the caller, 16-byte aligned)
+ * with the angles (pos / position_scale) * base^(-2i / rotary_dim) for
+ * pos in [0, max_position) and i in [0, rotary_dim / 2).  The angles and
+ * their cos/sin are computed in fp64 and rounded once to fp32.  Linear
+ * scaling is position_scale = factor; dynamic-NTK scaling is an adjusted
+ * base (computed by the caller).  Build the table once per configuration.
+ */
+PKV_API pkv_status pkv_rope_cos_sin_table(float *cos_sin, int max_position, int rotary_dim,
+                                          double base, double position_scale, void *stream);
+
+/*
+ * rope_reshape_and_cache: for every token t, at position positions[t]:
+ *   - rotate the first rotary_dim dimensions of every q head of query
+ *     ([num_tokens, num_qo_heads, head_dim]) and every kv head of key
+ *     ([num_tokens, Hkv, head_dim]) in place: the pair (x_a, x_b) of
+ *     frequency i turns by the table's angle, x_a' = x_a cos - x_b sin,
+ *     x_b' = x_b cos + x_a sin, with (a, b) = (i, i + rotary_dim/2) when
+ *     is_neox_style, else (2i, 2i + 1) (RoFormer's rotary embedding); the
+ *     other dimensions are not touched;
+ *   - then, as pkv_reshape_and_cache, store the rotated key row and the value
+ *     row at flat slot slot_mapping[t] (negative: not cached).
+ * Arithmetic in fp32, rounded to the dtype of the cache once.  positions and
+ * slot_mapping are int64 device arrays; cos_sin is a table built by
+ * pkv_rope_cos_sin_table with this rotary_dim and max_position rows.  A token
+ * whose position is outside [0, max_position) is left untouched (query, key
+ * and cache) and sets PKV_DEVERR_POSITION; a slot >= num_blocks * block_size
+ * skips that token's cache write and sets PKV_DEVERR_SLOT.  query may be
+ * NULL when num_qo_heads == 0.  Requirements: rotary_dim even, 0 < rotary_dim
+ * <= head_dim and a multiple of 2 * (16 / element size) (16 for bf16, 8 for
+ * fp32); head_dim a multiple of 16 / element size; every pointer 16-byte
+ * aligned (positions and slot_mapping 8-byte).  head_dim is not limited to
+ * 64 and 128 here.
+ */
+PKV_API pkv_status pkv_rope_reshape_and_cache(void *query, void *key, const void *value,
+                                              void *k_cache, void *v_cache,
+                                              const int64_t *positions,
+                                              const int64_t *slot_mapping, int64_t num_tokens,
+                                              int num_qo_heads, pkv_cache_desc cache,
+                                              const float *cos_sin, int max_position,
+                                              int rotary_dim, int is_neox_style,
+                                              int32_t *dev_error, void *stream);
 
 /*
  * Workspace bytes pkv_paged_decode needs: split-KV partials for

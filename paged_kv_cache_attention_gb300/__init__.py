@@ -32,7 +32,9 @@ __all__ = [
     "build", "load_library", "PkvError", "reshape_and_cache", "paged_decode",
     "varlen_prefill", "varlen_prefill_contiguous", "paged_decode_noalloc",
     "paged_decode_workspace_size", "varlen_prefill_workspace_size",
-    "DEVERR_BLOCK_ID", "DEVERR_SLOT", "DEVERR_SEQLEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
+    "rope_cos_sin_table", "rope_reshape_and_cache", "ntk_scaled_base",
+    "DEVERR_BLOCK_ID", "DEVERR_SLOT", "DEVERR_SEQLEN", "DEVERR_TIMEOUT", "DEVERR_POSITION",
+    "EXPORTED_SYMBOLS",
 ]
 
 PKV_F32 = 0
@@ -41,12 +43,13 @@ DEVERR_BLOCK_ID = 1
 DEVERR_SLOT = 2
 DEVERR_SEQLEN = 4
 DEVERR_TIMEOUT = 8
+DEVERR_POSITION = 16
 
 EXPORTED_SYMBOLS = (
     "pkv_status_string", "pkv_version", "pkv_reshape_and_cache",
     "pkv_paged_decode_workspace_size", "pkv_paged_decode",
     "pkv_varlen_prefill_workspace_size", "pkv_varlen_prefill",
-    "pkv_varlen_prefill_contiguous",
+    "pkv_varlen_prefill_contiguous", "pkv_rope_cos_sin_table", "pkv_rope_reshape_and_cache",
 )
 
 
@@ -106,6 +109,12 @@ def load_library(path: Optional[str] = None):
                                                       i32, i32, P, i32, i32, i32, i32, f32, P,
                                                       P, sz, P, P]
         lib.pkv_varlen_prefill_contiguous.restype = i32
+        f64 = ctypes.c_double
+        lib.pkv_rope_cos_sin_table.argtypes = [P, i32, i32, f64, f64, P]
+        lib.pkv_rope_cos_sin_table.restype = i32
+        lib.pkv_rope_reshape_and_cache.argtypes = [P, P, P, P, P, P, P, i64, i32, CacheDesc, P,
+                                                   i32, i32, i32, P, P]
+        lib.pkv_rope_reshape_and_cache.restype = i32
         _lib = lib
         return lib
 
@@ -213,6 +222,66 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, dev_error=None
         _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
         key.shape[0], desc, _ptr(dev_error), _stream_handle(stream))
     _check("pkv_reshape_and_cache", st)
+
+
+def ntk_scaled_base(base: float, rotary_dim: int, alpha: float) -> float:
+    """Base of NTK-aware rotary scaling: stretching the context alpha times
+    raises the base to base * alpha^(rotary_dim / (rotary_dim - 2)), so that
+    the lowest frequency is interpolated by alpha while the highest is kept.
+    A dynamic-NTK caller picks alpha from the length it needs and passes the
+    result as ``base`` to rope_cos_sin_table."""
+    _require(rotary_dim > 2 and alpha > 0, "ntk_scaled_base: rotary_dim > 2, alpha > 0")
+    return float(base) * float(alpha) ** (rotary_dim / (rotary_dim - 2))
+
+
+def rope_cos_sin_table(max_position: int, rotary_dim: int, base: float = 10000.0,
+                       position_scale: float = 1.0, device=None, stream=None):
+    """The rotary table [max_position, rotary_dim // 2, 2] float32 of
+    (cos, sin) of (pos / position_scale) * base^(-2i / rotary_dim), computed
+    in fp64 on the GPU.  position_scale is the linear scaling factor."""
+    torch = _torch()
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    tab = torch.empty(max(max_position, 0), rotary_dim // 2, 2, dtype=torch.float32, device=dev)
+    st = load_library().pkv_rope_cos_sin_table(_ptr(tab) if tab.numel() else None,
+                                               int(max_position), int(rotary_dim), float(base),
+                                               float(position_scale), _stream_handle(stream))
+    _check("pkv_rope_cos_sin_table", st)
+    return tab
+
+
+def rope_reshape_and_cache(query, key, value, k_cache, v_cache, positions, slot_mapping,
+                           cos_sin, rotary_dim: Optional[int] = None, is_neox_style: bool = True,
+                           dev_error=None, stream=None) -> None:
+    """Rotate query [T, Hq, D] and key [T, Hkv, D] in place by positions [T]
+    (int64) using the table cos_sin ([max_position, rotary_dim // 2, 2]), then
+    write the rotated key and the value to the pools at slot_mapping [T]
+    (int64; negative = not cached).  query may be None."""
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache)
+    _cuda_contig("key", key, k_cache.dtype, 3)
+    _cuda_contig("value", value, k_cache.dtype, 3)
+    _cuda_contig("positions", positions, torch.int64, 1)
+    _cuda_contig("slot_mapping", slot_mapping, torch.int64, 1)
+    _cuda_contig("cos_sin", cos_sin, torch.float32, 3)
+    T = key.shape[0]
+    _require(key.shape == value.shape and key.shape[1:] == k_cache.shape[2:],
+             "key/value must be [T, num_kv_heads, head_dim] matching the cache")
+    _require(positions.shape[0] == T and slot_mapping.shape[0] == T,
+             "positions and slot_mapping must have T entries")
+    rd = int(rotary_dim) if rotary_dim is not None else 2 * cos_sin.shape[1]
+    _require(cos_sin.shape[1] * 2 == rd and cos_sin.shape[2] == 2,
+             "cos_sin must be [max_position, rotary_dim // 2, 2]")
+    Hq = 0
+    if query is not None:
+        _cuda_contig("query", query, k_cache.dtype, 3)
+        _require(query.shape[0] == T and query.shape[2] == key.shape[2],
+                 "query must be [T, num_qo_heads, head_dim]")
+        Hq = query.shape[1]
+    st = load_library().pkv_rope_reshape_and_cache(
+        _ptr(query), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(positions),
+        _ptr(slot_mapping), T, Hq, desc, _ptr(cos_sin), cos_sin.shape[0], rd,
+        int(bool(is_neox_style)), _ptr(dev_error), _stream_handle(stream))
+    _check("pkv_rope_reshape_and_cache", st)
 
 
 def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,

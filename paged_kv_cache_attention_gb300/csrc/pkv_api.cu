@@ -189,6 +189,65 @@ pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cac
                                               static_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_rope_cos_sin_table(float *cos_sin, int max_position, int rotary_dim,
+                                  double base, double position_scale, void *stream) {
+    if (max_position < 0 || rotary_dim <= 0 || rotary_dim % 2 != 0) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(base) || base <= 0.0 || !std::isfinite(position_scale) ||
+        position_scale <= 0.0)
+        return PKV_ERR_INVALID_ARG;
+    if (max_position == 0) return PKV_OK;
+    if (!cos_sin || !aligned(cos_sin, 16)) return PKV_ERR_INVALID_ARG;
+    return from_cuda(launch_rope_table(cos_sin, max_position, rotary_dim, base, position_scale,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_rope_reshape_and_cache(void *query, void *key, const void *value, void *k_cache,
+                                      void *v_cache, const int64_t *positions,
+                                      const int64_t *slot_mapping, int64_t num_tokens,
+                                      int num_qo_heads, pkv_cache_desc cache,
+                                      const float *cos_sin, int max_position, int rotary_dim,
+                                      int is_neox_style, int32_t *dev_error, void *stream) {
+    if (num_tokens < 0 || num_qo_heads < 0 || max_position <= 0) return PKV_ERR_INVALID_ARG;
+    if (cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0 ||
+        cache.head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (cache.dtype != PKV_F32 && cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    const int V = 16 / elem_bytes(cache.dtype);
+    if (rotary_dim <= 0 || rotary_dim > cache.head_dim || rotary_dim % 2 != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (rotary_dim % (2 * V) != 0 || cache.head_dim % V != 0) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_qo_heads * cache.head_dim > (1 << 24) ||
+        (int64_t)cache.num_kv_heads * cache.head_dim > (1 << 24))
+        return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!key || !value || !k_cache || !v_cache || !positions || !slot_mapping || !cos_sin ||
+        (num_qo_heads > 0 && !query))
+        return PKV_ERR_INVALID_ARG;
+    if ((query && !aligned(query, 16)) || !aligned(key, 16) || !aligned(value, 16) ||
+        !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(cos_sin, 16) ||
+        !aligned(positions, 8) || !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    RopeParams p;
+    p.query = query;
+    p.key = key;
+    p.value = value;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.positions = positions;
+    p.slot_mapping = slot_mapping;
+    p.cos_sin = reinterpret_cast<const float2 *>(cos_sin);
+    p.dev_error = dev_error;
+    p.num_tokens = num_tokens;
+    p.capacity = cache.num_blocks * (int64_t)cache.block_size;
+    p.max_position = max_position;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = cache.num_kv_heads;
+    p.head_dim = cache.head_dim;
+    p.rotary_dim = rotary_dim;
+    return from_cuda(launch_rope_reshape_cache(p, cache.dtype, is_neox_style != 0,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 size_t pkv_paged_decode_workspace_size(int batch, int num_qo_heads, int head_dim,
                                        int max_seqlen, int partition_size, int window_left) {
     if (batch <= 0 || num_qo_heads <= 0 || head_dim <= 0 || max_seqlen < 0) return 256;

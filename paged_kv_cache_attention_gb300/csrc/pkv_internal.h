@@ -66,6 +66,27 @@ cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
                           const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                           cudaStream_t stream);
 
+// Rotary embedding fused with the cache write.
+struct RopeParams {
+    void *query;                   // [T, Hq, D], rotated in place (may be null if Hq == 0)
+    void *key;                     // [T, Hkv, D], rotated in place
+    const void *value;             // [T, Hkv, D]
+    void *k_cache, *v_cache;       // NHD pools
+    const int64_t *positions;      // [T]
+    const int64_t *slot_mapping;   // [T]
+    const float2 *cos_sin;         // [max_position][rotary_dim / 2] (cos, sin)
+    int32_t *dev_error;
+    int64_t num_tokens;
+    int64_t capacity;              // num_blocks * block_size
+    int64_t max_position;
+    int num_qo_heads, num_kv_heads, head_dim, rotary_dim;
+};
+
+cudaError_t launch_rope_table(float *table, int max_position, int rotary_dim, double base,
+                              double position_scale, cudaStream_t stream);
+cudaError_t launch_rope_reshape_cache(const RopeParams &p, int dtype, bool neox,
+                                      cudaStream_t stream);
+
 // contiguous: K/V are [total_k, Hkv, D] rows addressed by cu_k (the tensor
 // maps use 128-row boxes); otherwise paged pools of cache.block_size rows.
 cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, bool contiguous,

@@ -262,6 +262,52 @@ def make_varlen_kv(q_lens, kv_lens, num_qo_heads, num_kv_heads, head_dim, block_
                       cumsum0(ql), cumsum0(kvl), sk, window_left, scale, causal)
 
 
+@dataclass
+class RopeCase:
+    """New tokens for the rotary step fused with the cache write."""
+    name: str
+    query: torch.Tensor           # [T, Hq, D]
+    key: torch.Tensor             # [T, Hkv, D]
+    value: torch.Tensor
+    k_cache: torch.Tensor         # [num_blocks, bs, Hkv, D], NaN before the write
+    v_cache: torch.Tensor
+    positions: torch.Tensor       # int64 [T]
+    slot_mapping: torch.Tensor    # int64 [T], distinct; some -1 (not cached)
+    rotary_dim: int
+    base: float
+    position_scale: float
+    neox: bool
+    max_position: int
+
+
+def make_rope(num_tokens: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+              rotary_dim: int, block_size: int, dtype, seed: int, max_position: int = 8192,
+              base: float = 10000.0, position_scale: float = 1.0, neox: bool = True,
+              skip_every: int = 7, name: str = "rope") -> RopeCase:
+    """num_tokens tokens at uniform positions in [0, max_position) (the first
+    two at 0 and max_position - 1), written to distinct random slots of a NaN
+    pool with a quarter of spare room; every skip_every-th token has slot -1."""
+    gen = _gen(seed)
+    T = int(num_tokens)
+    nb = max(1, pages_for(T + T // 4, block_size))
+    q = randn((T, num_qo_heads, head_dim), dtype, gen)
+    k = randn((T, num_kv_heads, head_dim), dtype, gen)
+    v = randn((T, num_kv_heads, head_dim), dtype, gen)
+    pos = torch.randint(0, max_position, (T,), generator=gen, dtype=torch.int64)
+    if T > 0:
+        pos[0] = 0
+    if T > 1:
+        pos[1] = max_position - 1
+    slots = torch.randperm(nb * block_size, generator=gen)[:T].to(torch.int64)
+    if skip_every > 0:
+        slots[skip_every - 1::skip_every] = -1
+    shape = (nb, block_size, num_kv_heads, head_dim)
+    kc = torch.full(shape, float("nan"), dtype=dtype)
+    vc = torch.full(shape, float("nan"), dtype=dtype)
+    return RopeCase(name, q, k, v, kc, vc, pos, slots, int(rotary_dim), float(base),
+                    float(position_scale), bool(neox), int(max_position))
+
+
 # ---------------------------------------------------------------------------
 # the five serving configurations
 # ---------------------------------------------------------------------------
@@ -337,6 +383,7 @@ class MixedCase:
     v_cache: torch.Tensor
     decode: DecodeCase            # attends over cache length + 1
     prefill: VarlenCase
+    positions: Optional[torch.Tensor] = None  # int64 [T]: position of each new token
 
     @property
     def num_new_tokens(self):
@@ -359,12 +406,14 @@ def make_mixed(dec_lens, chunk_q: int, chunk_prefix: int, n_chunks: int, num_qo_
     dec_bt, pre_bt = pool.block_tables
     # slots of the new tokens: position L_b of decode sequence b, then
     # positions chunk_prefix .. kv_pre-1 of each prefill request
-    slots = []
+    slots, positions = [], []
     for b, L in enumerate(dec_lens):
         slots.append(int(dec_bt[b, L // block_size]) * block_size + L % block_size)
+        positions.append(L)
     for r in range(n_chunks):
         for p in range(chunk_prefix, kv_pre):
             slots.append(int(pre_bt[r, p // block_size]) * block_size + p % block_size)
+            positions.append(p)
     T = len(slots)
     key = randn((T, num_kv_heads, head_dim), dtype, gen)
     value = randn((T, num_kv_heads, head_dim), dtype, gen)
@@ -379,7 +428,8 @@ def make_mixed(dec_lens, chunk_q: int, chunk_prefix: int, n_chunks: int, num_qo_
     pre = VarlenCase(name + "-prefill", q_pre, pool.k_cache, pool.v_cache, pre_bt,
                      cumsum0(ql), cumsum0(kvl), None, -1, scale, True)
     return MixedCase(name, key, value, torch.tensor(slots, dtype=torch.int64),
-                     pool.k_cache, pool.v_cache, dec, pre)
+                     pool.k_cache, pool.v_cache, dec, pre,
+                     torch.tensor(positions, dtype=torch.int64))
 
 
 def config5_mixed() -> MixedCase:

@@ -163,3 +163,47 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError):
         pkv.paged_decode(q, kc, kc, torch.zeros(2, 1, dtype=torch.int32),
                          torch.zeros(2, dtype=torch.int32), max_seqlen=16)
+
+
+@nogpu
+@pytest.mark.parametrize("change,expected", [
+    (dict(num_tokens=0), 0),
+    (dict(num_tokens=-1), 1),
+    (dict(rd=0), 1),
+    (dict(rd=130), 1),              # longer than head_dim
+    (dict(rd=7), 1),                # odd
+    (dict(rd=24), 2),               # bf16 needs a multiple of 16
+    (dict(max_pos=0), 1),
+    (dict(query=None), 1),          # query missing with num_qo_heads > 0
+    (dict(query=None, hq=0), 4),    # valid; no device to launch on here
+    (dict(table=FAKE + 8), 1),      # not 16-byte aligned
+    (dict(dtype=3), 2),
+])
+def test_rope_reshape_and_cache_validation(change, expected):
+    lib = pkv.load_library()
+    a = dict(num_tokens=10, rd=64, max_pos=4096, query=FAKE, hq=32, table=FAKE, dtype=1)
+    a.update(change)
+    st = lib.pkv_rope_reshape_and_cache(a["query"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                        a["num_tokens"], a["hq"], _desc(dtype=a["dtype"]),
+                                        a["table"], a["max_pos"], a["rd"], 1, None, None)
+    if expected == 4:
+        assert st != 0 and st not in (1, 2, 3)
+    else:
+        assert st == expected
+
+
+@nogpu
+def test_rope_table_validation():
+    f = pkv.load_library().pkv_rope_cos_sin_table
+    assert f(FAKE, 0, 64, 10000.0, 1.0, None) == 0       # nothing to fill
+    assert f(FAKE, 10, 63, 10000.0, 1.0, None) == 1      # odd rotary_dim
+    assert f(FAKE, 10, 64, -1.0, 1.0, None) == 1         # base must be positive
+    assert f(FAKE, 10, 64, 10000.0, 0.0, None) == 1      # scale must be positive
+    assert f(None, 10, 64, 10000.0, 1.0, None) == 1
+
+
+def test_ntk_scaled_base():
+    assert pkv.ntk_scaled_base(10000.0, 128, 1.0) == 10000.0
+    # the lowest frequency base^(-(rd-2)/rd) is divided by exactly alpha
+    b = pkv.ntk_scaled_base(10000.0, 128, 4.0)
+    assert abs(b ** (-126 / 128) * 4.0 - 10000.0 ** (-126 / 128)) < 1e-15

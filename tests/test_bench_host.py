@@ -38,6 +38,14 @@ def test_decode_bytes_count_window():
     assert bench.kv_bytes_decode(case) == (10 + 100) * 2 * 64 * 2 * 2
 
 
+def test_rope_bytes_by_hand():
+    """2 q heads, 1 kv head, head_dim 8, rotary_dim 4, bf16: q reads and writes
+    4 dims of 2 heads (32 B), k is read (16 B), its 4 rotated dims written
+    back (8 B) and its row cached (16 B), v read and cached (32 B), plus 16 B
+    of position and slot: 120 B a token."""
+    assert bench.rope_bytes(3, 2, 1, 8, 4, 2) == 360
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
