@@ -70,7 +70,7 @@ def _load():
             lib.oracle_reshape_and_cache.restype = None
             lib.oracle_attention.argtypes = [
                 P, P, P, ctypes.c_int, P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, P,
+                ctypes.c_int, P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, P, P,
                 ctypes.c_int, ctypes.c_int, ctypes.c_double, P, ctypes.c_int, ctypes.c_int]
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_rope.argtypes = [P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, P,
@@ -136,12 +136,13 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping) -> None:
 
 def attention(q, k_cache, v_cache, block_table, cu_seq_lens_q, kv_lens, sink=None,
               causal: bool = True, window_left: int = -1, sm_scale: float = 1.0,
-              rows=None, threads: int = 0, with_lse: bool = False):
+              rows=None, threads: int = 0, with_lse: bool = False, alibi_slopes=None):
     """Paged attention of every query row (or of ``rows``) in fp64.
 
     q: [total_q, Hq, D]; caches: [num_blocks, block_size, Hkv, D] (NHD pages);
     block_table: [batch, max_blocks_per_seq] int32; cu_seq_lens_q: [batch+1];
-    kv_lens: [batch]; sink: [Hq] float32 or None (no sink).
+    kv_lens: [batch]; sink: [Hq] float32 or None (no sink); alibi_slopes: [Hq]
+    float32 or None (no ALiBi bias).
     Returns out [nrows, Hq, D] float64 (and lse [nrows, Hq] if with_lse).
     """
     q = np.ascontiguousarray(q)
@@ -159,6 +160,9 @@ def attention(q, k_cache, v_cache, block_table, cu_seq_lens_q, kv_lens, sink=Non
     if D2 != D:
         raise ValueError("head_dim mismatch")
     sk = None if sink is None else np.ascontiguousarray(sink, dtype=np.float32)
+    al = None if alibi_slopes is None else np.ascontiguousarray(alibi_slopes, dtype=np.float32)
+    if al is not None and al.shape != (Hq,):
+        raise ValueError("alibi_slopes must have num_qo_heads entries")
     if rows is None:
         rw = None
         nrows = int(cu[-1]) if batch > 0 else 0
@@ -170,7 +174,7 @@ def attention(q, k_cache, v_cache, block_table, cu_seq_lens_q, kv_lens, sink=Non
     rc = _load().oracle_attention(
         _ptr(out), _ptr(lse), _ptr(q), qd, _ptr(k_cache), _ptr(v_cache), kd, num_blocks,
         block_size, Hkv, D, _ptr(bt), bt.shape[1] if bt.ndim == 2 else 0, _ptr(cu), _ptr(kl),
-        batch, Hq, _ptr(sk), int(bool(causal)), int(window_left), float(sm_scale), _ptr(rw),
+        batch, Hq, _ptr(sk), _ptr(al), int(bool(causal)), int(window_left), float(sm_scale), _ptr(rw),
         nrows, int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attention failed with code {rc}")
@@ -195,10 +199,10 @@ def rope(x, positions, rotary_dim: int, base: float = 10000.0, position_scale: f
 
 def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, sink=None,
                  window_left: int = -1, sm_scale: float = 1.0, rows=None, threads: int = 0,
-                 with_lse: bool = False):
+                 with_lse: bool = False, alibi_slopes=None):
     """Single-token decode: one query per sequence at position cache_seqlens[b]-1."""
     B = q.shape[0]
     cu = np.arange(B + 1, dtype=np.int32)
     return attention(q, k_cache, v_cache, block_table, cu, cache_seqlens, sink=sink,
                      causal=True, window_left=window_left, sm_scale=sm_scale, rows=rows,
-                     threads=threads, with_lse=with_lse)
+                     threads=threads, with_lse=with_lse, alibi_slopes=alibi_slopes)

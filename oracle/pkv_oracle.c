@@ -24,6 +24,8 @@
  *   - sink softmax: the per-query-head sink logit is one extra softmax column
  *     that is dropped after normalising, so the denominator gains exp(sink[h])
  *     (sink_attention_reference.py, sink_softmax);
+ *   - ALiBi (optional): slope[h] * (j - position) is added to the scaled
+ *     logit (vLLM attention.py, PagedAttentionWithALiBi);
  *   - o = sum_j p_j v_j (the final einsum).
  *
  * Readings where the pages are silent (they are listed with the design notes):
@@ -126,6 +128,7 @@ typedef struct {
     const int32_t *kv_lens;/* [batch] */
     int batch, num_qo_heads;
     const float *sink;     /* [Hq] or NULL */
+    const float *alibi;    /* [Hq] ALiBi slopes or NULL */
     int causal, window_left;
     double sm_scale;
     const int32_t *rows;   /* which query rows to compute, or NULL = all */
@@ -172,6 +175,11 @@ static int attend_one(job_t *J, int out_row, int t, int h, double *s_buf) {
             for (int d = 0; d < D; ++d)
                 dot += widen(J->q, J->q_dtype, qbase + d) * widen(J->k_cache, J->kv_dtype, kbase + d);
             s_buf[j] = J->sm_scale * dot;
+            /* ALiBi: the scaled logit gains slope[h] times the signed distance
+             * of the key from the query's position (vLLM attention.py,
+             * PagedAttentionWithALiBi.set_attn_bias: bias[i][j] = j - i times
+             * the head's slope, added to the scaled scores) */
+            if (J->alibi) s_buf[j] += (double)J->alibi[h] * (double)((int64_t)j - qpos);
             if (s_buf[j] > m) m = s_buf[j];
             any = 1;
         }
@@ -241,9 +249,9 @@ int oracle_attention(double *out, double *lse, const void *q, int q_dtype, const
                      const void *v_cache, int kv_dtype, int64_t num_blocks, int block_size,
                      int num_kv_heads, int head_dim, const int32_t *block_table,
                      int max_blocks_per_seq, const int32_t *cu_q, const int32_t *kv_lens,
-                     int batch, int num_qo_heads, const float *sink, int causal,
-                     int window_left, double sm_scale, const int32_t *rows, int nrows,
-                     int nthreads) {
+                     int batch, int num_qo_heads, const float *sink, const float *alibi,
+                     int causal, int window_left, double sm_scale, const int32_t *rows,
+                     int nrows, int nthreads) {
     if (num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0 || head_dim <= 0 ||
         block_size <= 0 || batch < 0 || nrows < 0)
         return -4;
@@ -255,7 +263,7 @@ int oracle_attention(double *out, double *lse, const void *q, int q_dtype, const
     J.num_kv_heads = num_kv_heads; J.head_dim = head_dim;
     J.block_table = block_table; J.max_blocks_per_seq = max_blocks_per_seq;
     J.cu_q = cu_q; J.kv_lens = kv_lens; J.batch = batch; J.num_qo_heads = num_qo_heads;
-    J.sink = sink; J.causal = causal; J.window_left = window_left; J.sm_scale = sm_scale;
+    J.sink = sink; J.alibi = alibi; J.causal = causal; J.window_left = window_left; J.sm_scale = sm_scale;
     J.rows = rows; J.nrows = nrows;
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);

@@ -40,8 +40,10 @@ def paginate(dense_k, dense_v, block_size, rng, spare=3, max_blocks=None):
     return kp, vp, bt
 
 
-def brute_force(q_list, k_list, v_list, sink, causal, window_left, sm_scale):
-    """Dense fp64 attention per request; returns (out [total_q, Hq, D], lse)."""
+def brute_force(q_list, k_list, v_list, sink, causal, window_left, sm_scale, alibi=None):
+    """Dense fp64 attention per request; returns (out [total_q, Hq, D], lse).
+    alibi: [Hq] slopes; the logit of key j for the query at position pos gains
+    slope * (j - pos)."""
     outs, lses = [], []
     for q, k, v in zip(q_list, k_list, v_list):
         q = q.astype(np.float64)
@@ -55,6 +57,8 @@ def brute_force(q_list, k_list, v_list, sink, causal, window_left, sm_scale):
         logits = np.einsum("qhd,khd->hqk", q, kk) * sm_scale  # [Hq, q, kv]
         pos = (kv_len - q_len + np.arange(q_len))[:, None]
         col = np.arange(kv_len)[None, :]
+        if alibi is not None:
+            logits = logits + np.asarray(alibi, np.float64)[:, None, None] * (col - pos)[None]
         mask = np.ones((q_len, kv_len), dtype=bool)
         if causal:
             mask &= col <= pos

@@ -54,6 +54,15 @@ MUTATIONS = {
     "rope: unrotated tail dropped": (
         "for (int d = 0; d < head_dim; ++d) out[row + d] = widen(x, dtype, row + d);",
         "for (int d = 0; d < head_dim; ++d) out[row + d] = 0.0;"),
+    "alibi: distance with the wrong sign": (
+        "(double)J->alibi[h] * (double)((int64_t)j - qpos)",
+        "(double)J->alibi[h] * (double)(qpos - (int64_t)j)"),
+    "alibi: slope of the kv head": (
+        "(double)J->alibi[h] * (double)((int64_t)j - qpos)",
+        "(double)J->alibi[h / group] * (double)((int64_t)j - qpos)"),
+    "alibi: bias scaled by sm_scale": (
+        "if (J->alibi) s_buf[j] += (double)J->alibi[h]",
+        "if (J->alibi) s_buf[j] += J->sm_scale * (double)J->alibi[h]"),
     "cache write ignores the skip marker": (
         "if (s < 0) continue;", "if (s < -1) continue;"),
 }

@@ -10,7 +10,10 @@ Each test checks the oracle against a fact the pages or the mathematics fix:
   * closed forms: window_left = 0 leaves one key, o = v * sigmoid(s - sink);
   * invariances: physical page relabelling, page size, window >= kv_len,
     decode == last prefill row, chunk == suffix of a longer chunk;
-  * an independent dense brute force in numpy on tiny inputs;
+  * an independent dense brute force in numpy on tiny inputs (with and
+    without ALiBi);
+  * ALiBi: the page's own prompt bias (arange(L)[None, :] - arange(L)[:, None]
+    times the head's slope, under the causal mask) handed to torch SDPA;
   * the rotary step: RoFormer's complex-multiplication statement of the
     rotation, composition of rotations, relative-position invariance of the
     rotated dot product, linear position scaling and the neox / GPT-J pairing
@@ -291,10 +294,12 @@ def test_matches_bruteforce(seed):
     sink = None if seed % 4 == 0 else (rng.standard_normal(Hkv * G) * 3).astype(np.float32)
     qd, kd, vd = random_dense(rng, q_lens, kv_lens, Hkv * G, Hkv, D)
     kp, vp, bt = paginate(kd, vd, bs, rng)
+    alibi = (rng.uniform(0.01, 0.6, Hkv * G).astype(np.float32) if seed % 2 else None)
     out, lse = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(q_lens),
                                 np.array(kv_lens, np.int32), sink=sink, causal=causal,
-                                window_left=window, sm_scale=0.21, with_lse=True)
-    ref, ref_lse = brute_force(qd, kd, vd, sink, causal, window, 0.21)
+                                window_left=window, sm_scale=0.21, with_lse=True,
+                                alibi_slopes=alibi)
+    ref, ref_lse = brute_force(qd, kd, vd, sink, causal, window, 0.21, alibi=alibi)
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
     fin = np.isfinite(ref_lse)
     assert np.array_equal(fin, np.isfinite(lse))
@@ -426,3 +431,90 @@ def test_rope_neox_is_gptj_on_interleaved_dims():
     neox = oracle.rope(x, pos, rd, neox=True)
     gptj = oracle.rope(np.ascontiguousarray(x[..., perm]), pos, rd, neox=False)
     np.testing.assert_allclose(gptj, neox[..., perm], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# ALiBi
+# ---------------------------------------------------------------------------
+
+def _alibi_slopes(n):
+    """The geometric slopes of the ALiBi paper for n heads: 2^(-8 i / n)."""
+    return np.array([2.0 ** (-8.0 * (i + 1) / n) for i in range(n)], np.float32)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs,lens", [(4, 4, 16, 4, [9, 30]), (8, 2, 32, 16, [40, 3]),
+                                              (8, 1, 64, 8, [65])])
+@pytest.mark.parametrize("with_sink", [False, True])
+def test_alibi_prefill_matches_the_pages_bias_through_sdpa(Hq, Hkv, D, bs, lens, with_sink):
+    """vLLM attention.py, PagedAttentionWithALiBi.set_attn_bias: for a prompt of
+    length L the bias is (arange(L)[None, :] - arange(L)[:, None]) times each
+    head's slope, added to the scaled scores under the lower-triangular mask.
+    With a sink, one more key with a zero value row and logit sink[h]."""
+    rng = np.random.default_rng(19 + Hq + D)
+    qd, kd, vd = random_dense(rng, lens, lens, Hq, Hkv, D)
+    kp, vp, bt = paginate(kd, vd, bs, rng)
+    slopes = _alibi_slopes(Hq) * np.float32(3.0)  # steeper than the paper's, to matter
+    sink = rng.standard_normal(Hq).astype(np.float32) if with_sink else None
+    scale = 1.0 / math.sqrt(D)
+    out = oracle.attention(np.concatenate(qd), kp, vp, bt, cu(lens), np.array(lens, np.int32),
+                           sink=sink, causal=True, sm_scale=scale, alibi_slopes=slopes)
+    G = Hq // Hkv
+    ref = []
+    for r, L in enumerate(lens):
+        b = torch.arange(L, dtype=torch.float64)
+        bias = (b[None, :] - b[:, None])[None] * torch.from_numpy(slopes.astype(np.float64))[:, None, None]
+        bias = bias.masked_fill(torch.ones(L, L, dtype=torch.bool).triu(1)[None], float("-inf"))
+        qt = torch.from_numpy(qd[r].astype(np.float64)).permute(1, 0, 2)[None]
+        kt = torch.from_numpy(kd[r].astype(np.float64)).repeat_interleave(G, 1).permute(1, 0, 2)[None]
+        vt = torch.from_numpy(vd[r].astype(np.float64)).repeat_interleave(G, 1).permute(1, 0, 2)[None]
+        if sink is not None:
+            col = torch.from_numpy(sink.astype(np.float64))[:, None, None].expand(Hq, L, 1)
+            bias = torch.cat([bias, col], -1)
+            z = torch.zeros(1, Hq, 1, D, dtype=torch.float64)
+            kt, vt = torch.cat([kt, z], 2), torch.cat([vt, z], 2)
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=bias[None],
+                                                             scale=scale)
+        ref.append(o[0].permute(1, 0, 2).numpy())
+    np.testing.assert_allclose(out, np.concatenate(ref), rtol=0, atol=1e-12)
+
+
+def test_alibi_zero_slopes_is_no_alibi():
+    rng = np.random.default_rng(20)
+    qd, kd, vd = random_dense(rng, [5, 20], [30, 20], 4, 2, 16)
+    kp, vp, bt = paginate(kd, vd, 4, rng)
+    args = (np.concatenate(qd), kp, vp, bt, cu([5, 20]), np.array([30, 20], np.int32))
+    a = oracle.attention(*args, sm_scale=0.3)
+    b = oracle.attention(*args, sm_scale=0.3, alibi_slopes=np.zeros(4, np.float32))
+    np.testing.assert_array_equal(a, b)
+
+
+def test_alibi_decode_is_the_last_prompt_row():
+    """The decode query at position L-1 sees bias slope * (j - (L-1)): the
+    last row of the prompt's bias matrix."""
+    rng = np.random.default_rng(21)
+    L, Hq, Hkv, D = 37, 8, 2, 32
+    qd, kd, vd = random_dense(rng, [L], [L], Hq, Hkv, D)
+    kp, vp, bt = paginate(kd, vd, 8, rng)
+    slopes = _alibi_slopes(Hq)
+    full = oracle.attention(qd[0], kp, vp, bt, cu([L]), np.array([L], np.int32),
+                            sm_scale=0.2, alibi_slopes=slopes)
+    dec = oracle.paged_decode(np.ascontiguousarray(qd[0][-1:]), kp, vp, bt,
+                              np.array([L], np.int32), sm_scale=0.2, alibi_slopes=slopes)
+    np.testing.assert_allclose(dec[0], full[-1], rtol=0, atol=1e-13)
+
+
+def test_alibi_identical_keys_give_geometric_weights():
+    """All keys equal: the softmax weights of a decode query are proportional
+    to exp(slope * j), so with value rows e_j the output is that geometric
+    distribution (closed form)."""
+    L, D = 6, 8
+    q = np.ones((1, 1, D), np.float32)
+    k = np.tile(np.full((1, 1, D), 0.5, np.float32), (L, 1, 1))
+    v = np.zeros((L, 1, D), np.float32)
+    v[np.arange(L), 0, np.arange(L)] = 1.0
+    kp, vp, bt = paginate([k], [v], 4, np.random.default_rng(22))
+    slope = 0.7
+    out = oracle.paged_decode(q, kp, vp, bt, np.array([L], np.int32), sm_scale=0.3,
+                              alibi_slopes=np.array([slope], np.float32))
+    w = np.exp(np.float64(np.float32(slope)) * np.arange(L))
+    np.testing.assert_allclose(out[0, 0, :L], w / w.sum(), rtol=0, atol=1e-15)
