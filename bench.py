@@ -378,6 +378,7 @@ def extra_configs(dev, K, peaks):
             tens.append(dict(q=c.q.to(dev), kc=c.k_cache.to(dev), vc=c.v_cache.to(dev),
                              bt=c.block_table.to(dev), sl=c.cache_seqlens.to(dev),
                              sink=None if c.sink is None else c.sink.to(dev), c=c,
+                             alibi=None if c.alibi is None else c.alibi.to(dev),
                              ws=torch.empty(pkv.paged_decode_workspace_size(
                                  c.batch, c.num_qo_heads, c.q.shape[2], c.max_seqlen,
                                  c.partition_size, c.window_left), dtype=torch.uint8,
@@ -390,7 +391,7 @@ def extra_configs(dev, K, peaks):
                 pkv.paged_decode(t["q"], t["kc"], t["vc"], t["bt"], t["sl"], c.max_seqlen,
                                  sink=t["sink"], window_left=c.window_left,
                                  sm_scale=c.sm_scale, partition_size=c.partition_size,
-                                 workspace=t["ws"])
+                                 workspace=t["ws"], alibi_slopes=t["alibi"])
         for _ in range(3):
             go()
         torch.cuda.synchronize()
@@ -409,6 +410,10 @@ def extra_configs(dev, K, peaks):
         torch.cuda.empty_cache()
 
     run_decode("config2_decode_B64_L512-4096", [W.config2_decode()])
+    c2a = W.config2_decode()
+    c2a.alibi = W.alibi_slopes("geometric", c2a.num_qo_heads, None)
+    run_decode("config2_decode_B64_alibi", [c2a])
+    del c2a
     run_decode("config3_decode_B8_L32K-128K_2layers", [W.config3_long(0), W.config3_long(1)])
     c4 = W.config4_prefill()
     q, kc, vc = c4.q.to(dev), c4.k_cache.to(dev), c4.v_cache.to(dev)
@@ -419,23 +424,26 @@ def extra_configs(dev, K, peaks):
                      dtype=torch.uint8, device=dev)
     outp = torch.empty_like(q)
 
-    def go4():
-        pkv.varlen_prefill(q, kc, vc, bt, cq, ck, c4.max_seqlen_q, c4.max_seqlen_k, sink=sink,
-                           sm_scale=c4.sm_scale, out=outp, workspace=ws)
-    for _ in range(3):
-        go4()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(K):
-        go4()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / K
     fl = prefill_flops(c4)
-    tf = fl / (ms * 1e-3) / 1e12
-    out["config4_prefill_B16"] = {"ms": round(ms, 4), "flops": fl, "TFLOP/s": round(tf, 1),
-                                  "frac_bf16_measured_burst": round(tf / peaks["bf16_tflops"], 3)}
+    geo = W.alibi_slopes("geometric", q.shape[1], None).to(dev)
+    for name, al in (("config4_prefill_B16", None), ("config4_prefill_B16_alibi", geo)):
+        def go4():
+            pkv.varlen_prefill(q, kc, vc, bt, cq, ck, c4.max_seqlen_q, c4.max_seqlen_k,
+                               sink=sink, sm_scale=c4.sm_scale, out=outp, workspace=ws,
+                               alibi_slopes=al)
+        for _ in range(3):
+            go4()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(K):
+            go4()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / K
+        tf = fl / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "flops": fl, "TFLOP/s": round(tf, 1),
+                     "frac_bf16_measured_burst": round(tf / peaks["bf16_tflops"], 3)}
     del q, kc, vc, outp, ws
     torch.cuda.empty_cache()
 

@@ -36,6 +36,8 @@
  *   keep key j iff j < kv_len, j <= qpos (causal only), and
  *                  (window_left < 0 or j >= qpos - window_left)
  *   s_j   = sm_scale * <q[i,h,:], k[j,g,:]>  (fp32)
+ *           + alibi_slopes[h] * (j - qpos)   (only with ALiBi slopes: vLLM
+ *                                     attention.py, PagedAttentionWithALiBi)
  *   o     = sum_j exp(s_j) v[j,g,:] / (sum_j exp(s_j) + exp(sink[h]))
  *   lse   = log(sum_j exp(s_j) + exp(sink[h]))           (natural log)
  * sink[h] is a logit, not scaled by sm_scale; sink == NULL means no sink.
@@ -195,6 +197,8 @@ PKV_API size_t pkv_paged_decode_workspace_size(int batch, int num_qo_heads, int 
  *                 the length including it)
  *   max_seqlen    host int >= every cache_seqlens[b] (sizes the grid)
  *   sink          [num_qo_heads] fp32 (device) or NULL
+ *   alibi_slopes  [num_qo_heads] fp32 (device) or NULL: with slopes the
+ *                 logit of key j gains alibi_slopes[h] * (j - (L_b - 1))
  *   window_left   -1 for none, else keep keys j >= L_b - 1 - window_left
  *   partition_size split-KV partition in tokens (0 = 512); a multiple of
  *                 block_size, at most 16384; partitions start at multiples of
@@ -208,10 +212,10 @@ PKV_API size_t pkv_paged_decode_workspace_size(int batch, int num_qo_heads, int 
 PKV_API pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
                             pkv_cache_desc cache, const int32_t *block_table,
                             int max_blocks_per_seq, const int32_t *cache_seqlens,
-                            int max_seqlen, const float *sink, int batch, int num_qo_heads,
-                            int window_left, float sm_scale, int partition_size,
-                            float *lse_out, void *workspace, size_t workspace_bytes,
-                            int32_t *dev_error, void *stream);
+                            int max_seqlen, const float *sink, const float *alibi_slopes,
+                            int batch, int num_qo_heads, int window_left, float sm_scale,
+                            int partition_size, float *lse_out, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_error, void *stream);
 
 /* Workspace bytes pkv_varlen_prefill needs (its work-tile list). */
 PKV_API size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
@@ -229,7 +233,8 @@ PKV_API size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, in
  *                  0: no upper bound, window_left >= 0 still drops keys
  *                  before qpos - window_left (FlashInfer
  *                  sink_attention_reference.py, non-causal varlen mask)
- *   sink, window_left, sm_scale, lse_out ([total_q, num_qo_heads]) as in
+ *   sink, alibi_slopes (bias alibi_slopes[h] * (j - qpos)), window_left,
+ *   sm_scale, lse_out ([total_q, num_qo_heads]) as in
  *   paged_decode.  Causal rows whose position is negative (q_len > kv_len)
  *   keep no key.  Supported: bf16 pools, head_dim 128, block_size 16 or 32,
  *   G = num_qo_heads / num_kv_heads a power of two <= 16; anything else
@@ -240,9 +245,10 @@ PKV_API pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_ca
                               const int32_t *block_table, int max_blocks_per_seq,
                               const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
                               int max_seqlen_q, int max_seqlen_k, int total_q,
-                              const float *sink, int batch, int num_qo_heads, int causal,
-                              int window_left, float sm_scale, float *lse_out, void *workspace,
-                              size_t workspace_bytes, int32_t *dev_error, void *stream);
+                              const float *sink, const float *alibi_slopes, int batch,
+                              int num_qo_heads, int causal, int window_left, float sm_scale,
+                              float *lse_out, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_error, void *stream);
 
 /*
  * varlen_prefill_contiguous: varlen_prefill with the keys and values of all
@@ -264,8 +270,9 @@ PKV_API pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const
                                                  const int32_t *cu_seq_lens_q,
                                                  const int32_t *cu_seq_lens_k, int max_seqlen_q,
                                                  int max_seqlen_k, int total_q, const float *sink,
-                                                 int batch, int num_qo_heads, int causal,
-                                                 int window_left, float sm_scale, float *lse_out,
+                                                 const float *alibi_slopes, int batch,
+                                                 int num_qo_heads, int causal, int window_left,
+                                                 float sm_scale, float *lse_out,
                                                  void *workspace, size_t workspace_bytes,
                                                  int32_t *dev_error, void *stream);
 
@@ -276,7 +283,8 @@ PKV_API pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const
  * must not allocate once it is running.  The pages have no counterpart: this
  * entry point exists only for such callers.
  *
- * It takes the same arguments as pkv_paged_decode minus the workspace.  The
+ * It takes the same arguments as pkv_paged_decode minus the workspace and
+ * minus alibi_slopes (no ALiBi bias).  The
  * split-KV scratch is instead a fixed device array inside the library of
  * PKV_NOALLOC_DECODE_SCRATCH_BYTES bytes; every GPU that loads the library
  * holds that array until the process exits.  A problem whose scratch need

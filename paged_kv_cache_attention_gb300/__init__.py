@@ -97,16 +97,16 @@ def load_library(path: Optional[str] = None):
         lib.pkv_reshape_and_cache.restype = i32
         lib.pkv_paged_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.pkv_paged_decode_workspace_size.restype = sz
-        lib.pkv_paged_decode.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, i32, i32, i32,
-                                         f32, i32, P, P, sz, P, P]
+        lib.pkv_paged_decode.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, P, i32, i32,
+                                         i32, f32, i32, P, P, sz, P, P]
         lib.pkv_paged_decode.restype = i32
         lib.pkv_varlen_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.pkv_varlen_prefill_workspace_size.restype = sz
         lib.pkv_varlen_prefill.argtypes = [P, P, P, P, CacheDesc, P, i32, P, P, i32, i32, i32, P,
-                                           i32, i32, i32, i32, f32, P, P, sz, P, P]
+                                           P, i32, i32, i32, i32, f32, P, P, sz, P, P]
         lib.pkv_varlen_prefill.restype = i32
         lib.pkv_varlen_prefill_contiguous.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, i32,
-                                                      i32, i32, P, i32, i32, i32, i32, f32, P,
+                                                      i32, i32, P, P, i32, i32, i32, i32, f32, P,
                                                       P, sz, P, P]
         lib.pkv_varlen_prefill_contiguous.restype = i32
         f64 = ctypes.c_double
@@ -174,6 +174,12 @@ def _cache_desc(k_cache, v_cache) -> CacheDesc:
              "k_cache and v_cache must have the same shape and dtype")
     nb, bs, hkv, d = k_cache.shape
     return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache.dtype))
+
+
+def _head_vector(name, t, Hq):
+    if t is not None:
+        _cuda_contig(name, t, _torch().float32, 1)
+        _require(t.shape[0] == Hq, f"{name} must have num_qo_heads entries")
 
 
 def paged_decode_workspace_size(batch: int, num_qo_heads: int, head_dim: int, max_seqlen: int,
@@ -287,13 +293,14 @@ def rope_reshape_and_cache(query, key, value, k_cache, v_cache, positions, slot_
 def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,
                  sink=None, window_left: int = -1, sm_scale: Optional[float] = None,
                  partition_size: int = 512, out=None, lse=None, workspace=None,
-                 dev_error=None, stream=None):
+                 dev_error=None, stream=None, alibi_slopes=None):
     """Single-token decode over the paged pools; returns out [B, Hq, D].
 
     q: [B, Hq, D] (dtype of the cache); block_table: [B, max_blocks] int32;
     cache_seqlens: [B] int32, the attended length (query at position L-1);
     max_seqlen: host int >= max(cache_seqlens); sink: [Hq] float32 or None;
-    lse: optional [B, Hq] float32 output (natural log, sink included).
+    lse: optional [B, Hq] float32 output (natural log, sink included);
+    alibi_slopes: [Hq] float32 or None (bias slope * (j - (L - 1))).
     """
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache)
@@ -307,6 +314,7 @@ def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: in
     if sink is not None:
         _cuda_contig("sink", sink, torch.float32, 1)
         _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
+    _head_vector("alibi_slopes", alibi_slopes, Hq)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -320,7 +328,8 @@ def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: in
     ws = _workspace(need, q.device, workspace)
     st = load_library().pkv_paged_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
-        block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink), B, Hq,
+        block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink),
+        _ptr(alibi_slopes), B, Hq,
         int(window_left), scale, int(partition_size), _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
     _check("pkv_paged_decode", st)
@@ -330,7 +339,7 @@ def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: in
 def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_k,
                    max_seqlen_q: int, max_seqlen_k: int, sink=None, causal: bool = True,
                    window_left: int = -1, sm_scale: Optional[float] = None, out=None, lse=None,
-                   workspace=None, dev_error=None, stream=None):
+                   workspace=None, dev_error=None, stream=None, alibi_slopes=None):
     """Varlen / chunk prefill over the paged pools; returns out [total_q, Hq, D].
 
     q: [total_q, Hq, D] bf16; cu_seq_lens_q / cu_seq_lens_k: [B+1] int32;
@@ -351,6 +360,7 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
     if sink is not None:
         _cuda_contig("sink", sink, torch.float32, 1)
         _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
+    _head_vector("alibi_slopes", alibi_slopes, Hq)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -365,7 +375,8 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
     st = load_library().pkv_varlen_prefill(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
         block_table.shape[1], _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), int(max_seqlen_q),
-        int(max_seqlen_k), int(total_q), _ptr(sink), B, Hq, int(bool(causal)),
+        int(max_seqlen_k), int(total_q), _ptr(sink), _ptr(alibi_slopes), B, Hq,
+        int(bool(causal)),
         int(window_left), scale, _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
         _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill", st)
@@ -375,7 +386,8 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
 def varlen_prefill_contiguous(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_seqlen_q: int,
                               max_seqlen_k: int, sink=None, causal: bool = True,
                               window_left: int = -1, sm_scale: Optional[float] = None, out=None,
-                              lse=None, workspace=None, dev_error=None, stream=None):
+                              lse=None, workspace=None, dev_error=None, stream=None,
+                              alibi_slopes=None):
     """Varlen prefill with contiguous keys: request r's keys and values are
     rows cu_seq_lens_k[r] .. cu_seq_lens_k[r+1]-1 of k and v ([total_k, Hkv, D]
     bf16).  Otherwise as varlen_prefill; returns out [total_q, Hq, D]."""
@@ -394,6 +406,7 @@ def varlen_prefill_contiguous(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_seqlen_
     if sink is not None:
         _cuda_contig("sink", sink, torch.float32, 1)
         _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
+    _head_vector("alibi_slopes", alibi_slopes, Hq)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -408,7 +421,8 @@ def varlen_prefill_contiguous(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_seqlen_
     st = load_library().pkv_varlen_prefill_contiguous(
         _ptr(out), _ptr(q), _ptr(k) if total_k else None, _ptr(v) if total_k else None,
         int(total_k), Hkv, D, _dtype_code(q.dtype), _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k),
-        int(max_seqlen_q), int(max_seqlen_k), int(total_q), _ptr(sink), B, Hq,
+        int(max_seqlen_q), int(max_seqlen_k), int(total_q), _ptr(sink), _ptr(alibi_slopes), B,
+        Hq,
         int(bool(causal)), int(window_left), scale, _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill_contiguous", st)
@@ -446,7 +460,8 @@ def paged_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, max_se
         out = torch.empty_like(q)
     scale = float(sm_scale) if sm_scale is not None else D ** -0.5
     st = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
-            block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink), B, Hq,
+            block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink),
+        _ptr(alibi_slopes), B, Hq,
             int(window_left), scale, int(partition_size), _ptr(lse), _ptr(dev_error),
             _stream_handle(stream))
     _check("pkv_paged_decode_noalloc", st)

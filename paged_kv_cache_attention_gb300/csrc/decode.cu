@@ -221,14 +221,17 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
         for (int mt = 0; mt < DK; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) oacc[ht][mt][e] = 0.f;
-    float m_run[NHT], l_run[NHT];
+    float m_run[NHT], l_run[NHT], al2[NHT];
     bool head_ok[NHT];
 #pragma unroll
     for (int ht = 0; ht < NHT; ++ht) {
         m_run[ht] = kNegInf;
         l_run[ht] = 0.f;
         head_ok[ht] = ht * 8 + gq < G;
+        // ALiBi slope of this lane's head row, in log2 units (0: no bias)
+        al2[ht] = (p.alibi && head_ok[ht]) ? p.alibi[g * G + ht * 8 + gq] * kLog2e : 0.f;
     }
+    const int qpos = L - 1;  // the decode query's position
 
     int consumed = 0;
     for (int j = 0; j < nmine; ++j) {
@@ -283,7 +286,10 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
                     for (int e = 0; e < 2; ++e) {
                         const int tok = tok0 + nt * 8 + 2 * tq + e;
                         const bool ok = head_ok[ht] && tok >= tok_lo && tok < tok_hi;
-                        const float sv = ok ? sacc[nt][2 * ht + e] * p.scale_log2 : kNegInf;
+                        const float sv =
+                            ok ? fmaf(sacc[nt][2 * ht + e], p.scale_log2,
+                                      al2[ht] * (float)(tok - qpos))
+                               : kNegInf;
                         sacc[nt][2 * ht + e] = sv;
                         mx = fmaxf(mx, sv);
                     }
@@ -458,7 +464,8 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
                 part_dot += __shfl_xor_sync(0xffffffffu, part_dot, off);
-            const float s = part_dot * p.scale_log2;
+            const float bias = p.alibi ? p.alibi[g * G + h] * kLog2e * (float)(tok - (L - 1)) : 0.f;
+            const float s = fmaf(part_dot, p.scale_log2, bias);
             const float m_new = fmaxf(m[h], s);
             const float alpha = exp2f(m[h] - m_new);
             const float pe = exp2f(s - m_new);

@@ -48,7 +48,8 @@ extern "C" pkv_status pkv_paged_decode_noalloc(
     const pkv_status st = scratch_address(&scratch);
     if (st != PKV_OK) return st;
     return pkv_paged_decode(out, q, k_cache, v_cache, cache, block_table, max_blocks_per_seq,
-                            cache_seqlens, max_seqlen, sink, batch, num_qo_heads, window_left,
+                            cache_seqlens, max_seqlen, sink, /*alibi_slopes=*/nullptr, batch,
+                            num_qo_heads, window_left,
                             sm_scale, partition_size, lse_out, scratch,
                             PKV_NOALLOC_DECODE_SCRATCH_BYTES, dev_error, stream);
 }

@@ -165,7 +165,7 @@ const char *pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return 200; }
 
 pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                  void *v_cache, const int64_t *slot_mapping, int64_t num_tokens,
@@ -259,10 +259,10 @@ size_t pkv_paged_decode_workspace_size(int batch, int num_qo_heads, int head_dim
 pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
                             pkv_cache_desc cache, const int32_t *block_table,
                             int max_blocks_per_seq, const int32_t *cache_seqlens,
-                            int max_seqlen, const float *sink, int batch, int num_qo_heads,
-                            int window_left, float sm_scale, int partition_size,
-                            float *lse_out, void *workspace, size_t workspace_bytes,
-                            int32_t *dev_error, void *stream) {
+                            int max_seqlen, const float *sink, const float *alibi_slopes,
+                            int batch, int num_qo_heads, int window_left, float sm_scale,
+                            int partition_size, float *lse_out, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_error, void *stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if (batch < 0 || batch > 65535 || num_qo_heads <= 0 || max_seqlen < 0 ||
@@ -295,6 +295,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
     p.block_table = block_table;
     p.seqlens = cache_seqlens;
     p.sink = sink;
+    p.alibi = alibi_slopes;
     p.lse_out = lse_out;
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.lse_off);
     p.part_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.o_off);
@@ -348,7 +349,8 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
                        const int32_t *block_table, int max_blocks_per_seq,
                        const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
                        int max_seqlen_q, int max_seqlen_k, int total_q, const float *sink,
-                       int batch, int num_qo_heads, int causal, int window_left, float sm_scale,
+                       const float *alibi_slopes, int batch, int num_qo_heads, int causal,
+                       int window_left, float sm_scale,
                        float *lse_out, void *workspace, size_t workspace_bytes,
                        int32_t *dev_error, void *stream) {
     if (cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
@@ -380,6 +382,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
     p.cu_q = cu_seq_lens_q;
     p.cu_k = cu_seq_lens_k;
     p.sink = sink;
+    p.alibi = alibi_slopes;
     p.lse_out = lse_out;
     p.tiles = static_cast<int32_t *>(workspace);
     p.dev_error = dev_error;
@@ -431,16 +434,17 @@ pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
                               const int32_t *block_table, int max_blocks_per_seq,
                               const int32_t *cu_seq_lens_q, const int32_t *cu_seq_lens_k,
                               int max_seqlen_q, int max_seqlen_k, int total_q,
-                              const float *sink, int batch, int num_qo_heads, int causal,
-                              int window_left, float sm_scale, float *lse_out, void *workspace,
-                              size_t workspace_bytes, int32_t *dev_error, void *stream) {
+                              const float *sink, const float *alibi_slopes, int batch,
+                              int num_qo_heads, int causal, int window_left, float sm_scale,
+                              float *lse_out, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_error, void *stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     return prefill_run(out, q, k_cache, v_cache, cache, false,
                        cache.num_blocks * cache.block_size, block_table, max_blocks_per_seq,
                        cu_seq_lens_q, cu_seq_lens_k, max_seqlen_q, max_seqlen_k, total_q, sink,
-                       batch, num_qo_heads, causal, window_left, sm_scale, lse_out, workspace,
-                       workspace_bytes, dev_error, stream);
+                       alibi_slopes, batch, num_qo_heads, causal, window_left, sm_scale,
+                       lse_out, workspace, workspace_bytes, dev_error, stream);
 }
 
 pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k, const void *v,
@@ -448,10 +452,11 @@ pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k
                                          const int32_t *cu_seq_lens_q,
                                          const int32_t *cu_seq_lens_k, int max_seqlen_q,
                                          int max_seqlen_k, int total_q, const float *sink,
-                                         int batch, int num_qo_heads, int causal,
-                                         int window_left, float sm_scale, float *lse_out,
-                                         void *workspace, size_t workspace_bytes,
-                                         int32_t *dev_error, void *stream) {
+                                         const float *alibi_slopes, int batch,
+                                         int num_qo_heads, int causal, int window_left,
+                                         float sm_scale, float *lse_out, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_error,
+                                         void *stream) {
     if (total_k < 0 || num_kv_heads <= 0 || head_dim <= 0) return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     pkv_cache_desc cache;
@@ -462,9 +467,9 @@ pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k
     cache.dtype = dtype;
     return prefill_run(out, q, k, v, cache, true, total_k,
                        nullptr, max_seqlen_k / 128 + 2, cu_seq_lens_q, cu_seq_lens_k,
-                       max_seqlen_q, max_seqlen_k, total_q, sink, batch, num_qo_heads, causal,
-                       window_left, sm_scale, lse_out, workspace, workspace_bytes, dev_error,
-                       stream);
+                       max_seqlen_q, max_seqlen_k, total_q, sink, alibi_slopes, batch,
+                       num_qo_heads, causal, window_left, sm_scale, lse_out, workspace,
+                       workspace_bytes, dev_error, stream);
 }
 
 }  // extern "C"

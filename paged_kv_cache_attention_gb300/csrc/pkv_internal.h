@@ -20,6 +20,7 @@ struct DecodeParams {
     const int32_t *block_table;  // [B, max_blocks_per_seq]
     const int32_t *seqlens;      // [B]
     const float *sink;           // [Hq] or nullptr
+    const float *alibi;          // [Hq] ALiBi slopes or nullptr
     float *lse_out;              // [B, Hq] or nullptr
     float *part_lse;             // [B, Hq, num_parts] (log2 units)
     float *part_o;               // [B, Hq, num_parts, D], normalised partial outputs
@@ -42,6 +43,7 @@ struct PrefillParams {
     const int32_t *cu_q;           // [B+1]
     const int32_t *cu_k;           // [B+1]
     const float *sink;             // [Hq] or nullptr
+    const float *alibi;            // [Hq] ALiBi slopes or nullptr
     float *lse_out;                // [total_q, Hq] or nullptr
     int32_t *tiles;                // work list, built on the device
     int32_t *dev_error;

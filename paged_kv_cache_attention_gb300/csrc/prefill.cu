@@ -8,7 +8,9 @@
 // block_table; the per-head sink joins the softmax denominator (FlashInfer
 // sink_attention_reference.py, varlen branch and sink_softmax).  Without the
 // causal bound a row keeps every key at or after position - window_left (the
-// same reference's non-causal varlen mask).  The contiguous form reads request
+// same reference's non-causal varlen mask).  With ALiBi slopes the scaled
+// logit of key j gains slope[head] * (j - position) (vLLM attention.py,
+// PagedAttentionWithALiBi).  The contiguous form reads request
 // r's keys from rows cu_k[r] .. cu_k[r+1]-1 of [total_k, Hkv, D] arrays, as in
 // the docs' varlen path.
 //
@@ -261,8 +263,9 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
 // the attention kernel
 // ---------------------------------------------------------------------------
 // BS: rows per page of the paged pools; CONTIG: K/V are contiguous rows
-// addressed by cu_k (then BS = 128, one box per 64-dim half per tile).
-template <int BS, bool CONTIG>
+// addressed by cu_k (then BS = 128, one box per 64-dim half per tile);
+// ALIBI: the logits gain slope[head] * (key - position).
+template <int BS, bool CONTIG, bool ALIBI>
 __global__ void __launch_bounds__(PfLayout::THREADS, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -484,6 +487,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         float *xl = reinterpret_cast<float *>(smem + Lay::OFF_XL);
         const float sl2 = p.scale_log2;
         const int wl = p.window_left;
+        // ALiBi slope of this row's head in log2 units
+        const float al2 = ALIBI ? p.alibi[head] * kLog2e : 0.f;
 
         float m_run = kNegInf, l_run = 0.f;
         bool alive = true;
@@ -502,6 +507,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             tc::ld_32x32b_x32(tS, ra);
             tc::ld_32x32b_x32(tS + 32, rb);
             tc::wait_ld();
+            if constexpr (ALIBI) {
+                // x = s * scale + slope * (key - position), log2 units; the
+                // softmax below then runs on x with unit scale
+                const float b0 = al2 * (float)(key0 - qpos);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    ra[i] = __float_as_uint(
+                        fmaf(__uint_as_float(ra[i]), sl2, fmaf((float)i, al2, b0)));
+                    rb[i] = __float_as_uint(
+                        fmaf(__uint_as_float(rb[i]), sl2, fmaf((float)(i + 32), al2, b0)));
+                }
+            }
             if (!full) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -522,7 +539,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             slot[hc] = mine;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             const float mx = fmaxf(mine, slot[hc ^ 1]);
-            const float m_tile = mx * sl2;
+            const float m_tile = ALIBI ? mx : mx * sl2;
             const bool grow = m_tile > m_run + kRescaleThreshold;
             // tcgen05.ld/st are warp-collective: the warp rescales together,
             // lanes whose maximum did not grow enough multiply by 1
@@ -545,7 +562,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             }
             // P = 2^(s * scale - m) as bf16 (masked keys hold -inf: 2^-inf = 0)
             const float msub = m_run == kNegInf ? 0.f : m_run;
-            const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(-msub, -msub);
+            const float psc = ALIBI ? 1.f : sl2;  // x is already scaled with ALiBi
+            const uint64_t scale2 = f2_pack(psc, psc), neg2 = f2_pack(-msub, -msub);
             uint64_t ps2[2] = {0ull, 0ull};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -651,9 +669,15 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, 
         kern<<<grid, PfLayout::THREADS, PfLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k, *tmap_v);
         return cudaGetLastError();
     };
-    if (contiguous) return go(prefill_tc_kernel<kTileN, true>);
-    if (cache.block_size == 16) return go(prefill_tc_kernel<16, false>);
-    if (cache.block_size == 32) return go(prefill_tc_kernel<32, false>);
+    if (p.alibi) {
+        if (contiguous) return go(prefill_tc_kernel<kTileN, true, true>);
+        if (cache.block_size == 16) return go(prefill_tc_kernel<16, false, true>);
+        if (cache.block_size == 32) return go(prefill_tc_kernel<32, false, true>);
+    } else {
+        if (contiguous) return go(prefill_tc_kernel<kTileN, true, false>);
+        if (cache.block_size == 16) return go(prefill_tc_kernel<16, false, false>);
+        if (cache.block_size == 32) return go(prefill_tc_kernel<32, false, false>);
+    }
     return cudaErrorNotSupported;
 }
 

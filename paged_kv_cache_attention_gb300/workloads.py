@@ -138,6 +138,7 @@ class DecodeCase:
     window_left: int
     sm_scale: float
     partition_size: int = 512
+    alibi: Optional[torch.Tensor] = None  # float32 [Hq] ALiBi slopes or None
 
     @property
     def batch(self):
@@ -165,6 +166,7 @@ class VarlenCase:
     window_left: int
     sm_scale: float
     causal: bool = True
+    alibi: Optional[torch.Tensor] = None  # float32 [Hq] ALiBi slopes or None
 
     @property
     def batch(self):
@@ -200,8 +202,9 @@ def cumsum0(lens: torch.Tensor) -> torch.Tensor:
 def make_decode(lens, num_qo_heads, num_kv_heads, head_dim, block_size, dtype, seed,
                 sink: str = "none", window_left: int = -1, sm_scale: Optional[float] = None,
                 spare: int = 64, partition_size: int = 512, name: str = "decode",
-                extra_blocks_per_seq: int = 0) -> DecodeCase:
-    """A decode batch over a shuffled pool.  sink: 'none' | 'randn' | 'zero'."""
+                extra_blocks_per_seq: int = 0, alibi: str = "none") -> DecodeCase:
+    """A decode batch over a shuffled pool.  sink: 'none' | 'randn' | 'zero';
+    alibi: 'none' | 'geometric' | 'uniform' (see alibi_slopes)."""
     gen = _gen(seed)
     lens = [int(x) for x in lens]
     pc = [pages_for(L, block_size) + extra_blocks_per_seq for L in lens]
@@ -211,7 +214,20 @@ def make_decode(lens, num_qo_heads, num_kv_heads, head_dim, block_size, dtype, s
     scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(head_dim)
     return DecodeCase(name, q, pool.k_cache, pool.v_cache, pool.block_tables[0],
                       torch.tensor(lens, dtype=torch.int32), sk, window_left, scale,
-                      partition_size)
+                      partition_size, alibi_slopes(alibi, num_qo_heads, gen))
+
+
+def alibi_slopes(kind: str, n: int, gen) -> Optional[torch.Tensor]:
+    """ALiBi slopes for n query heads: 'geometric' = the ALiBi paper's
+    2^(-8 (i+1) / n); 'uniform' = seeded U[0.01, 1] (steep and shallow heads
+    mixed); 'none' = no bias."""
+    if kind == "none":
+        return None
+    if kind == "geometric":
+        return torch.tensor([2.0 ** (-8.0 * (i + 1) / n) for i in range(n)], dtype=torch.float32)
+    if kind == "uniform":
+        return (torch.rand(n, generator=gen, dtype=torch.float32) * 0.99 + 0.01)
+    raise ValueError(kind)
 
 
 def _make_sink(kind: str, n: int, gen) -> Optional[torch.Tensor]:
@@ -227,7 +243,7 @@ def _make_sink(kind: str, n: int, gen) -> Optional[torch.Tensor]:
 def make_varlen(q_lens, prefix_lens, num_qo_heads, num_kv_heads, head_dim, block_size,
                 dtype, seed, sink: str = "randn", window_left: int = -1,
                 sm_scale: Optional[float] = None, spare: int = 64, causal: bool = True,
-                name: str = "varlen") -> VarlenCase:
+                name: str = "varlen", alibi: str = "none") -> VarlenCase:
     """A varlen chunk-prefill batch: request r has q_lens[r] new queries over
     prefix_lens[r] cached tokens plus the new tokens themselves (kv_len =
     prefix + q_len), all already in the pool."""
@@ -241,13 +257,14 @@ def make_varlen(q_lens, prefix_lens, num_qo_heads, num_kv_heads, head_dim, block
     sk = _make_sink(sink, num_qo_heads, gen)
     scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(head_dim)
     return VarlenCase(name, q, pool.k_cache, pool.v_cache, pool.block_tables[0],
-                      cumsum0(ql), cumsum0(kvl), sk, window_left, scale, causal)
+                      cumsum0(ql), cumsum0(kvl), sk, window_left, scale, causal,
+                      alibi_slopes(alibi, num_qo_heads, gen))
 
 
 def make_varlen_kv(q_lens, kv_lens, num_qo_heads, num_kv_heads, head_dim, block_size, dtype,
                    seed, sink: str = "randn", window_left: int = -1,
                    sm_scale: Optional[float] = None, spare: int = 64, causal: bool = True,
-                   name: str = "varlen") -> VarlenCase:
+                   name: str = "varlen", alibi: str = "none") -> VarlenCase:
     """A varlen batch with explicit per-request kv lengths (q_len may exceed
     kv_len; such rows sit at negative positions and attend to nothing)."""
     gen = _gen(seed)
@@ -259,7 +276,8 @@ def make_varlen_kv(q_lens, kv_lens, num_qo_heads, num_kv_heads, head_dim, block_
     sk = _make_sink(sink, num_qo_heads, gen)
     scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(head_dim)
     return VarlenCase(name, q, pool.k_cache, pool.v_cache, pool.block_tables[0],
-                      cumsum0(ql), cumsum0(kvl), sk, window_left, scale, causal)
+                      cumsum0(ql), cumsum0(kvl), sk, window_left, scale, causal,
+                      alibi_slopes(alibi, num_qo_heads, gen))
 
 
 @dataclass

@@ -33,7 +33,7 @@ def gpu_decode(case, partition_size=None, with_lse=False, err=None, max_seqlen=N
                            sink=to_dev(case.sink), window_left=case.window_left,
                            sm_scale=case.sm_scale,
                            partition_size=partition_size or case.partition_size, lse=lse,
-                           dev_error=err)
+                           dev_error=err, alibi_slopes=to_dev(case.alibi))
     torch.cuda.synchronize()
     o = out.float().cpu().numpy()
     return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
@@ -44,7 +44,8 @@ def oracle_decode(case, rows=None, with_lse=False):
         W.to_oracle(case.q), W.to_oracle(case.k_cache), W.to_oracle(case.v_cache),
         case.block_table.numpy(), case.cache_seqlens.numpy(),
         sink=None if case.sink is None else case.sink.numpy(), window_left=case.window_left,
-        sm_scale=case.sm_scale, rows=rows, with_lse=with_lse)
+        sm_scale=case.sm_scale, rows=rows, with_lse=with_lse,
+        alibi_slopes=None if case.alibi is None else case.alibi.numpy())
 
 
 def gpu_prefill(case, with_lse=False, err=None):
@@ -56,7 +57,7 @@ def gpu_prefill(case, with_lse=False, err=None):
                              to_dev(case.cu_seq_lens_k), case.max_seqlen_q, case.max_seqlen_k,
                              sink=to_dev(case.sink), causal=case.causal,
                              window_left=case.window_left, sm_scale=case.sm_scale, lse=lse,
-                             dev_error=err)
+                             dev_error=err, alibi_slopes=to_dev(case.alibi))
     torch.cuda.synchronize()
     o = out.float().cpu().numpy()
     return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
@@ -86,7 +87,7 @@ def gpu_prefill_contiguous(case, k, v, with_lse=False, err=None):
         to_dev(case.q), to_dev(k), to_dev(v), to_dev(case.cu_seq_lens_q),
         to_dev(case.cu_seq_lens_k), case.max_seqlen_q, case.max_seqlen_k,
         sink=to_dev(case.sink), causal=case.causal, window_left=case.window_left,
-        sm_scale=case.sm_scale, lse=lse, dev_error=err)
+        sm_scale=case.sm_scale, lse=lse, dev_error=err, alibi_slopes=to_dev(case.alibi))
     torch.cuda.synchronize()
     o = out.float().cpu().numpy()
     return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
@@ -97,7 +98,8 @@ def oracle_prefill(case, rows=None, with_lse=False):
         W.to_oracle(case.q), W.to_oracle(case.k_cache), W.to_oracle(case.v_cache),
         case.block_table.numpy(), case.cu_seq_lens_q.numpy(), case.kv_lens.numpy(),
         sink=None if case.sink is None else case.sink.numpy(), causal=case.causal,
-        window_left=case.window_left, sm_scale=case.sm_scale, rows=rows, with_lse=with_lse)
+        window_left=case.window_left, sm_scale=case.sm_scale, rows=rows, with_lse=with_lse,
+        alibi_slopes=None if case.alibi is None else case.alibi.numpy())
 
 
 def max_abs(a, b):

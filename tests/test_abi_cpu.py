@@ -73,7 +73,7 @@ def _desc(nb=64, bs=16, hkv=8, d=128, dtype=1):
 def _decode(lib, desc=None, batch=4, hq=32, window=-1, part=512, ws_bytes=1 << 30,
             ws=FAKE, q=FAKE, max_blocks=8, max_seqlen=128, scale=0.1):
     return lib.pkv_paged_decode(FAKE, q, FAKE, FAKE, desc or _desc(), FAKE, max_blocks, FAKE,
-                                max_seqlen, None, batch, hq, window, scale, part, None, ws,
+                                max_seqlen, None, None, batch, hq, window, scale, part, None, ws,
                                 ws_bytes, None, None)
 
 
@@ -128,7 +128,7 @@ def test_prefill_validation(change, expected):
     a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30, window=-1)
     a.update(change)
     st = lib.pkv_varlen_prefill(FAKE, FAKE, FAKE, FAKE, _desc(dtype=a["dtype"]), FAKE, 8, FAKE,
-                                FAKE, 64, 128, a["total_q"], None, 2, a["hq"], a["causal"],
+                                FAKE, 64, 128, a["total_q"], None, None, 2, a["hq"], a["causal"],
                                 a["window"], 0.1, None, FAKE, a["ws_bytes"], None, None)
     assert st == expected
 
@@ -153,7 +153,8 @@ def test_prefill_contiguous_validation(change, expected):
     a.update(change)
     st = lib.pkv_varlen_prefill_contiguous(
         FAKE, FAKE, a["k"], FAKE, a["total_k"], a["hkv"], a["d"], a["dtype"], FAKE, FAKE, 64,
-        128, a["total_q"], None, 2, a["hq"], 1, -1, 0.1, None, FAKE, a["ws_bytes"], None, None)
+        128, a["total_q"], None, None, 2, a["hq"], 1, -1, 0.1, None, FAKE, a["ws_bytes"], None,
+        None)
     assert st == expected
 
 

@@ -196,3 +196,49 @@ def test_config5_decode_half_after_cache_write():
     rows = list(range(0, 256, 17))
     ref = oracle_decode(dec, rows=rows)
     assert max_abs(got[rows], ref) <= TOL[torch.bfloat16]
+
+
+# ---------------------------------------------------------------------------
+# ALiBi
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(32, 8, 128, 16), (16, 16, 64, 32), (32, 2, 128, 16),
+                                         (6, 2, 64, 16)])
+@pytest.mark.parametrize("alibi", ["geometric", "uniform"])
+def test_alibi_bf16(Hq, Hkv, D, bs, alibi):
+    lens = [1, 17, 511, 513, 1500, 4096]
+    case = W.make_decode(lens, Hq, Hkv, D, bs, torch.bfloat16, seed=Hq + D + bs + 5,
+                         sink="randn", alibi=alibi)
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("window,part", [(-1, 64), (100, 512), (1000, 16384)])
+def test_alibi_windows_and_partitions(window, part):
+    case = W.make_decode([3, 700, 2049, 5000], 32, 8, 128, 16, torch.bfloat16, seed=window + 41,
+                         sink="randn", window_left=window, alibi="uniform")
+    got = gpu_decode(case, partition_size=part)
+    assert max_abs(got, oracle_decode(case)) <= TOL[torch.bfloat16]
+
+
+def test_alibi_fp32_path():
+    case = W.make_decode([1, 31, 70, 300], 4, 2, 64, 32, torch.float32, seed=42, sink="randn",
+                         alibi="uniform")
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.float32]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.float32]
+
+
+def test_alibi_long_context_sampled():
+    """Slopes as shallow as 2^-8 over 32K-128K keys: the bias spans hundreds of
+    log2 units and the fp32 distance arithmetic must stay exact enough."""
+    gen = torch.Generator().manual_seed(43)
+    lens = torch.randint(32768, 131072, (4,), generator=gen).tolist()
+    case = W.make_decode(lens, 64, 8, 64, 16, torch.bfloat16, seed=43, sink="randn",
+                         alibi="geometric")
+    got = gpu_decode(case)
+    ref = oracle_decode(case, rows=[0, 3])
+    assert max_abs(got[[0, 3]], ref) <= TOL[torch.bfloat16]

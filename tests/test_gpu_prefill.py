@@ -171,6 +171,48 @@ def test_contiguous_rows_past_the_arrays_are_flagged():
     assert max_abs(got[:40], ref) <= TOL[BF16]
 
 
+# ---------------------------------------------------------------------------
+# ALiBi
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("window,sink,alibi", [(-1, "randn", "geometric"), (-1, "none", "uniform"),
+                                               (127, "randn", "uniform"), (0, "randn", "geometric")])
+def test_alibi_prefill(causal, window, sink, alibi):
+    q_lens = [200, 1, 513, 64, 300]
+    kv_lens = [500, 2001, 513, 64, 40]
+    case = W.make_varlen_kv(q_lens, kv_lens, 32, 8, 128, 16, BF16, seed=window + 110,
+                            sink=sink, window_left=window, causal=causal, alibi=alibi)
+    _check(case)
+
+
+@pytest.mark.parametrize("G,Hkv,bs", [(1, 8, 32), (4, 4, 16), (16, 1, 16)])
+def test_alibi_prefill_group_sizes(G, Hkv, bs):
+    case = W.make_varlen([1, 33, 129, 250], [0, 300, 128, 1000], G * Hkv, Hkv, 128, bs, BF16,
+                         seed=G * 17 + bs, sink="randn", alibi="uniform")
+    _check(case)
+
+
+def test_alibi_contiguous():
+    case = W.make_varlen_kv([5, 127, 300], [5, 1000, 300], 32, 8, 128, 16, BF16, seed=120,
+                            sink="randn", alibi="geometric", causal=False)
+    _check_contig(case, pad_rows=64)
+
+
+def test_alibi_decode_equals_prefill_with_one_query():
+    dec = W.make_decode([1, 300, 1024, 4097], 32, 8, 128, 16, BF16, seed=121, sink="randn",
+                        window_left=700, alibi="uniform")
+    B = dec.batch
+    var = W.VarlenCase("as-prefill", dec.q, dec.k_cache, dec.v_cache, dec.block_table,
+                       W.cumsum0(torch.ones(B, dtype=torch.int32)),
+                       W.cumsum0(dec.cache_seqlens), dec.sink, dec.window_left, dec.sm_scale,
+                       True, dec.alibi)
+    a = gpu_decode(dec)
+    b = gpu_prefill(var)
+    assert np.abs(a - b).max() <= 2e-2
+    assert max_abs(b, oracle_decode(dec)) <= TOL[BF16]
+
+
 def test_decode_equals_prefill_with_one_query():
     """Cross-op: paged_decode == varlen_prefill with q_len = 1 per request."""
     dec = W.make_decode([1, 300, 1024, 4097], 32, 8, 128, 16, BF16, seed=23, sink="randn",
