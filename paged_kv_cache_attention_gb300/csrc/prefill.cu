@@ -306,6 +306,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     const int ntiles = geo.ntiles;
     const int last_key_end = (geo.kt_lo + ntiles) * kTileN;
     const bool tail = ntiles > 0 && last_key_end > geo.kv_len;
+    // Key tiles in processing order.  With ALiBi they run from the query's end
+    // backwards: the nearest keys carry the largest bias, so the first tile
+    // usually holds the row maximum and its P = 2^0 is exact in bf16.
+    auto tile_of = [&](int j) { return ALIBI ? ntiles - 1 - j : j; };  // offset from kt_lo
+    auto is_tail = [&](int j) { return tail && tile_of(j) == ntiles - 1; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -329,8 +334,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             for (int j = 0; j < ntiles && alive; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = (j >> 1) & 1;
-                const int key0 = (geo.kt_lo + j) * kTileN;
-                const int rel = j * NPG;
+                const int key0 = (geo.kt_lo + tile_of(j)) * kTileN;
+                const int rel = tile_of(j) * NPG;
                 if (!CONTIG && (rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
                     ids_batch = rel >> 5;
                     const int pg = pg0 + ids_batch * 32 + lane;
@@ -365,7 +370,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                     tma_load_3d(sV + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmv,
                                 bar(Lay::B_VFULL + s), h * 64, geo.g, row);
                 }
-                if (j == ntiles - 1 && tail) {
+                if (is_tail(j)) {
                     // rows at or past kv_len of the last value tile may hold any
                     // bits: zero them so P = 0 never meets a non-finite value
                     alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
@@ -425,7 +430,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                     if (!alive) break;
                     tc::fence_after_sync();
                     if (x == 0) {
-                        if (j == ntiles - 1 && tail)
+                        if (is_tail(j))
                             alive = mbar_wait_bounded(bar(Lay::B_VFIX), 0, p.dev_error);
                         else
                             alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
@@ -497,7 +502,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                                mbar_wait_bounded(bar(Lay::B_SFULL + x), j & 1, p.dev_error));
             if (!alive) break;
             tc::fence_after_sync();
-            const int key0 = (geo.kt_lo + j) * kTileN + hc * 64;  // first key of this half
+            const int key0 = (geo.kt_lo + tile_of(j)) * kTileN + hc * 64;  // first key of this half
             const bool full = (key0 + 63 <= cpos) && (key0 + 64 <= geo.kv_len) &&
                               (wl < 0 || key0 >= qpos - wl);
             // keys this row keeps: [klo, khi] (inclusive), relative to key0
@@ -507,18 +512,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             tc::ld_32x32b_x32(tS, ra);
             tc::ld_32x32b_x32(tS + 32, rb);
             tc::wait_ld();
-            if constexpr (ALIBI) {
-                // x = s * scale + slope * (key - position), log2 units; the
-                // softmax below then runs on x with unit scale
-                const float b0 = al2 * (float)(key0 - qpos);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    ra[i] = __float_as_uint(
-                        fmaf(__uint_as_float(ra[i]), sl2, fmaf((float)i, al2, b0)));
-                    rb[i] = __float_as_uint(
-                        fmaf(__uint_as_float(rb[i]), sl2, fmaf((float)(i + 32), al2, b0)));
-                }
-            }
+            // ALiBi bias of this half's first key, log2 units
+            const float b0 = ALIBI ? al2 * (float)(key0 - qpos) : 0.f;
             if (!full) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -526,21 +521,53 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                     if (!(i + 32 <= khi && i + 32 >= klo)) rb[i] = __float_as_uint(kNegInf);
                 }
             }
-            float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+            float mine;
+            if constexpr (ALIBI) {
+                // x = s * scale + slope * (key - position) in place, log2
+                // units, as packed pairs: the bias pairs of columns (4k, 4k+1)
+                // and (4k+2, 4k+3) come from two chains stepping by 4 slope.
+                // The maximum is then exact (the row's largest P is 2^0 when
+                // it sets a fresh maximum, exact in bf16).
+                const uint64_t sc2 = f2_pack(sl2, sl2), step2 = f2_pack(4.f * al2, 4.f * al2);
+                uint64_t bc[2] = {f2_pack(b0, b0 + al2), f2_pack(b0 + 2.f * al2, b0 + 3.f * al2)};
+                float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                mx4[i & 1] = fmax3(mx4[i & 1], __uint_as_float(ra[2 * i]),
-                                   __uint_as_float(ra[2 * i + 1]));
-                mx4[2 + (i & 1)] = fmax3(mx4[2 + (i & 1)], __uint_as_float(rb[2 * i]),
-                                         __uint_as_float(rb[2 * i + 1]));
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t *src = hh ? rb : ra;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * i]),
+                                                 __uint_as_float(src[2 * i + 1])),
+                                         sc2, bc[i & 1]),
+                                  x0, x1);
+                        bc[i & 1] = f2_add(bc[i & 1], step2);
+                        src[2 * i] = __float_as_uint(x0);
+                        src[2 * i + 1] = __float_as_uint(x1);
+                        mx4[2 * hh + (i & 1)] = fmax3(mx4[2 * hh + (i & 1)], x0, x1);
+                    }
+                }
+                mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
+            } else {
+                float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    mx4[i & 1] = fmax3(mx4[i & 1], __uint_as_float(ra[2 * i]),
+                                       __uint_as_float(ra[2 * i + 1]));
+                    mx4[2 + (i & 1)] = fmax3(mx4[2 + (i & 1)], __uint_as_float(rb[2 * i]),
+                                             __uint_as_float(rb[2 * i + 1]));
+                }
+                mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             }
-            const float mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             float *slot = xmax + (((j & 1) * kNQ + x) * 128 + row) * 2;
             slot[hc] = mine;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             const float mx = fmaxf(mine, slot[hc ^ 1]);
-            const float m_tile = ALIBI ? mx : mx * sl2;
-            const bool grow = m_tile > m_run + kRescaleThreshold;
+            const float m_tile = ALIBI ? mx : mx * sl2;  // ALiBi rows hold scaled x already
+            // Lazy rescale: O is rescaled only when the maximum grows by more
+            // than the threshold.  ALiBi rescales on any growth, so the row's
+            // largest P stays 2^0 (see the tile order above).
+            const bool grow = m_tile > m_run + (ALIBI ? 0.f : kRescaleThreshold);
             // tcgen05.ld/st are warp-collective: the warp rescales together,
             // lanes whose maximum did not grow enough multiply by 1
             if (__any_sync(0xffffffffu, grow)) {
@@ -560,9 +587,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 }
                 if (grow) m_run = m_tile;
             }
-            // P = 2^(s * scale - m) as bf16 (masked keys hold -inf: 2^-inf = 0)
+            // P = 2^(s * scale - m) as bf16 (masked keys hold -inf:
+            // 2^-inf = 0); with ALiBi the row already holds x = s * scale +
+            // bias, so the multiplier is 1.
             const float msub = m_run == kNegInf ? 0.f : m_run;
-            const float psc = ALIBI ? 1.f : sl2;  // x is already scaled with ALiBi
+            const float psc = ALIBI ? 1.f : sl2;
             const uint64_t scale2 = f2_pack(psc, psc), neg2 = f2_pack(-msub, -msub);
             uint64_t ps2[2] = {0ull, 0ull};
 #pragma unroll

@@ -220,9 +220,12 @@ def make_decode(lens, num_qo_heads, num_kv_heads, head_dim, block_size, dtype, s
 def alibi_slopes(kind: str, n: int, gen) -> Optional[torch.Tensor]:
     """ALiBi slopes for n query heads: 'geometric' = the ALiBi paper's
     2^(-8 (i+1) / n); 'uniform' = seeded U[0.01, 1] (steep and shallow heads
-    mixed); 'none' = no bias."""
+    mixed); 'steep' = seeded U[0.5, 2] (one key dominates each row); 'none' =
+    no bias."""
     if kind == "none":
         return None
+    if kind == "steep":
+        return torch.rand(n, generator=gen, dtype=torch.float32) * 1.5 + 0.5
     if kind == "geometric":
         return torch.tensor([2.0 ** (-8.0 * (i + 1) / n) for i in range(n)], dtype=torch.float32)
     if kind == "uniform":

@@ -193,6 +193,18 @@ def test_alibi_prefill_group_sizes(G, Hkv, bs):
     _check(case)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_alibi_steep_slopes_peaked(causal):
+    """Slopes in [0.5, 2]: each row's weight sits on one or two keys, so the
+    output is nearly one value row and the rounding of the dominant P to bf16
+    is not averaged away.  Rows span many key tiles and ragged ends."""
+    q_lens = [1, 7, 130, 513, 64]
+    kv_lens = [3000, 7, 1000, 513, 2]
+    case = W.make_varlen_kv(q_lens, kv_lens, 32, 8, 128, 16, BF16, seed=130 + int(causal),
+                            sink="randn", causal=causal, alibi="steep")
+    _check(case)
+
+
 def test_alibi_contiguous():
     case = W.make_varlen_kv([5, 127, 300], [5, 1000, 300], 32, 8, 128, 16, BF16, seed=120,
                             sink="randn", alibi="geometric", causal=False)
