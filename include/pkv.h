@@ -109,7 +109,7 @@ typedef struct pkv_cache_desc {
     int64_t num_blocks;   /* pages in each pool */
     int32_t block_size;   /* tokens per page: 16 or 32 */
     int32_t num_kv_heads; /* Hkv */
-    int32_t head_dim;     /* D: 64 or 128 */
+    int32_t head_dim;     /* D: 64, 80, 96, 112, 128 or 256 (see each call) */
     int32_t dtype;        /* pkv_dtype of the pools, q and out */
 } pkv_cache_desc;
 
@@ -200,6 +200,9 @@ PKV_API size_t pkv_paged_decode_workspace_size(int batch, int num_qo_heads, int 
  *   alibi_slopes  [num_qo_heads] fp32 (device) or NULL: with slopes the
  *                 logit of key j gains alibi_slopes[h] * (j - (L_b - 1))
  *   window_left   -1 for none, else keep keys j >= L_b - 1 - window_left
+ *   head sizes: bf16 64/80/96/112/128/256, fp32 64/80/96/112/128 (the
+ *                 kernels pad to 64, 128 or 256 with zeros; the padding reads
+ *                 no memory)
  *   partition_size split-KV partition in tokens (0 = 512); a multiple of
  *                 block_size, at most 16384; partitions start at multiples of
  *                 it
@@ -236,7 +239,8 @@ PKV_API size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, in
  *   sink, alibi_slopes (bias alibi_slopes[h] * (j - qpos)), window_left,
  *   sm_scale, lse_out ([total_q, num_qo_heads]) as in
  *   paged_decode.  Causal rows whose position is negative (q_len > kv_len)
- *   keep no key.  Supported: bf16 pools, head_dim 128, block_size 16 or 32,
+ *   keep no key.  Supported: bf16 pools, head_dim 64/80/96/112/128 (the
+ *   tiles are padded to 128 with zeros), block_size 16 or 32,
  *   G = num_qo_heads / num_kv_heads a power of two <= 16; anything else
  *   returns PKV_ERR_UNSUPPORTED.
  */

@@ -81,9 +81,9 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
 // Combine the per-warp softmax states of one CTA and write the partition's
 // normalised output and log-sum-exp (log2 units).  s_o holds the warps'
 // O accumulators already rescaled to the common maximum.
-__device__ __forceinline__ void write_partition(const DecodeParams &p, int b, int g, int pidx,
-                                                int D, const float *s_m, const float *s_l,
-                                                const float *s_o) {
+__device__ __forceinline__ void write_partition_rows(const DecodeParams &p, int b, int g,
+                                                     int pidx, int D, int Ds, const float *s_m,
+                                                     const float *s_l, const float *s_o) {
     const int G = p.group;
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
         const int h = i / D, d = i - h * D;
@@ -98,9 +98,21 @@ __device__ __forceinline__ void write_partition(const DecodeParams &p, int b, in
         }
         const int hq = g * G + h;
         const int64_t idx = ((int64_t)b * p.num_qo_heads + hq) * p.num_parts + pidx;
-        p.part_o[idx * D + d] = Ls > 0.f ? s_o[h * D + d] / Ls : 0.f;
+        p.part_o[idx * D + d] = Ls > 0.f ? s_o[h * Ds + d] / Ls : 0.f;
         if (d == 0) p.part_lse[idx] = Ls > 0.f ? M + log2f(Ls) : kNegInf;
     }
+}
+
+// D: the head size (row stride of part_o); Ds: the row stride of s_o (D
+// padded to the kernel's tile width).
+template <int Ds>
+__device__ __forceinline__ void write_partition(const DecodeParams &p, int b, int g, int pidx,
+                                                int D, const float *s_m, const float *s_l,
+                                                const float *s_o) {
+    if (D == Ds)  // the usual case: divide by a compile-time width
+        write_partition_rows(p, b, g, pidx, Ds, Ds, s_m, s_l, s_o);
+    else
+        write_partition_rows(p, b, g, pidx, D, Ds, s_m, s_l, s_o);
 }
 
 // ---------------------------------------------------------------------------
@@ -201,17 +213,22 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
     // Q as the A operand (rows = query heads of this kv head, zero-padded to 16)
     const int gq = lane >> 2, tq = lane & 3;
     const int G = p.group;
+    // D is the tile width; the head size Dh <= D is a multiple of 16, so a
+    // 16-dim k-step lies wholly inside or wholly past it (past it: zeros,
+    // matching the zero-filled columns the TMA boxes bring beyond Dh)
+    const int Dh = p.head_dim;
     const __nv_bfloat16 *qb =
-        static_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)b * p.num_qo_heads + g * G) * D;
+        static_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)b * p.num_qo_heads + g * G) * Dh;
     uint32_t qa[DK][4];
 #pragma unroll
     for (int kk = 0; kk < DK; ++kk) {
         const int d0 = kk * 16 + 2 * tq;
-        const bool h0 = gq < G, h1 = (NHT > 1) && (gq + 8 < G);
-        qa[kk][0] = h0 ? ld_b32(qb + gq * D + d0) : 0u;
-        qa[kk][1] = h1 ? ld_b32(qb + (gq + 8) * D + d0) : 0u;
-        qa[kk][2] = h0 ? ld_b32(qb + gq * D + d0 + 8) : 0u;
-        qa[kk][3] = h1 ? ld_b32(qb + (gq + 8) * D + d0 + 8) : 0u;
+        const bool in = kk * 16 < Dh;
+        const bool h0 = in && gq < G, h1 = in && (NHT > 1) && (gq + 8 < G);
+        qa[kk][0] = h0 ? ld_b32(qb + gq * Dh + d0) : 0u;
+        qa[kk][1] = h1 ? ld_b32(qb + (gq + 8) * Dh + d0) : 0u;
+        qa[kk][2] = h0 ? ld_b32(qb + gq * Dh + d0 + 8) : 0u;
+        qa[kk][3] = h1 ? ld_b32(qb + (gq + 8) * Dh + d0 + 8) : 0u;
     }
 
     float oacc[NHT][DK][4];
@@ -403,7 +420,7 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
         }
     }
     __syncthreads();
-    write_partition(p, b, g, pidx, D, s_m, s_l, s_o);
+    write_partition<D>(p, b, g, pidx, Dh, s_m, s_l, s_o);
 }
 
 // ---------------------------------------------------------------------------
@@ -427,7 +444,8 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
     if (tok_lo >= tok_hi) return;
 
     const int G = p.group, Hkv = p.num_kv_heads;
-    const float *qb = static_cast<const float *>(p.q) + ((int64_t)b * p.num_qo_heads + g * G) * D;
+    const int Dh = p.head_dim;  // <= D; dims past it are zero in q and skipped in k, v
+    const float *qb = static_cast<const float *>(p.q) + ((int64_t)b * p.num_qo_heads + g * G) * Dh;
     float q[kMaxGroup][DPL], o[kMaxGroup][DPL], m[kMaxGroup], l[kMaxGroup];
 #pragma unroll
     for (int h = 0; h < kMaxGroup; ++h) {
@@ -435,7 +453,7 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
         l[h] = 0.f;
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
-            q[h][i] = h < G ? qb[h * D + lane + 32 * i] : 0.f;
+            q[h][i] = (h < G && lane + 32 * i < Dh) ? qb[h * Dh + lane + 32 * i] : 0.f;
             o[h][i] = 0.f;
         }
     }
@@ -448,12 +466,13 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
             if (lane == 0) flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
             continue;
         }
-        const int64_t base = (((int64_t)blk * block_size + tok % block_size) * Hkv + g) * D;
+        const int64_t base = (((int64_t)blk * block_size + tok % block_size) * Hkv + g) * Dh;
         float k[DPL], v[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
-            k[i] = kc[base + lane + 32 * i];
-            v[i] = vc[base + lane + 32 * i];
+            const bool in = lane + 32 * i < Dh;
+            k[i] = in ? kc[base + lane + 32 * i] : 0.f;
+            v[i] = in ? vc[base + lane + 32 * i] : 0.f;
         }
 #pragma unroll
         for (int h = 0; h < kMaxGroup; ++h) {
@@ -501,7 +520,7 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
         }
     }
     __syncthreads();
-    write_partition(p, b, g, pidx, D, s_m, s_l, s_o);
+    write_partition<D>(p, b, g, pidx, Dh, s_m, s_l, s_o);
 }
 
 // ---------------------------------------------------------------------------
@@ -627,7 +646,7 @@ decode_merge_kernel(const DecodeParams p, int D, int block_size) {
 template <typename OutT, int D>
 __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_warp_kernel(const DecodeParams p, int block_size) {
-    constexpr int VEC = D / 32;  // columns per lane: 2 or 4
+    constexpr int VEC = D / 32;  // columns per lane: 2, 4 or 8
     const int lane = threadIdx.x & 31;
     const int64_t unit = (int64_t)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
     if (unit >= (int64_t)p.batch * p.num_qo_heads) return;
@@ -656,7 +675,18 @@ decode_merge_warp_kernel(const DecodeParams p, int block_size) {
         for (int k = 0; k < cnt; ++k) {
             const float w = __shfl_sync(0xffffffffu, w_mine, k);
             const float *row = po + (int64_t)(c0 + k) * D;
-            if constexpr (VEC == 4) {
+            if constexpr (VEC == 8) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(row);
+                const float4 u4 = *reinterpret_cast<const float4 *>(row + 4);
+                acc[0] = fmaf(w, v4.x, acc[0]);
+                acc[1] = fmaf(w, v4.y, acc[1]);
+                acc[2] = fmaf(w, v4.z, acc[2]);
+                acc[3] = fmaf(w, v4.w, acc[3]);
+                acc[4] = fmaf(w, u4.x, acc[4]);
+                acc[5] = fmaf(w, u4.y, acc[5]);
+                acc[6] = fmaf(w, u4.z, acc[6]);
+                acc[7] = fmaf(w, u4.w, acc[7]);
+            } else if constexpr (VEC == 4) {
                 const float4 v4 = *reinterpret_cast<const float4 *>(row);
                 acc[0] = fmaf(w, v4.x, acc[0]);
                 acc[1] = fmaf(w, v4.y, acc[1]);
@@ -690,12 +720,15 @@ template <typename OutT>
 cudaError_t launch_merge(const DecodeParams &p, int D, int BS, cudaStream_t stream) {
     // many heads with few partitions: warp per head; otherwise CTA per head
     const int64_t units = (int64_t)p.batch * p.num_qo_heads;
-    if (p.num_parts <= 64 && units >= 8LL * device_sm_count()) {
+    if (p.num_parts <= 64 && units >= 8LL * device_sm_count() &&
+        (D == 64 || D == 128 || D == 256)) {
         const unsigned blocks = (unsigned)((units + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
         if (D == 64)
             decode_merge_warp_kernel<OutT, 64><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
-        else
+        else if (D == 128)
             decode_merge_warp_kernel<OutT, 128><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
+        else
+            decode_merge_warp_kernel<OutT, 256><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
         return cudaGetLastError();
     }
     const int merge_smem = p.num_parts * (int)sizeof(float);
@@ -737,27 +770,35 @@ cudaError_t launch_tc_g(const DecodeParams &p, const CUtensorMap *tk, const CUte
 cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
                           const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                           cudaStream_t stream) {
+    // D: the head size; T: the kernel's tile width (D rounded up to 64, 128
+    // or 256; the padded dims are zeros and cost no HBM traffic)
     const int D = cache.head_dim, BS = cache.block_size;
+    const int T = D <= 64 ? 64 : D <= 128 ? 128 : 256;
     cudaError_t e = cudaSuccess;
     if (p.group > kMaxGroup || p.partition_size > kMaxPartition) return cudaErrorNotSupported;
+    if (D % 16 != 0 || D > 256 || p.head_dim != D) return cudaErrorNotSupported;
     if (cache.dtype == PKV_F32) {
         dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
-        if (D == 64)
+        if (T == 64)
             decode_f32_kernel<64><<<grid, kDecThreads, 0, stream>>>(p, BS);
-        else if (D == 128)
+        else if (T == 128)
             decode_f32_kernel<128><<<grid, kDecThreads, 0, stream>>>(p, BS);
         else
             return cudaErrorNotSupported;
         e = cudaGetLastError();
     } else {
-        if (D == 64 && BS == 16)
+        if (T == 64 && BS == 16)
             e = launch_tc_g<64, 16>(p, tmap_k, tmap_v, stream);
-        else if (D == 64 && BS == 32)
+        else if (T == 64 && BS == 32)
             e = launch_tc_g<64, 32>(p, tmap_k, tmap_v, stream);
-        else if (D == 128 && BS == 16)
+        else if (T == 128 && BS == 16)
             e = launch_tc_g<128, 16>(p, tmap_k, tmap_v, stream);
-        else if (D == 128 && BS == 32)
+        else if (T == 128 && BS == 32)
             e = launch_tc_g<128, 32>(p, tmap_k, tmap_v, stream);
+        else if (T == 256 && BS == 16)
+            e = launch_tc_g<256, 16>(p, tmap_k, tmap_v, stream);
+        else if (T == 256 && BS == 32)
+            e = launch_tc_g<256, 32>(p, tmap_k, tmap_v, stream);
         else
             return cudaErrorNotSupported;
     }

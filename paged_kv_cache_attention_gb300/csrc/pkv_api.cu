@@ -59,7 +59,10 @@ pkv_status check_cache(const pkv_cache_desc &c) {
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0)
         return PKV_ERR_INVALID_ARG;
     if (c.dtype != PKV_F32 && c.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (c.head_dim != 64 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    switch (c.head_dim) {  // the head sizes the attention kernels take
+        case 64: case 80: case 96: case 112: case 128: case 256: break;
+        default: return PKV_ERR_UNSUPPORTED;
+    }
     if (c.block_size != 16 && c.block_size != 32) return PKV_ERR_UNSUPPORTED;
     if (c.num_blocks * (int64_t)c.block_size >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
@@ -271,6 +274,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
     if (num_qo_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     const int G = num_qo_heads / cache.num_kv_heads;
     if (G > 16) return PKV_ERR_UNSUPPORTED;
+    if (cache.dtype == PKV_F32 && cache.head_dim > 128) return PKV_ERR_UNSUPPORTED;
     const int P = partition_size > 0 ? partition_size : kDefaultPartition;
     if (partition_size < 0 || P % cache.block_size != 0 || P > kMaxPartition)
         return PKV_ERR_INVALID_ARG;
@@ -308,6 +312,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.max_seqlen = max_seqlen;
     p.window_left = window_left;
+    p.head_dim = cache.head_dim;
     p.partition_size = P;
     p.num_parts = np;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
@@ -354,7 +359,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
                        float *lse_out, void *workspace, size_t workspace_bytes,
                        int32_t *dev_error, void *stream) {
     if (cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (cache.head_dim % 16 != 0 || cache.head_dim > 128) return PKV_ERR_UNSUPPORTED;
     if (batch < 0 || num_qo_heads <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         total_q < 0 || max_blocks_per_seq <= 0 || window_left < -1 || !std::isfinite(sm_scale))
         return PKV_ERR_INVALID_ARG;
@@ -396,6 +401,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
     p.max_seqlen_k = max_seqlen_k;
     p.total_q = total_q;
     p.window_left = window_left;
+    p.head_dim = cache.head_dim;
     p.causal = causal ? 1 : 0;
     p.total_k = contiguous ? (int)kv_rows : 0;
     p.rows_per_head = 128 / G;

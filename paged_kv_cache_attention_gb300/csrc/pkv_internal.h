@@ -29,6 +29,7 @@ struct DecodeParams {
     int batch, num_qo_heads, num_kv_heads, group;
     int max_blocks_per_seq, max_seqlen;
     int window_left;
+    int head_dim;                // D of q, out and the pools; the kernels pad it to 64/128/256
     int partition_size;
     int num_parts;               // grid.x: partitions per sequence the grid covers
     float scale_log2;            // sm_scale * log2(e)
@@ -52,6 +53,7 @@ struct PrefillParams {
     int max_blocks_per_seq, max_seqlen_q, max_seqlen_k, total_q;
     int window_left;
     int causal;                    // 1: keys j <= query position; 0: no upper bound
+    int head_dim;                  // D <= 128; the tiles are padded to 128 with zeros
     int total_k;                   // contiguous K/V: rows in the arrays (unused when paged)
     int rows_per_head;             // query tokens per 128-row tile (128 / group)
     int max_tiles;                 // capacity of the work list

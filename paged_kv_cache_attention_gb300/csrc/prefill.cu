@@ -402,9 +402,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         if (ntiles > 0 && lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
+            const int ksteps = p.head_dim / 16;  // k-steps past the head size multiply zeros
             auto issue_s = [&](int x, int s) {
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    if (kk >= ksteps) break;
                     const uint32_t koff = (kk >> 2) * Lay::HALF + (kk & 3) * 32;
                     const uint64_t a = tc::smem_desc_sw128(sQ + x * Lay::Q_BYTES + koff, 16, 1024);
                     const uint64_t b = tc::smem_desc_sw128(sK + s * Lay::T_BYTES + koff, 16, 1024);
@@ -639,8 +641,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             oscale = f / Z;
             lse = (M + log2f(Z)) * kLn2;
         }
+        // the head size Dh <= 128 is a multiple of 16: the stores below skip
+        // whole 8-column vectors past it (those columns of O are zero padding)
+        const int Dh = p.head_dim;
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) +
-                              ((int64_t)(geo.q_start + tok) * p.num_qo_heads + head) * kHeadDim +
+                              ((int64_t)(geo.q_start + tok) * p.num_qo_heads + head) * Dh +
                               hc * 64;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -657,6 +662,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int e = 8 * i;
+                    if (hc * 64 + c * 32 + e >= Dh) break;
                     dst[i] = make_uint4(
                         pack_bf16(__uint_as_float(r32[e + 0]) * oscale, __uint_as_float(r32[e + 1]) * oscale),
                         pack_bf16(__uint_as_float(r32[e + 2]) * oscale, __uint_as_float(r32[e + 3]) * oscale),
@@ -686,7 +692,8 @@ cudaError_t set_smem(K kernel, int bytes) {
 cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, bool contiguous,
                            const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
                            const CUtensorMap *tmap_v, cudaStream_t stream) {
-    if (cache.head_dim != kHeadDim || cache.dtype != PKV_BF16) return cudaErrorNotSupported;
+    if (cache.head_dim > kHeadDim || cache.head_dim % 16 != 0 || cache.dtype != PKV_BF16)
+        return cudaErrorNotSupported;
     prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

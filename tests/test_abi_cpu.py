@@ -79,7 +79,9 @@ def _decode(lib, desc=None, batch=4, hq=32, window=-1, part=512, ws_bytes=1 << 3
 
 @nogpu
 @pytest.mark.parametrize("kw,expected", [
-    (dict(desc=_desc(d=80)), 2),                 # head_dim without a kernel
+    (dict(desc=_desc(d=72)), 2),                 # head_dim without a kernel
+    (dict(desc=_desc(d=512)), 2),
+    (dict(desc=_desc(d=256, dtype=0)), 2),       # fp32 decode stops at 128
     (dict(desc=_desc(bs=8)), 2),                 # block size without a kernel
     (dict(desc=_desc(dtype=7)), 2),              # unknown dtype
     (dict(desc=_desc(nb=0)), 1),                 # empty pool
@@ -118,6 +120,8 @@ def test_reshape_and_cache_validation():
 @nogpu
 @pytest.mark.parametrize("change,expected", [
     (dict(window=-2), 1),
+    (dict(d=256), 2),               # prefill tiles stop at head_dim 128
+    (dict(d=72), 2),
     (dict(dtype=0), 2),             # fp32 prefill not in this version
     (dict(hq=24), 2),               # group of 3 (not a power of two)
     (dict(total_q=0), 0),
@@ -125,9 +129,10 @@ def test_reshape_and_cache_validation():
 ])
 def test_prefill_validation(change, expected):
     lib = pkv.load_library()
-    a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30, window=-1)
+    a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30, window=-1, d=128)
     a.update(change)
-    st = lib.pkv_varlen_prefill(FAKE, FAKE, FAKE, FAKE, _desc(dtype=a["dtype"]), FAKE, 8, FAKE,
+    st = lib.pkv_varlen_prefill(FAKE, FAKE, FAKE, FAKE, _desc(dtype=a["dtype"], d=a["d"]), FAKE,
+                                8, FAKE,
                                 FAKE, 64, 128, a["total_q"], None, None, 2, a["hq"], a["causal"],
                                 a["window"], 0.1, None, FAKE, a["ws_bytes"], None, None)
     assert st == expected
@@ -139,7 +144,8 @@ def test_prefill_validation(change, expected):
     (dict(hkv=0), 1),
     (dict(dtype=3), 2),
     (dict(dtype=0), 2),             # fp32 prefill not in this version
-    (dict(d=64), 2),                # head_dim 128 only
+    (dict(d=72), 2),                # not a multiple of 16
+    (dict(d=256), 2),               # prefill tiles stop at 128
     (dict(hq=24), 2),               # group of 3 (not a power of two)
     (dict(hq=12), 1),               # not a multiple of num_kv_heads
     (dict(k=None), 1),              # keys missing although total_k > 0

@@ -242,3 +242,41 @@ def test_alibi_long_context_sampled():
     got = gpu_decode(case)
     ref = oracle_decode(case, rows=[0, 3])
     assert max_abs(got[[0, 3]], ref) <= TOL[torch.bfloat16]
+
+
+# ---------------------------------------------------------------------------
+# head sizes 80 / 96 / 112 / 256
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [80, 96, 112, 256])
+@pytest.mark.parametrize("Hq,Hkv,bs", [(32, 8, 16), (16, 1, 32), (8, 8, 16)])
+def test_head_sizes_bf16(D, Hq, Hkv, bs):
+    lens = [1, 17, 511, 513, 2000]
+    case = W.make_decode(lens, Hq, Hkv, D, bs, torch.bfloat16, seed=D + Hq + bs, sink="randn",
+                         window_left=700 if bs == 32 else -1)
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("D", [80, 112])
+def test_head_sizes_fp32(D):
+    case = W.make_decode([1, 31, 70, 300], 4, 2, D, 32, torch.float32, seed=D, sink="randn")
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.float32]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.float32]
+
+
+@pytest.mark.parametrize("D", [96, 256])
+def test_head_sizes_many_heads_warp_merge(D):
+    """Many (sequence, head) pairs with few partitions: the warp-per-head
+    merge for 256, the CTA merge for 96."""
+    gen = torch.Generator().manual_seed(D)
+    lens = torch.randint(1, 1500, (64,), generator=gen).tolist()
+    case = W.make_decode(lens, 32, 8, D, 16, torch.bfloat16, seed=D + 1, sink="randn",
+                         alibi="geometric")
+    got = gpu_decode(case)
+    rows = list(range(0, 64, 5))
+    assert max_abs(got[rows], oracle_decode(case, rows=rows)) <= TOL[torch.bfloat16]

@@ -225,6 +225,28 @@ def test_alibi_decode_equals_prefill_with_one_query():
     assert max_abs(b, oracle_decode(dec)) <= TOL[BF16]
 
 
+# ---------------------------------------------------------------------------
+# head sizes 64 / 80 / 96 / 112 (tiles padded to 128 with zeros)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 80, 96, 112])
+@pytest.mark.parametrize("G,Hkv", [(4, 8), (1, 4), (16, 1)])
+def test_head_sizes(D, G, Hkv):
+    q_lens = [1, 33, 129, 300]
+    kv_lens = [1, 333, 1000, 300]
+    case = W.make_varlen_kv(q_lens, kv_lens, G * Hkv, Hkv, D, 16, BF16, seed=D + G,
+                            sink="randn", window_left=200 if G == 1 else -1,
+                            alibi="geometric" if G == 16 else "none")
+    _check(case)
+
+
+@pytest.mark.parametrize("D", [80, 112])
+def test_head_sizes_contiguous_non_causal(D):
+    case = W.make_varlen_kv([5, 127, 300], [5, 1000, 300], 32, 8, D, 16, BF16, seed=D + 3,
+                            sink="randn", causal=False)
+    _check_contig(case, pad_rows=32)
+
+
 def test_decode_equals_prefill_with_one_query():
     """Cross-op: paged_decode == varlen_prefill with q_len = 1 per request."""
     dec = W.make_decode([1, 300, 1024, 4097], 32, 8, 128, 16, BF16, seed=23, sink="randn",
