@@ -43,8 +43,9 @@
  * sink[h] is a logit, not scaled by sm_scale; sink == NULL means no sink.
  * A row that keeps no key gets o = 0 and lse = sink[h] (or -inf).
  *
- * Paged pool layout ("NHD pages"): k_cache and v_cache are each a contiguous
- *   [num_blocks, block_size, num_kv_heads, head_dim]
+ * Paged pool layout: k_cache and v_cache are each a contiguous
+ *   [num_blocks, block_size, num_kv_heads, head_dim]   (PKV_NHD), or
+ *   [num_blocks, num_kv_heads, block_size, head_dim]   (PKV_HND)
  * array.  Logical position p of sequence b lives in page
  * block_table[b * max_blocks_per_seq + p / block_size], row p % block_size;
  * its flat slot is page * block_size + p % block_size.  block_table entries
@@ -96,6 +97,11 @@ typedef enum pkv_status {
 
 typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 
+/* Layout of each pool.  NHD: [num_blocks, block_size, num_kv_heads, head_dim]
+ * (a token's row of all kv heads is contiguous).  HND: [num_blocks,
+ * num_kv_heads, block_size, head_dim] (a page of one kv head is contiguous). */
+typedef enum pkv_layout { PKV_NHD = 0, PKV_HND = 1 } pkv_layout;
+
 /* Device-side error bits OR-ed into *dev_error. */
 #define PKV_DEVERR_BLOCK_ID 1u /* block_table entry of an attended position outside [0, num_blocks) */
 #define PKV_DEVERR_SLOT 2u     /* slot_mapping entry >= num_blocks * block_size */
@@ -111,6 +117,7 @@ typedef struct pkv_cache_desc {
     int32_t num_kv_heads; /* Hkv */
     int32_t head_dim;     /* D: 64, 80, 96, 112, 128 or 256 (see each call) */
     int32_t dtype;        /* pkv_dtype of the pools, q and out */
+    int32_t layout;       /* pkv_layout of the pools */
 } pkv_cache_desc;
 
 /* Human-readable name of a pkv_status. */

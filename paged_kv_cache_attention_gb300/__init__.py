@@ -65,7 +65,10 @@ class PkvError(RuntimeError):
 class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32)]
+
+
+LAYOUTS = {"NHD": 0, "HND": 1}
 
 
 _lib = None
@@ -167,13 +170,22 @@ def _cuda_contig(name, t, dtype=None, ndim=None):
         _require(t.dim() == ndim, f"{name} must have {ndim} dims, got {t.dim()}")
 
 
-def _cache_desc(k_cache, v_cache) -> CacheDesc:
+def _pool_dims(k_cache, layout: str):
+    """(num_blocks, block_size, num_kv_heads, head_dim) of a pool: NHD pools
+    are [num_blocks, block_size, Hkv, D], HND pools [num_blocks, Hkv,
+    block_size, D]."""
+    _require(layout in LAYOUTS, f"layout must be one of {sorted(LAYOUTS)}")
+    nb, a, b, d = k_cache.shape
+    return (nb, a, b, d) if layout == "NHD" else (nb, b, a, d)
+
+
+def _cache_desc(k_cache, v_cache, layout: str = "NHD") -> CacheDesc:
     _cuda_contig("k_cache", k_cache, ndim=4)
     _cuda_contig("v_cache", v_cache, ndim=4)
     _require(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype,
              "k_cache and v_cache must have the same shape and dtype")
-    nb, bs, hkv, d = k_cache.shape
-    return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache.dtype))
+    nb, bs, hkv, d = _pool_dims(k_cache, layout)
+    return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache.dtype), LAYOUTS[layout])
 
 
 def _head_vector(name, t, Hq):
@@ -209,7 +221,7 @@ def _workspace(nbytes: int, device, workspace):
 # ---------------------------------------------------------------------------
 
 def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, dev_error=None,
-                      stream=None) -> None:
+                      stream=None, layout: str = "NHD") -> None:
     """k_cache/v_cache flat slot slot_mapping[t] <- key/value[t] (in place).
 
     key, value: [T, Hkv, D] contiguous, dtype of the cache; slot_mapping: [T]
@@ -217,11 +229,11 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, dev_error=None
     receives PKV_DEVERR_SLOT for slots outside the pool.
     """
     torch = _torch()
-    desc = _cache_desc(k_cache, v_cache)
+    desc = _cache_desc(k_cache, v_cache, layout)
     _cuda_contig("key", key, k_cache.dtype, 3)
     _cuda_contig("value", value, k_cache.dtype, 3)
     _cuda_contig("slot_mapping", slot_mapping, torch.int64, 1)
-    _require(key.shape == value.shape and key.shape[1:] == k_cache.shape[2:],
+    _require(key.shape == value.shape and key.shape[1:] == (desc.num_kv_heads, desc.head_dim),
              "key/value must be [T, num_kv_heads, head_dim] matching the cache")
     _require(slot_mapping.shape[0] == key.shape[0], "slot_mapping must have T entries")
     st = load_library().pkv_reshape_and_cache(
@@ -257,20 +269,20 @@ def rope_cos_sin_table(max_position: int, rotary_dim: int, base: float = 10000.0
 
 def rope_reshape_and_cache(query, key, value, k_cache, v_cache, positions, slot_mapping,
                            cos_sin, rotary_dim: Optional[int] = None, is_neox_style: bool = True,
-                           dev_error=None, stream=None) -> None:
+                           dev_error=None, stream=None, layout: str = "NHD") -> None:
     """Rotate query [T, Hq, D] and key [T, Hkv, D] in place by positions [T]
     (int64) using the table cos_sin ([max_position, rotary_dim // 2, 2]), then
     write the rotated key and the value to the pools at slot_mapping [T]
     (int64; negative = not cached).  query may be None."""
     torch = _torch()
-    desc = _cache_desc(k_cache, v_cache)
+    desc = _cache_desc(k_cache, v_cache, layout)
     _cuda_contig("key", key, k_cache.dtype, 3)
     _cuda_contig("value", value, k_cache.dtype, 3)
     _cuda_contig("positions", positions, torch.int64, 1)
     _cuda_contig("slot_mapping", slot_mapping, torch.int64, 1)
     _cuda_contig("cos_sin", cos_sin, torch.float32, 3)
     T = key.shape[0]
-    _require(key.shape == value.shape and key.shape[1:] == k_cache.shape[2:],
+    _require(key.shape == value.shape and key.shape[1:] == (desc.num_kv_heads, desc.head_dim),
              "key/value must be [T, num_kv_heads, head_dim] matching the cache")
     _require(positions.shape[0] == T and slot_mapping.shape[0] == T,
              "positions and slot_mapping must have T entries")
@@ -293,22 +305,24 @@ def rope_reshape_and_cache(query, key, value, k_cache, v_cache, positions, slot_
 def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,
                  sink=None, window_left: int = -1, sm_scale: Optional[float] = None,
                  partition_size: int = 512, out=None, lse=None, workspace=None,
-                 dev_error=None, stream=None, alibi_slopes=None):
+                 dev_error=None, stream=None, alibi_slopes=None, layout: str = "NHD"):
     """Single-token decode over the paged pools; returns out [B, Hq, D].
 
     q: [B, Hq, D] (dtype of the cache); block_table: [B, max_blocks] int32;
     cache_seqlens: [B] int32, the attended length (query at position L-1);
     max_seqlen: host int >= max(cache_seqlens); sink: [Hq] float32 or None;
     lse: optional [B, Hq] float32 output (natural log, sink included);
-    alibi_slopes: [Hq] float32 or None (bias slope * (j - (L - 1))).
+    alibi_slopes: [Hq] float32 or None (bias slope * (j - (L - 1)));
+    layout: "NHD" pools [num_blocks, block_size, Hkv, D] or "HND" pools
+    [num_blocks, Hkv, block_size, D].
     """
     torch = _torch()
-    desc = _cache_desc(k_cache, v_cache)
+    desc = _cache_desc(k_cache, v_cache, layout)
     _cuda_contig("q", q, k_cache.dtype, 3)
     _cuda_contig("block_table", block_table, torch.int32, 2)
     _cuda_contig("cache_seqlens", cache_seqlens, torch.int32, 1)
     B, Hq, D = q.shape
-    _require(D == k_cache.shape[3], "head_dim of q and cache differ")
+    _require(D == desc.head_dim, "head_dim of q and cache differ")
     _require(block_table.shape[0] == B and cache_seqlens.shape[0] == B,
              "block_table / cache_seqlens batch mismatch")
     if sink is not None:
@@ -339,7 +353,8 @@ def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: in
 def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_k,
                    max_seqlen_q: int, max_seqlen_k: int, sink=None, causal: bool = True,
                    window_left: int = -1, sm_scale: Optional[float] = None, out=None, lse=None,
-                   workspace=None, dev_error=None, stream=None, alibi_slopes=None):
+                   workspace=None, dev_error=None, stream=None, alibi_slopes=None,
+                   layout: str = "NHD"):
     """Varlen / chunk prefill over the paged pools; returns out [total_q, Hq, D].
 
     q: [total_q, Hq, D] bf16; cu_seq_lens_q / cu_seq_lens_k: [B+1] int32;
@@ -348,7 +363,7 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
     still bounds keys from below).
     """
     torch = _torch()
-    desc = _cache_desc(k_cache, v_cache)
+    desc = _cache_desc(k_cache, v_cache, layout)
     _cuda_contig("q", q, k_cache.dtype, 3)
     _cuda_contig("block_table", block_table, torch.int32, 2)
     _cuda_contig("cu_seq_lens_q", cu_seq_lens_q, torch.int32, 1)
@@ -370,7 +385,7 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
         _cuda_contig("lse", lse, torch.float32, 2)
         _require(tuple(lse.shape) == (total_q, Hq), "lse must be [total_q, Hq]")
     scale = float(sm_scale) if sm_scale is not None else D ** -0.5
-    need = varlen_prefill_workspace_size(B, Hq, k_cache.shape[2], total_q, max_seqlen_q)
+    need = varlen_prefill_workspace_size(B, Hq, desc.num_kv_heads, total_q, max_seqlen_q)
     ws = _workspace(need, q.device, workspace)
     st = load_library().pkv_varlen_prefill(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
@@ -432,7 +447,7 @@ def varlen_prefill_contiguous(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_seqlen_
 def paged_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,
                          sink=None, window_left: int = -1, sm_scale: Optional[float] = None,
                          partition_size: int = 512, out=None, lse=None, dev_error=None,
-                         stream=None):
+                         stream=None, layout: str = "NHD"):
     """paged_decode without a caller workspace, for callers that cannot
     allocate device memory at the call site.  The library's fixed device
     scratch array (PKV_NOALLOC_DECODE_SCRATCH_BYTES, 32 MiB) replaces the
@@ -449,7 +464,7 @@ def paged_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, max_se
         fn.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, i32, i32, i32, f32, i32, P, P,
                        P]
         fn.restype = i32
-    desc = _cache_desc(k_cache, v_cache)
+    desc = _cache_desc(k_cache, v_cache, layout)
     _cuda_contig("q", q, k_cache.dtype, 3)
     _cuda_contig("block_table", block_table, torch.int32, 2)
     _cuda_contig("cache_seqlens", cache_seqlens, torch.int32, 1)

@@ -5,7 +5,8 @@
 // cache at the flat slots slot_mapping names.  With the NHD page layout a
 // token's row (num_kv_heads * head_dim elements) is contiguous both in the
 // input and in the pool, so the scatter is a row copy: 16-byte vector loads
-// and stores, K and V rows interleaved over one flat index space.  The copy is
+// and stores, K and V rows interleaved over one flat index space.  With the
+// HND layout the same vectors go to one page row per kv head.  The copy is
 // bit-exact (integers, no arithmetic on the values).
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -19,11 +20,15 @@ constexpr int kVecPerThread = 4;  // 16-byte vectors each thread moves
 
 // Flat index space: [2 (K, V)][num_tokens][vecs_per_row].  Each thread moves
 // kVecPerThread vectors spaced one grid apart, loads first, then stores.
+// HND pools: vector c of a token's row belongs to kv head c / vecs_per_head
+// and goes to that head's page, row slot % block_size.
+template <bool HND>
 __global__ void __launch_bounds__(kThreads)
 reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                          uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                          const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
-                         int64_t vecs_per_row, int64_t capacity, int32_t *dev_error) {
+                         int64_t vecs_per_row, int64_t capacity, int block_size,
+                         int64_t vecs_per_head, int32_t *dev_error) {
     const int64_t per_tensor = num_tokens * vecs_per_row;
     const int64_t total = 2 * per_tensor;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -48,7 +53,14 @@ reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict_
                 continue;
             }
             v[u] = is_v[u] ? __ldg(value + j) : __ldg(key + j);
-            dst[u] = slot * vecs_per_row + c;
+            if constexpr (HND) {
+                const int64_t g = c / vecs_per_head, cv = c - g * vecs_per_head;
+                const int64_t blk = slot / block_size, off = slot - blk * block_size;
+                const int64_t heads = vecs_per_row / vecs_per_head;
+                dst[u] = ((blk * heads + g) * block_size + off) * vecs_per_head + cv;
+            } else {
+                dst[u] = slot * vecs_per_row + c;
+            }
         }
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
@@ -66,6 +78,7 @@ reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict_
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                      void *v_cache, const int64_t *slot_mapping,
                                      int64_t num_tokens, int64_t row_bytes, int64_t capacity,
+                                     int block_size, int64_t head_bytes, bool hnd,
                                      int32_t *dev_error, cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;
     const int64_t vecs_per_row = row_bytes / 16;
@@ -75,10 +88,11 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
     const int64_t cap = int64_t(device_sm_count()) * 32;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+    auto kern = hnd ? reshape_and_cache_kernel<true> : reshape_and_cache_kernel<false>;
+    kern<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
-        vecs_per_row, capacity, dev_error);
+        vecs_per_row, capacity, block_size, head_bytes / 16, dev_error);
     return cudaGetLastError();
 }
 

@@ -134,7 +134,7 @@ struct DecTC {
     static_assert(kMaxGroup * D * 4 <= RING_BYTES, "merge scratch must fit in the ring");
 };
 
-template <int D, int BS, int NHT, int NST>
+template <int D, int BS, int NHT, int NST, bool HND>
 __global__ void __launch_bounds__(kDecThreads)
 decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
@@ -199,11 +199,14 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
         }
         mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
         const uint32_t dst = wring + s * C::STAGE_BYTES;
-        const int row = blk * BS;
+        // box coordinates of (page, kv head): NHD (x, head, page * BS), HND
+        // (x, 0, page * Hkv + head)
+        const int cy = HND ? 0 : g;
+        const int cz = HND ? blk * p.num_kv_heads + g : blk * BS;
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
-            tma_load_3d_hint(dst + h * C::HALF_BYTES, &tmk, bar, h * 64, g, row, policy);
-            tma_load_3d_hint(dst + C::PAGE_BYTES + h * C::HALF_BYTES, &tmv, bar, h * 64, g, row,
+            tma_load_3d_hint(dst + h * C::HALF_BYTES, &tmk, bar, h * 64, cy, cz, policy);
+            tma_load_3d_hint(dst + C::PAGE_BYTES + h * C::HALF_BYTES, &tmv, bar, h * 64, cy, cz,
                              policy);
         }
     };
@@ -466,7 +469,9 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
             if (lane == 0) flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
             continue;
         }
-        const int64_t base = (((int64_t)blk * block_size + tok % block_size) * Hkv + g) * Dh;
+        const int64_t base =
+            p.hnd ? (((int64_t)blk * Hkv + g) * block_size + tok % block_size) * Dh
+                  : (((int64_t)blk * block_size + tok % block_size) * Hkv + g) * Dh;
         float k[DPL], v[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
@@ -749,7 +754,8 @@ template <int D, int BS, int NHT, int NST>
 cudaError_t launch_tc(const DecodeParams &p, const CUtensorMap *tk, const CUtensorMap *tv,
                       cudaStream_t stream) {
     using C = DecTC<D, BS, NHT, NST>;
-    auto kern = decode_bf16_tc_kernel<D, BS, NHT, NST>;
+    auto kern = p.hnd ? decode_bf16_tc_kernel<D, BS, NHT, NST, true>
+                      : decode_bf16_tc_kernel<D, BS, NHT, NST, false>;
     cudaError_t e = set_smem(kern, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_kv_heads, p.num_parts, p.batch);

@@ -55,16 +55,41 @@ pkv_status encode_rows_map(CUtensorMap *map, const void *base, int D, int heads,
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// TMA view of one paged pool whose box is one (page, kv head) half-row tile
+// of bs rows x 64 dims.  NHD: {D, Hkv, num_blocks * bs}, box {64, 1, bs} at
+// (x, head, page * bs).  HND: {D, bs, num_blocks * Hkv}, box {64, bs, 1} at
+// (x, 0, page * Hkv + head).  Both land as bs rows of 128 bytes.
+pkv_status encode_pool_map(CUtensorMap *map, const void *base, const pkv_cache_desc &c) {
+    if (c.layout == PKV_NHD)
+        return encode_rows_map(map, base, c.head_dim, c.num_kv_heads,
+                               c.num_blocks * c.block_size, 1, c.block_size);
+    auto enc = encoder();
+    if (!enc) return PKV_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.block_size,
+                          (cuuint64_t)(c.num_blocks * c.num_kv_heads)};
+    cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2,
+                             (cuuint64_t)c.head_dim * 2 * c.block_size};
+    cuuint32_t box[3] = {64, (cuuint32_t)c.block_size, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
 pkv_status check_cache(const pkv_cache_desc &c) {
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0)
         return PKV_ERR_INVALID_ARG;
     if (c.dtype != PKV_F32 && c.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (c.layout != PKV_NHD && c.layout != PKV_HND) return PKV_ERR_UNSUPPORTED;
     switch (c.head_dim) {  // the head sizes the attention kernels take
         case 64: case 80: case 96: case 112: case 128: case 256: break;
         default: return PKV_ERR_UNSUPPORTED;
     }
     if (c.block_size != 16 && c.block_size != 32) return PKV_ERR_UNSUPPORTED;
     if (c.num_blocks * (int64_t)c.block_size >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    if (c.num_blocks * (int64_t)c.num_kv_heads >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
 
@@ -168,7 +193,7 @@ const char *pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 200; }
+int pkv_version(void) { return 300; }
 
 pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                  void *v_cache, const int64_t *slot_mapping, int64_t num_tokens,
@@ -178,17 +203,20 @@ pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cac
         cache.head_dim <= 0)
         return PKV_ERR_INVALID_ARG;
     if (cache.dtype != PKV_F32 && cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (cache.layout != PKV_NHD && cache.layout != PKV_HND) return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PKV_OK;
     if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
-    const int64_t row_bytes =
-        (int64_t)cache.num_kv_heads * cache.head_dim * elem_bytes(cache.dtype);
+    const int64_t head_bytes = (int64_t)cache.head_dim * elem_bytes(cache.dtype);
+    const int64_t row_bytes = (int64_t)cache.num_kv_heads * head_bytes;
     if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (cache.layout == PKV_HND && head_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
     if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) ||
         !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
         return PKV_ERR_INVALID_ARG;
     const int64_t capacity = cache.num_blocks * (int64_t)cache.block_size;
     return from_cuda(launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping,
-                                              num_tokens, row_bytes, capacity, dev_error,
+                                              num_tokens, row_bytes, capacity, cache.block_size,
+                                              head_bytes, cache.layout == PKV_HND, dev_error,
                                               static_cast<cudaStream_t>(stream)));
 }
 
@@ -215,6 +243,7 @@ pkv_status pkv_rope_reshape_and_cache(void *query, void *key, const void *value,
         cache.head_dim <= 0)
         return PKV_ERR_INVALID_ARG;
     if (cache.dtype != PKV_F32 && cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (cache.layout != PKV_NHD && cache.layout != PKV_HND) return PKV_ERR_UNSUPPORTED;
     const int V = 16 / elem_bytes(cache.dtype);
     if (rotary_dim <= 0 || rotary_dim > cache.head_dim || rotary_dim % 2 != 0)
         return PKV_ERR_INVALID_ARG;
@@ -247,6 +276,8 @@ pkv_status pkv_rope_reshape_and_cache(void *query, void *key, const void *value,
     p.num_kv_heads = cache.num_kv_heads;
     p.head_dim = cache.head_dim;
     p.rotary_dim = rotary_dim;
+    p.block_size = cache.block_size;
+    p.hnd = cache.layout == PKV_HND ? 1 : 0;
     return from_cuda(launch_rope_reshape_cache(p, cache.dtype, is_neox_style != 0,
                                                static_cast<cudaStream_t>(stream)));
 }
@@ -313,6 +344,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
     p.max_seqlen = max_seqlen;
     p.window_left = window_left;
     p.head_dim = cache.head_dim;
+    p.hnd = cache.layout == PKV_HND ? 1 : 0;
     p.partition_size = P;
     p.num_parts = np;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
@@ -321,13 +353,8 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
     std::memset(&tk, 0, sizeof tk);
     std::memset(&tv, 0, sizeof tv);
     if (cache.dtype == PKV_BF16) {
-        const int64_t rows = cache.num_blocks * cache.block_size;
-        if ((st = encode_rows_map(&tk, k_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
-                                  cache.block_size)) != PKV_OK)
-            return st;
-        if ((st = encode_rows_map(&tv, v_cache, cache.head_dim, cache.num_kv_heads, rows, 1,
-                                  cache.block_size)) != PKV_OK)
-            return st;
+        if ((st = encode_pool_map(&tk, k_cache, cache)) != PKV_OK) return st;
+        if ((st = encode_pool_map(&tv, v_cache, cache)) != PKV_OK) return st;
     }
     return from_cuda(launch_decode(p, cache, &tk, &tv, static_cast<cudaStream_t>(stream)));
 }
@@ -402,6 +429,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
     p.total_q = total_q;
     p.window_left = window_left;
     p.head_dim = cache.head_dim;
+    p.hnd = (!contiguous && cache.layout == PKV_HND) ? 1 : 0;
     p.causal = causal ? 1 : 0;
     p.total_k = contiguous ? (int)kv_rows : 0;
     p.rows_per_head = 128 / G;
@@ -421,12 +449,17 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
     if ((st = encode_rows_map(&tq, q, cache.head_dim, num_qo_heads, total_q, G, 128 / G)) !=
         PKV_OK)
         return st;
-    if ((st = encode_rows_map(&tk, k, cache.head_dim, cache.num_kv_heads, kv_rows, 1,
-                              box_rows)) != PKV_OK)
-        return st;
-    if ((st = encode_rows_map(&tv, v, cache.head_dim, cache.num_kv_heads, kv_rows, 1,
-                              box_rows)) != PKV_OK)
-        return st;
+    if (contiguous) {
+        if ((st = encode_rows_map(&tk, k, cache.head_dim, cache.num_kv_heads, kv_rows, 1,
+                                  box_rows)) != PKV_OK)
+            return st;
+        if ((st = encode_rows_map(&tv, v, cache.head_dim, cache.num_kv_heads, kv_rows, 1,
+                                  box_rows)) != PKV_OK)
+            return st;
+    } else {
+        if ((st = encode_pool_map(&tk, k, cache)) != PKV_OK) return st;
+        if ((st = encode_pool_map(&tv, v, cache)) != PKV_OK) return st;
+    }
     return from_cuda(launch_prefill(p, cache, contiguous, &tq, &tk, &tv,
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -471,6 +504,7 @@ pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k
     cache.num_kv_heads = num_kv_heads;
     cache.head_dim = head_dim;
     cache.dtype = dtype;
+    cache.layout = PKV_NHD;
     return prefill_run(out, q, k, v, cache, true, total_k,
                        nullptr, max_seqlen_k / 128 + 2, cu_seq_lens_q, cu_seq_lens_k,
                        max_seqlen_q, max_seqlen_k, total_q, sink, alibi_slopes, batch,

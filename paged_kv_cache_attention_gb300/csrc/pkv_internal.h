@@ -30,6 +30,7 @@ struct DecodeParams {
     int max_blocks_per_seq, max_seqlen;
     int window_left;
     int head_dim;                // D of q, out and the pools; the kernels pad it to 64/128/256
+    int hnd;                     // pools in the HND layout (else NHD)
     int partition_size;
     int num_parts;               // grid.x: partitions per sequence the grid covers
     float scale_log2;            // sm_scale * log2(e)
@@ -54,15 +55,19 @@ struct PrefillParams {
     int window_left;
     int causal;                    // 1: keys j <= query position; 0: no upper bound
     int head_dim;                  // D <= 128; the tiles are padded to 128 with zeros
+    int hnd;                       // paged pools in the HND layout (else NHD)
     int total_k;                   // contiguous K/V: rows in the arrays (unused when paged)
     int rows_per_head;             // query tokens per 128-row tile (128 / group)
     int max_tiles;                 // capacity of the work list
     float scale_log2;
 };
 
+// hnd: pools in the HND layout; the copy then scatters each token's row by kv
+// head (head_bytes each) to page rows of block_size.
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                      void *v_cache, const int64_t *slot_mapping,
                                      int64_t num_tokens, int64_t row_bytes, int64_t capacity,
+                                     int block_size, int64_t head_bytes, bool hnd,
                                      int32_t *dev_error, cudaStream_t stream);
 
 // Returns cudaErrorNotSupported when no kernel matches the shape.
@@ -84,6 +89,8 @@ struct RopeParams {
     int64_t capacity;              // num_blocks * block_size
     int64_t max_position;
     int num_qo_heads, num_kv_heads, head_dim, rotary_dim;
+    int block_size;
+    int hnd;                       // pools in the HND layout (else NHD)
 };
 
 cudaError_t launch_rope_table(float *table, int max_position, int rotary_dim, double base,

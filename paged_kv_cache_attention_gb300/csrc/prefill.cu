@@ -32,6 +32,8 @@
 //               S, and finally normalises O (sink included) and stores it.
 // A small single-CTA kernel first builds the work list on the device
 // (counting sort by key-tile count, heaviest first).
+#include <type_traits>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 #include "pkv_tcgen05.cuh"
@@ -264,8 +266,9 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
 // ---------------------------------------------------------------------------
 // BS: rows per page of the paged pools; CONTIG: K/V are contiguous rows
 // addressed by cu_k (then BS = 128, one box per 64-dim half per tile);
-// ALIBI: the logits gain slope[head] * (key - position).
-template <int BS, bool CONTIG, bool ALIBI>
+// ALIBI: the logits gain slope[head] * (key - position); HND: paged pools in
+// the HND layout.
+template <int BS, bool CONTIG, bool ALIBI, bool HND>
 __global__ void __launch_bounds__(PfLayout::THREADS, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -326,7 +329,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                                     h * 64, geo.g * G, geo.q_start + geo.t0 + x * TPR);
             }
             const int32_t *bt = p.block_table + (int64_t)geo.r * p.max_blocks_per_seq;
-            const int oob_row = (int)(p.num_blocks * BS);
+            // box coordinates of (page, kv head): NHD (x, head, page * BS),
+            // HND (x, 0, page * Hkv + head); one past the pool reads zeros
+            const int cy = HND ? 0 : geo.g;
+            const int oob_row = HND ? (int)(p.num_blocks * p.num_kv_heads) : (int)(p.num_blocks * BS);
             const int pg0 = geo.kt_lo * NPG;       // first page of the CTA's key range
             const int npages_kv = (geo.kv_len + BS - 1) / BS;
             int ids_batch = -1, ids_row = oob_row;  // lane l: pool row of page pg0 + 32*batch + l
@@ -345,7 +351,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                         if (blk < 0 || blk >= p.num_blocks)
                             flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
                         else
-                            ids_row = blk * BS;
+                            ids_row = HND ? blk * p.num_kv_heads + geo.g : blk * BS;
                     }
                 }
                 int row = __shfl_sync(0xffffffffu, ids_row, ((rel & 31) + min(lane >> 1, NPG - 1)) & 31);
@@ -358,7 +364,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 if (lane < 2 * NPG) {
                     const int pg = lane >> 1, h = lane & 1;
                     tma_load_3d(sK + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmk,
-                                bar(Lay::B_KFULL + s), h * 64, geo.g, row);
+                                bar(Lay::B_KFULL + s), h * 64, cy, row);
                 }
                 // V
                 alive = mbar_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error);
@@ -368,7 +374,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 if (lane < 2 * NPG) {
                     const int pg = lane >> 1, h = lane & 1;
                     tma_load_3d(sV + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmv,
-                                bar(Lay::B_VFULL + s), h * 64, geo.g, row);
+                                bar(Lay::B_VFULL + s), h * 64, cy, row);
                 }
                 if (is_tail(j)) {
                     // rows at or past kv_len of the last value tile may hold any
@@ -705,16 +711,20 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, 
         kern<<<grid, PfLayout::THREADS, PfLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k, *tmap_v);
         return cudaGetLastError();
     };
-    if (p.alibi) {
-        if (contiguous) return go(prefill_tc_kernel<kTileN, true, true>);
-        if (cache.block_size == 16) return go(prefill_tc_kernel<16, false, true>);
-        if (cache.block_size == 32) return go(prefill_tc_kernel<32, false, true>);
-    } else {
-        if (contiguous) return go(prefill_tc_kernel<kTileN, true, false>);
-        if (cache.block_size == 16) return go(prefill_tc_kernel<16, false, false>);
-        if (cache.block_size == 32) return go(prefill_tc_kernel<32, false, false>);
-    }
-    return cudaErrorNotSupported;
+    auto paged = [&](auto alibi_tag) -> cudaError_t {
+        constexpr bool AL = decltype(alibi_tag)::value;
+        if (cache.block_size == 16)
+            return p.hnd ? go(prefill_tc_kernel<16, false, AL, true>)
+                         : go(prefill_tc_kernel<16, false, AL, false>);
+        if (cache.block_size == 32)
+            return p.hnd ? go(prefill_tc_kernel<32, false, AL, true>)
+                         : go(prefill_tc_kernel<32, false, AL, false>);
+        return cudaErrorNotSupported;
+    };
+    if (contiguous)
+        return p.alibi ? go(prefill_tc_kernel<kTileN, true, true, false>)
+                       : go(prefill_tc_kernel<kTileN, true, false, false>);
+    return p.alibi ? paged(std::true_type{}) : paged(std::false_type{});
 }
 
 }  // namespace pkv

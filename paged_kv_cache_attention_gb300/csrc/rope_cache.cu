@@ -229,8 +229,14 @@ rope_reshape_cache_kernel(RopeParams p) {
             const bool cache_it = slot[k] >= 0 && slot[k] < p.capacity;
             if (slot[k] >= p.capacity && first) flag_error(p.dev_error, PKV_DEVERR_SLOT);
             uint8_t *row = row_of(u);
-            uint8_t *crow = (u.kind == kVCopy ? vcb : kcb) +
-                            ((cache_it ? slot[k] : 0) * row_kv + (int64_t)u.h * p.head_dim) * ES;
+            // the slot's row of kv head h: NHD slot * row + h * D; HND
+            // ((page * Hkv + h) * bs + offset) * D
+            const int64_t sl = cache_it ? slot[k] : 0;
+            const int64_t crow_el =
+                p.hnd ? ((sl / p.block_size * p.num_kv_heads + u.h) * p.block_size +
+                         sl % p.block_size) * p.head_dim
+                      : sl * row_kv + (int64_t)u.h * p.head_dim;
+            uint8_t *crow = (u.kind == kVCopy ? vcb : kcb) + crow_el * ES;
             if (u.kind <= kKRot) {
                 const float4 *cs4 =
                     reinterpret_cast<const float4 *>(p.cos_sin + pos[k] * g.half + u.f0);

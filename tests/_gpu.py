@@ -23,17 +23,36 @@ def to_dev(t):
     return None if t is None else t.to(dev())
 
 
-def gpu_decode(case, partition_size=None, with_lse=False, err=None, max_seqlen=None):
+def to_hnd(pool):
+    """An NHD pool [num_blocks, block_size, Hkv, D] as the same pages in the
+    HND layout [num_blocks, Hkv, block_size, D] (pure re-indexing)."""
+    return pool.permute(0, 2, 1, 3).contiguous()
+
+
+def from_hnd(pool):
+    return pool.permute(0, 2, 1, 3).contiguous()
+
+
+def _pools(case, layout):
+    k, v = case.k_cache, case.v_cache
+    if layout == "HND":
+        k, v = to_hnd(k), to_hnd(v)
+    return to_dev(k), to_dev(v)
+
+
+def gpu_decode(case, partition_size=None, with_lse=False, err=None, max_seqlen=None,
+               layout="NHD"):
     d = dev()
     lse = torch.empty(case.batch, case.num_qo_heads, dtype=torch.float32, device=d) \
         if with_lse else None
-    out = pkv.paged_decode(to_dev(case.q), to_dev(case.k_cache), to_dev(case.v_cache),
+    kc, vc = _pools(case, layout)
+    out = pkv.paged_decode(to_dev(case.q), kc, vc,
                            to_dev(case.block_table), to_dev(case.cache_seqlens),
                            max_seqlen=case.max_seqlen if max_seqlen is None else max_seqlen,
                            sink=to_dev(case.sink), window_left=case.window_left,
                            sm_scale=case.sm_scale,
                            partition_size=partition_size or case.partition_size, lse=lse,
-                           dev_error=err, alibi_slopes=to_dev(case.alibi))
+                           dev_error=err, alibi_slopes=to_dev(case.alibi), layout=layout)
     torch.cuda.synchronize()
     o = out.float().cpu().numpy()
     return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o
@@ -48,16 +67,17 @@ def oracle_decode(case, rows=None, with_lse=False):
         alibi_slopes=None if case.alibi is None else case.alibi.numpy())
 
 
-def gpu_prefill(case, with_lse=False, err=None):
+def gpu_prefill(case, with_lse=False, err=None, layout="NHD"):
     d = dev()
     lse = torch.empty(case.total_q, case.q.shape[1], dtype=torch.float32, device=d) \
         if with_lse else None
-    out = pkv.varlen_prefill(to_dev(case.q), to_dev(case.k_cache), to_dev(case.v_cache),
+    kc, vc = _pools(case, layout)
+    out = pkv.varlen_prefill(to_dev(case.q), kc, vc,
                              to_dev(case.block_table), to_dev(case.cu_seq_lens_q),
                              to_dev(case.cu_seq_lens_k), case.max_seqlen_q, case.max_seqlen_k,
                              sink=to_dev(case.sink), causal=case.causal,
                              window_left=case.window_left, sm_scale=case.sm_scale, lse=lse,
-                             dev_error=err, alibi_slopes=to_dev(case.alibi))
+                             dev_error=err, alibi_slopes=to_dev(case.alibi), layout=layout)
     torch.cuda.synchronize()
     o = out.float().cpu().numpy()
     return (o, lse.cpu().numpy().astype(np.float64)) if with_lse else o

@@ -108,6 +108,9 @@ def test_decode_validation(kw, expected):
 def test_reshape_and_cache_validation():
     lib = pkv.load_library()
     f = lib.pkv_reshape_and_cache
+    bad_layout = _desc()
+    bad_layout.layout = 2
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, bad_layout, None, None) == 2
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 0, _desc(), None, None) == 0
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, _desc(), None, None) == 1
     assert f(None, FAKE, FAKE, FAKE, FAKE, 3, _desc(), None, None) == 1
