@@ -448,6 +448,37 @@ def extra_configs(dev, K, peaks):
     del q, kc, vc, outp, ws
     torch.cuda.empty_cache()
 
+    # the same lengths with head_dim 256 (16 query / 8 kv heads: the same
+    # flops), on the head_dim-256 prefill kernel
+    c4w = W.config4_prefill(16, 8, 256)
+    qw, kcw, vcw = c4w.q.to(dev), c4w.k_cache.to(dev), c4w.v_cache.to(dev)
+    btw, cqw, ckw, sinkw = (c4w.block_table.to(dev), c4w.cu_seq_lens_q.to(dev),
+                            c4w.cu_seq_lens_k.to(dev), c4w.sink.to(dev))
+    wsw = torch.empty(pkv.varlen_prefill_workspace_size(c4w.batch, 16, 8, c4w.total_q,
+                                                        c4w.max_seqlen_q),
+                      dtype=torch.uint8, device=dev)
+    outw = torch.empty_like(qw)
+
+    def gow():
+        pkv.varlen_prefill(qw, kcw, vcw, btw, cqw, ckw, c4w.max_seqlen_q, c4w.max_seqlen_k,
+                           sink=sinkw, sm_scale=c4w.sm_scale, out=outw, workspace=wsw)
+    for _ in range(3):
+        gow()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        gow()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    flw = prefill_flops(c4w)
+    tf = flw / (ms * 1e-3) / 1e12
+    out["config4_prefill_B16_D256"] = {"ms": round(ms, 4), "flops": flw, "TFLOP/s": round(tf, 1),
+                                       "frac_bf16_measured_burst": round(tf / peaks["bf16_tflops"], 3)}
+    del qw, kcw, vcw, outw, wsw
+    torch.cuda.empty_cache()
+
     # rotary embedding fused with the cache write, on the mixed step's 8448 new
     # tokens (their queries are the decode and prefill queries of the step)
     c5 = W.config5_mixed()

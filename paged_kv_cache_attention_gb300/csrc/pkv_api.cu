@@ -386,7 +386,8 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
                        float *lse_out, void *workspace, size_t workspace_bytes,
                        int32_t *dev_error, void *stream) {
     if (cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (cache.head_dim % 16 != 0 || cache.head_dim > 128) return PKV_ERR_UNSUPPORTED;
+    if (cache.head_dim % 16 != 0 || (cache.head_dim > 128 && cache.head_dim != 256))
+        return PKV_ERR_UNSUPPORTED;
     if (batch < 0 || num_qo_heads <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         total_q < 0 || max_blocks_per_seq <= 0 || window_left < -1 || !std::isfinite(sm_scale))
         return PKV_ERR_INVALID_ARG;
@@ -444,7 +445,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
         kv_rows = 1;
     }
     alignas(64) CUtensorMap tq, tk, tv;
-    const int box_rows = contiguous ? 128 : cache.block_size;
+    const int box_rows = contiguous ? (cache.head_dim == 256 ? 64 : 128) : cache.block_size;
     pkv_status st;
     if ((st = encode_rows_map(&tq, q, cache.head_dim, num_qo_heads, total_q, G, 128 / G)) !=
         PKV_OK)
@@ -506,7 +507,7 @@ pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k
     cache.dtype = dtype;
     cache.layout = PKV_NHD;
     return prefill_run(out, q, k, v, cache, true, total_k,
-                       nullptr, max_seqlen_k / 128 + 2, cu_seq_lens_q, cu_seq_lens_k,
+                       nullptr, max_seqlen_k / 64 + 2, cu_seq_lens_q, cu_seq_lens_k,
                        max_seqlen_q, max_seqlen_k, total_q, sink, alibi_slopes, batch,
                        num_qo_heads, causal, window_left, sm_scale, lse_out, workspace,
                        workspace_bytes, dev_error, stream);

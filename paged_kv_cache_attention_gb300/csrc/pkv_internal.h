@@ -54,7 +54,7 @@ struct PrefillParams {
     int max_blocks_per_seq, max_seqlen_q, max_seqlen_k, total_q;
     int window_left;
     int causal;                    // 1: keys j <= query position; 0: no upper bound
-    int head_dim;                  // D <= 128; the tiles are padded to 128 with zeros
+    int head_dim;                  // D <= 128 (tiles padded to 128 with zeros), or 256
     int hnd;                       // paged pools in the HND layout (else NHD)
     int total_k;                   // contiguous K/V: rows in the arrays (unused when paged)
     int rows_per_head;             // query tokens per 128-row tile (128 / group)
@@ -98,8 +98,16 @@ cudaError_t launch_rope_table(float *table, int max_position, int rotary_dim, do
 cudaError_t launch_rope_reshape_cache(const RopeParams &p, int dtype, bool neox,
                                       cudaStream_t stream);
 
+// head_dim 256: the attention kernel of prefill_wide.cu (64-key tiles; the
+// contiguous tensor maps use 64-row boxes).
+cudaError_t launch_prefill_wide(const PrefillParams &p, const pkv_cache_desc &cache,
+                                bool contiguous, const CUtensorMap *tmap_q,
+                                const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
+                                cudaStream_t stream);
+
 // contiguous: K/V are [total_k, Hkv, D] rows addressed by cu_k (the tensor
-// maps use 128-row boxes); otherwise paged pools of cache.block_size rows.
+// maps use 128-row boxes, 64 for head_dim 256); otherwise paged pools of
+// cache.block_size rows.
 cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, bool contiguous,
                            const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
                            const CUtensorMap *tmap_v, cudaStream_t stream);

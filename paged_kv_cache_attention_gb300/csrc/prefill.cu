@@ -37,6 +37,7 @@
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 #include "pkv_tcgen05.cuh"
+#include "prefill_common.cuh"
 
 namespace pkv {
 
@@ -84,64 +85,20 @@ struct PfLayout {
 __host__ __device__ constexpr int o_col(int x) { return x * 128; }
 __host__ __device__ constexpr int s_col(int x) { return kNQ * 128 + x * 128; }
 
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023);
-    return reinterpret_cast<uint8_t *>(a);
-}
+using pf::align1024;
+using pf::st_shared_zero16;
 
-__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
-}
-
-// Per-CTA geometry of one work item.
-struct Geo {
-    int r, t0, g;
-    int q_start, q_len, kv_len;
+// Per-CTA geometry of one work item: its request and the key tiles its two
+// query tiles attend.
+struct Geo : pf::Geo {
     int kt_lo, ntiles;
 };
-
-__device__ __forceinline__ int clip_len(int v, int cap, int32_t *err, bool report) {
-    if (v < 0) {
-        if (report) flag_error(err, PKV_DEVERR_SEQLEN);
-        return 0;
-    }
-    if (v > cap) {
-        if (report) flag_error(err, PKV_DEVERR_SEQLEN);
-        return cap;
-    }
-    return v;
-}
 
 __device__ __forceinline__ Geo make_geo(const PrefillParams &p, int4 item, int block_size,
                                         bool contiguous, bool report) {
     Geo G;
-    G.r = item.x;
-    G.t0 = item.y;
-    G.g = item.z;
-    G.q_start = p.cu_q[G.r];
-    G.q_len = clip_len(p.cu_q[G.r + 1] - G.q_start, p.max_seqlen_q, p.dev_error, report);
-    int cap_k = p.max_seqlen_k;
-    const long long cap_blocks = (long long)p.max_blocks_per_seq * block_size;
-    if (cap_blocks < cap_k) cap_k = (int)cap_blocks;
-    if (contiguous) {  // request r's key rows must lie inside the arrays
-        const int room = p.total_k - p.cu_k[G.r];
-        if (room < cap_k) cap_k = max(room, 0);
-    }
-    G.kv_len = clip_len(p.cu_k[G.r + 1] - p.cu_k[G.r], cap_k, p.dev_error, report);
-    const int tokens = kNQ * p.rows_per_head;
-    const int t_end = min(G.t0 + tokens, G.q_len);
-    const int qpos_min = G.kv_len - G.q_len + G.t0;
-    const int qpos_max = G.kv_len - G.q_len + t_end - 1;
-    const int hi = p.causal ? min(G.kv_len, qpos_max + 1) : G.kv_len;
-    int lo = 0;
-    if (p.window_left >= 0) lo = max(0, qpos_min - p.window_left);
-    if (hi <= lo || t_end <= G.t0) {
-        G.kt_lo = 0;
-        G.ntiles = 0;
-    } else {
-        G.kt_lo = lo / kTileN;
-        G.ntiles = (hi - 1) / kTileN - G.kt_lo + 1;
-    }
+    static_cast<pf::Geo &>(G) = pf::item_geo(p, item, block_size, contiguous, report);
+    pf::key_tiles(p, G, G.t0, G.t0 + kNQ * p.rows_per_head, kTileN, G.kt_lo, G.ntiles);
     return G;
 }
 
@@ -698,11 +655,14 @@ cudaError_t set_smem(K kernel, int bytes) {
 cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, bool contiguous,
                            const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
                            const CUtensorMap *tmap_v, cudaStream_t stream) {
-    if (cache.head_dim > kHeadDim || cache.head_dim % 16 != 0 || cache.dtype != PKV_BF16)
+    if (cache.dtype != PKV_BF16 || cache.head_dim % 16 != 0 ||
+        (cache.head_dim > kHeadDim && cache.head_dim != 256))
         return cudaErrorNotSupported;
     prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (cache.head_dim == 256)
+        return launch_prefill_wide(p, cache, contiguous, tmap_q, tmap_k, tmap_v, stream);
     const int grid = p.max_tiles;
     if (grid <= 0) return cudaSuccess;
     auto go = [&](auto kern) -> cudaError_t {

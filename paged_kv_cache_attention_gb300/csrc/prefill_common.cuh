@@ -1,0 +1,83 @@
+// prefill_common.cuh -- what the prefill kernels share: the geometry of a work
+// item (one request, one kv head, two query tiles of 128 GQA-packed rows) and
+// the key tiles its query rows attend.
+#pragma once
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace pf {
+
+constexpr int kItemTiles = 2;  // query tiles of 128 rows per work item
+constexpr float kNegInf = -INFINITY;
+
+struct Geo {
+    int r, t0, g;               // request, first query token, kv head
+    int q_start, q_len, kv_len;
+};
+
+__device__ __forceinline__ int clip_len(int v, int cap, int32_t *err, bool report) {
+    if (v < 0) {
+        if (report) flag_error(err, PKV_DEVERR_SEQLEN);
+        return 0;
+    }
+    if (v > cap) {
+        if (report) flag_error(err, PKV_DEVERR_SEQLEN);
+        return cap;
+    }
+    return v;
+}
+
+// The item's request lengths, clipped to the declared maxima, to the block
+// table's capacity and, for contiguous K/V, to the rows that exist.
+__device__ __forceinline__ Geo item_geo(const PrefillParams &p, int4 item, int block_size,
+                                        bool contiguous, bool report) {
+    Geo G;
+    G.r = item.x;
+    G.t0 = item.y;
+    G.g = item.z;
+    G.q_start = p.cu_q[G.r];
+    G.q_len = clip_len(p.cu_q[G.r + 1] - G.q_start, p.max_seqlen_q, p.dev_error, report);
+    int cap_k = p.max_seqlen_k;
+    const long long cap_blocks = (long long)p.max_blocks_per_seq * block_size;
+    if (cap_blocks < cap_k) cap_k = (int)cap_blocks;
+    if (contiguous) {  // request r's key rows must lie inside the arrays
+        const int room = p.total_k - p.cu_k[G.r];
+        if (room < cap_k) cap_k = max(room, 0);
+    }
+    G.kv_len = clip_len(p.cu_k[G.r + 1] - p.cu_k[G.r], cap_k, p.dev_error, report);
+    return G;
+}
+
+// Key tiles [kt_lo, kt_lo + n) of `tile` keys that hold every key the query
+// tokens [t_begin, t_end) of the request may attend (causal bound, window);
+// n = 0 when they attend none.
+__device__ __forceinline__ void key_tiles(const PrefillParams &p, const Geo &G, int t_begin,
+                                          int t_end, int tile, int &kt_lo, int &n) {
+    t_end = min(t_end, G.q_len);
+    const int qpos_min = G.kv_len - G.q_len + t_begin;
+    const int qpos_max = G.kv_len - G.q_len + t_end - 1;
+    const int hi = p.causal ? min(G.kv_len, qpos_max + 1) : G.kv_len;
+    int lo = 0;
+    if (p.window_left >= 0) lo = max(0, qpos_min - p.window_left);
+    if (hi <= lo || t_end <= t_begin) {
+        kt_lo = 0;
+        n = 0;
+    } else {
+        kt_lo = lo / tile;
+        n = (hi - 1) / tile - kt_lo + 1;
+    }
+}
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *ptr) {
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(ptr) + 1023) & ~uintptr_t(1023);
+    return reinterpret_cast<uint8_t *>(a);
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+}
+
+}  // namespace pf
+}  // namespace pkv

@@ -1,0 +1,559 @@
+// prefill_wide.cu -- varlen / chunk prefill for head_dim 256 on the
+// 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Same attention as prefill.cu (transformers docs "paged_attention", varlen
+// path; FlashInfer sink_attention_reference.py, varlen branch and
+// sink_softmax; vLLM attention.py: ALiBi, head sizes up to 256), same work
+// list (one request, one kv head, two query tiles of 128 GQA-packed rows per
+// item), same masks and numerics.  What changes with 256 dims is the budget:
+//   * an O accumulator of a 128-row tile takes 256 of the SM's 512 TMEM
+//     columns, so the two query tiles of an item run one after the other
+//     (each with its own key range), not side by side;
+//   * shared memory holds Q (64 KB) and 2-stage K and V rings of 64-key tiles
+//     (32 KB each): 192 KB;
+//   * S is double-buffered in TMEM (2 x 64 columns): the MMA issuer computes
+//     S(j+1) while the softmax warps work on S(j), so the tensor pipe is not
+//     idle during the softmax of one tile.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps
+// 2..9 softmax (two per TMEM lane quarter, each owning 32 of a row's 64 key
+// columns and 128 of its 256 output columns).
+#include <type_traits>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "pkv_tcgen05.cuh"
+#include "prefill_common.cuh"
+
+namespace pkv {
+
+namespace {
+
+using pf::kNegInf;
+
+constexpr int kD = 256;
+constexpr int kTileM = 128;
+constexpr int kTileN = 64;                 // keys per tile
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct WideLayout {
+    static constexpr int Q_BYTES = kTileM * kD * 2;       // 64 KB
+    static constexpr int Q_CHUNK = kTileM * 128;          // one 64-dim chunk: 16 KB
+    static constexpr int T_BYTES = kTileN * kD * 2;       // 32 KB per K or V tile
+    static constexpr int T_CHUNK = kTileN * 128;          // one 64-dim chunk: 8 KB
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + 2 * T_BYTES;
+    static constexpr int OFF_BAR = OFF_V + 2 * T_BYTES;
+    static constexpr int B_Q = 0;
+    static constexpr int B_QEMPTY = 1;
+    static constexpr int B_KFULL = 2;
+    static constexpr int B_KEMPTY = B_KFULL + 2;
+    static constexpr int B_VFULL = B_KEMPTY + 2;
+    static constexpr int B_VEMPTY = B_VFULL + 2;
+    // A parity wait is only valid within one phase of the barrier, so the
+    // barriers that can have two completions outstanding come in pairs:
+    // ODONE[k & 1] completes PV number k (phase k >> 1), VFIX[s] the zeroed
+    // tail of V stage s.
+    static constexpr int B_VFIX = B_VEMPTY + 2;
+    static constexpr int B_SFULL = B_VFIX + 2;
+    static constexpr int B_PFULL = B_SFULL + 2;
+    static constexpr int B_ODONE = B_PFULL + 2;
+    static constexpr int B_OFREE = B_ODONE + 2;
+    static constexpr int NBARS = B_OFREE + 1;
+    static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+    // row-max exchange [2 (tile parity)][128][2] and row-sum exchange
+    // [2 (query tile)][128][2] between the two warps of a row
+    static constexpr int OFF_XMAX = OFF_TMEM + 16;
+    static constexpr int OFF_XL = OFF_XMAX + 2 * 128 * 2 * 4;
+    static constexpr int SMEM = 1024 + OFF_XL + 2 * 128 * 2 * 4;
+    static constexpr int SOFT_THREADS = 256;
+    static constexpr int THREADS = 64 + SOFT_THREADS;
+    static constexpr int TMEM_COLS = 512;  // O: 0..255, S0: 256..319, S1: 320..383
+    static constexpr int O_COL = 0;
+};
+
+__host__ __device__ constexpr int s_col(int b) { return 256 + b * 64; }
+
+// The key tiles of query tile x of the item.
+struct TileRange {
+    int kt_lo, n;
+    bool rows;  // the tile holds at least one query row of the request
+};
+
+__device__ __forceinline__ TileRange tile_range(const PrefillParams &p, const pf::Geo &G,
+                                                int x) {
+    TileRange t;
+    const int tb = G.t0 + x * p.rows_per_head;
+    t.rows = tb < G.q_len;
+    pf::key_tiles(p, G, tb, tb + p.rows_per_head, kTileN, t.kt_lo, t.n);
+    if (!t.rows) t.n = 0;
+    return t;
+}
+
+template <int BS, bool CONTIG, bool ALIBI, bool HND>
+__global__ void __launch_bounds__(WideLayout::THREADS, 1)
+prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
+                    const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv) {
+    using Lay = WideLayout;
+    constexpr int NPG = kTileN / BS;  // pages per key tile
+
+    if ((int)blockIdx.x >= p.tiles[0]) return;  // beyond the work list
+    const int4 item = reinterpret_cast<const int4 *>(p.tiles + 64)[blockIdx.x];
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = pf::align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + Lay::OFF_Q, sK = sbase + Lay::OFF_K, sV = sbase + Lay::OFF_V;
+    const uint32_t bars = sbase + Lay::OFF_BAR;
+    auto bar = [&](int i) { return bars + 8u * i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const pf::Geo geo = pf::item_geo(p, item, BS, CONTIG, threadIdx.x == 0);
+    const TileRange tr[2] = {tile_range(p, geo, 0), tile_range(p, geo, 1)};
+    const int G = p.group;
+    const int TPR = p.rows_per_head;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Lay::NBARS; ++i)
+            mbar_init(bar(i), (i == Lay::B_PFULL || i == Lay::B_PFULL + 1 || i == Lay::B_OFREE)
+                                  ? (uint32_t)Lay::SOFT_THREADS
+                                  : 1u);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    // Key tiles in processing order (ALiBi: from the query's end backwards, so
+    // the nearest keys set the row maximum first) and the partial last tile.
+    auto tile_of = [&](int n, int j) { return ALIBI ? n - 1 - j : j; };
+    auto is_tail = [&](const TileRange &t, int j) {
+        return t.n > 0 && (t.kt_lo + t.n) * kTileN > geo.kv_len && tile_of(t.n, j) == t.n - 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const int32_t *bt = p.block_table + (int64_t)geo.r * p.max_blocks_per_seq;
+        const int cy = HND ? 0 : geo.g;
+        const int oob_row = HND ? (int)(p.num_blocks * p.num_kv_heads) : (int)(p.num_blocks * BS);
+        const int npages_kv = (geo.kv_len + BS - 1) / BS;
+        bool alive = true;
+        int kv_t = 0, q_loads = 0;
+        if (lane == 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+        }
+        for (int x = 0; x < pf::kItemTiles && alive; ++x) {
+            const TileRange t = tr[x];
+            if (t.n == 0) continue;
+            if (q_loads > 0)  // the previous tile's S products have read Q
+                alive = mbar_wait_bounded(bar(Lay::B_QEMPTY), (q_loads - 1) & 1, p.dev_error);
+            if (!alive) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(Lay::B_Q), Lay::Q_BYTES);
+                for (int c = 0; c < kD / 64; ++c)
+                    tma_load_3d(sQ + c * Lay::Q_CHUNK, &tmq, bar(Lay::B_Q), c * 64, geo.g * G,
+                                geo.q_start + geo.t0 + x * TPR);
+            }
+            ++q_loads;
+            const int pg0 = t.kt_lo * NPG;
+            int ids_batch = -1, ids_row = oob_row;
+            for (int j = 0; j < t.n && alive; ++j, ++kv_t) {
+                const int s = kv_t & 1;
+                const uint32_t ph = (kv_t >> 1) & 1;
+                const int tile = tile_of(t.n, j);
+                const int key0 = (t.kt_lo + tile) * kTileN;
+                const int rel = tile * NPG;
+                if (!CONTIG && (rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
+                    ids_batch = rel >> 5;
+                    const int pg = pg0 + ids_batch * 32 + lane;
+                    ids_row = oob_row;
+                    if (pg < npages_kv) {
+                        const int blk = bt[pg];
+                        if (blk < 0 || blk >= p.num_blocks)
+                            flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
+                        else
+                            ids_row = HND ? blk * p.num_kv_heads + geo.g : blk * BS;
+                    }
+                }
+                // lane l loads page l / 4, 64-dim chunk l % 4
+                int row = __shfl_sync(0xffffffffu, ids_row,
+                                      ((rel & 31) + min(lane >> 2, NPG - 1)) & 31);
+                if constexpr (CONTIG) row = p.cu_k[geo.r] + key0;  // rows past kv_len are masked
+                alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error);
+                if (!alive) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_KFULL + s), Lay::T_BYTES);
+                __syncwarp();
+                if (lane < 4 * NPG) {
+                    const int pg = lane >> 2, c = lane & 3;
+                    tma_load_3d(sK + s * Lay::T_BYTES + c * Lay::T_CHUNK + pg * BS * 128, &tmk,
+                                bar(Lay::B_KFULL + s), c * 64, cy, row);
+                }
+                alive = mbar_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error);
+                if (!alive) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_VFULL + s), Lay::T_BYTES);
+                __syncwarp();
+                if (lane < 4 * NPG) {
+                    const int pg = lane >> 2, c = lane & 3;
+                    tma_load_3d(sV + s * Lay::T_BYTES + c * Lay::T_CHUNK + pg * BS * 128, &tmv,
+                                bar(Lay::B_VFULL + s), c * 64, cy, row);
+                }
+                if (is_tail(t, j)) {
+                    // value rows at or past kv_len may hold any bits: zero them
+                    // so that P = 0 never meets a non-finite value
+                    alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
+                    if (!alive) break;
+                    const int first = max(geo.kv_len - key0, 0);
+                    const uint32_t vb = sV + s * Lay::T_BYTES;
+                    for (int e = first * 32 + lane; e < kTileN * 32; e += 32) {
+                        const int rr = e >> 5, c = e & 31;
+                        pf::st_shared_zero16(vb + (c >> 3) * Lay::T_CHUNK + sw128(rr, c & 7));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(Lay::B_VFIX + s));
+                }
+            }
+        }
+        // let the MMA issuer's last arrivals land before the CTA can exit
+        for (int k = max(0, kv_t - 2); k < kv_t && alive; ++k) {
+            const uint32_t ph = (k >> 1) & 1;
+            alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + (k & 1)), ph, p.dev_error) &&
+                    mbar_wait_bounded(bar(Lay::B_VEMPTY + (k & 1)), ph, p.dev_error);
+        }
+        if (alive && q_loads > 0)
+            mbar_wait_bounded(bar(Lay::B_QEMPTY), (q_loads - 1) & 1, p.dev_error);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
+            constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kD, 0, 1);
+            auto issue_s = [&](int b, int s) {
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t a =
+                        tc::smem_desc_sw128(sQ + (kk >> 2) * Lay::Q_CHUNK + off, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(
+                        sK + s * Lay::T_BYTES + (kk >> 2) * Lay::T_CHUNK + off, 16, 1024);
+                    tc::mma_ss(tmem + s_col(b), a, bd, idS, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(bar(Lay::B_SFULL + b));
+            };
+            bool alive = true;
+            int kv_t = 0, q_waits = 0, pv_cnt = 0, ofree_waits = 0;
+            int pu[2] = {0, 0}, vfix_cnt[2] = {0, 0};
+            for (int x = 0; x < pf::kItemTiles && alive; ++x) {
+                const TileRange t = tr[x];
+                if (t.n == 0) continue;
+                alive = mbar_wait_bounded(bar(Lay::B_Q), q_waits & 1, p.dev_error);
+                ++q_waits;
+                if (!alive) break;
+                tc::fence_after_sync();
+                const int base = kv_t;
+                for (int jj = 0; jj < 2 && jj < t.n && alive; ++jj) {
+                    const int tt = base + jj;
+                    alive = mbar_wait_bounded(bar(Lay::B_KFULL + (tt & 1)), (tt >> 1) & 1,
+                                              p.dev_error);
+                    if (!alive) break;
+                    tc::fence_after_sync();
+                    issue_s(jj & 1, tt & 1);
+                    tc::commit(bar(Lay::B_KEMPTY + (tt & 1)));
+                    if (jj == t.n - 1) tc::commit(bar(Lay::B_QEMPTY));
+                }
+                for (int j = 0; j < t.n && alive; ++j) {
+                    const int tt = base + j, s = tt & 1, b = j & 1;
+                    const uint32_t ph = (tt >> 1) & 1;
+                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + b), pu[b] & 1, p.dev_error);
+                    ++pu[b];
+                    if (!alive) break;
+                    if (is_tail(t, j)) {
+                        alive = mbar_wait_bounded(bar(Lay::B_VFIX + s), vfix_cnt[s] & 1,
+                                                  p.dev_error);
+                        ++vfix_cnt[s];
+                    } else {
+                        alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
+                    }
+                    if (!alive) break;
+                    if (j == 0 && pv_cnt > 0) {  // the previous tile's epilogue has read O
+                        alive = mbar_wait_bounded(bar(Lay::B_OFREE), ofree_waits & 1, p.dev_error);
+                        ++ofree_waits;
+                        if (!alive) break;
+                    }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk) {
+                        const uint64_t bd = tc::smem_desc_sw128(sV + s * Lay::T_BYTES + kk * 2048,
+                                                                Lay::T_CHUNK, 1024);
+                        tc::mma_ts(tmem + Lay::O_COL, tmem + s_col(b) + kk * 8, bd, idO,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(bar(Lay::B_ODONE + (pv_cnt & 1)));
+                    tc::commit(bar(Lay::B_VEMPTY + s));
+                    ++pv_cnt;
+                    if (j + 2 < t.n) {
+                        const int t2 = base + j + 2;
+                        alive = mbar_wait_bounded(bar(Lay::B_KFULL + (t2 & 1)), (t2 >> 1) & 1,
+                                                  p.dev_error);
+                        if (!alive) break;
+                        // P(j) lives where S(j+2) goes: PV(j) must be done
+                        const int k = pv_cnt - 1;
+                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
+                                                  p.dev_error);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                        issue_s(b, t2 & 1);
+                        tc::commit(bar(Lay::B_KEMPTY + (t2 & 1)));
+                        if (j + 2 == t.n - 1) tc::commit(bar(Lay::B_QEMPTY));
+                    }
+                }
+                kv_t += t.n;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        // Two warps per TMEM lane quarter: half hc owns key columns
+        // [32 hc, 32 hc + 32) of S, packed P columns [16 hc, 16 hc + 16) and
+        // output columns [128 hc, 128 hc + 128).
+        const int w = warp - 2;
+        const int quarter = warp & 3;
+        const int hc = w >> 2;
+        const int row = quarter * 32 + lane;
+        const int tok_local = row / G;
+        const int h_local = row - tok_local * G;
+        const int head = geo.g * G + h_local;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t pair_bar = 1 + quarter;
+        float *xmax = reinterpret_cast<float *>(smem + Lay::OFF_XMAX);
+        float *xl = reinterpret_cast<float *>(smem + Lay::OFF_XL);
+        const float sl2 = p.scale_log2;
+        const int wl = p.window_left;
+        const float al2 = ALIBI ? p.alibi[head] * kLog2e : 0.f;
+        const float sink_l2 = p.sink ? p.sink[head] * kLog2e : kNegInf;
+        bool alive = true;
+        int pv_base = 0, jg = 0;
+        int su[2] = {0, 0};
+        for (int x = 0; x < pf::kItemTiles; ++x) {
+            const TileRange t = tr[x];
+            if (!t.rows) continue;
+            const int tok = geo.t0 + x * TPR + tok_local;
+            const bool row_valid = tok < geo.q_len;
+            const int qpos = geo.kv_len - geo.q_len + tok;
+            const int cpos = p.causal ? qpos : (1 << 30);  // causal upper bound on keys
+            float m_run = kNegInf, l_run = 0.f;
+            for (int j = 0; j < t.n && alive; ++j, ++jg) {
+                const int b = j & 1;
+                alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(Lay::B_SFULL + b),
+                                                                   su[b] & 1, p.dev_error));
+                ++su[b];
+                if (!alive) break;
+                tc::fence_after_sync();
+                const int key0 = (t.kt_lo + tile_of(t.n, j)) * kTileN + hc * 32;
+                const bool full = (key0 + 31 <= cpos) && (key0 + 32 <= geo.kv_len) &&
+                                  (wl < 0 || key0 >= qpos - wl);
+                const int khi = min(cpos, geo.kv_len - 1) - key0;
+                const int klo = wl < 0 ? -1 : qpos - wl - key0;
+                uint32_t ra[32];
+                tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 32, ra);
+                tc::wait_ld();
+                if (!full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (!(i <= khi && i >= klo)) ra[i] = __float_as_uint(kNegInf);
+                }
+                float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+                if constexpr (ALIBI) {
+                    // x = s * scale + slope * (key - position), packed pairs
+                    const float b0 = al2 * (float)(key0 - qpos);
+                    const uint64_t sc2 = f2_pack(sl2, sl2), step2 = f2_pack(4.f * al2, 4.f * al2);
+                    uint64_t bc[2] = {f2_pack(b0, b0 + al2),
+                                      f2_pack(b0 + 2.f * al2, b0 + 3.f * al2)};
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]),
+                                                 __uint_as_float(ra[2 * i + 1])),
+                                         sc2, bc[i & 1]),
+                                  x0, x1);
+                        bc[i & 1] = f2_add(bc[i & 1], step2);
+                        ra[2 * i] = __float_as_uint(x0);
+                        ra[2 * i + 1] = __float_as_uint(x1);
+                        mx4[i & 3] = fmax3(mx4[i & 3], x0, x1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        mx4[i & 3] = fmax3(mx4[i & 3], __uint_as_float(ra[2 * i]),
+                                           __uint_as_float(ra[2 * i + 1]));
+                }
+                const float mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
+                float *slot = xmax + ((jg & 1) * 128 + row) * 2;
+                slot[hc] = mine;
+                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                const float mx = fmaxf(mine, slot[hc ^ 1]);
+                const float m_tile = ALIBI ? mx : mx * sl2;
+                const bool grow = m_tile > m_run + (ALIBI ? 0.f : kRescaleThreshold);
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float alpha = grow ? fast_exp2(m_run - m_tile) : 1.f;
+                    l_run *= alpha;
+                    if (j > 0) {
+                        // O is written by PV(j-1): wait for it before rescaling
+                        const int k = pv_base + j - 1;
+                        alive = __all_sync(0xffffffffu,
+                                           mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)),
+                                                             (k >> 1) & 1, p.dev_error));
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                        const uint32_t tO = tmem + lane_off + Lay::O_COL + hc * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint32_t r16[16];
+                            tc::ld_32x32b_x16(tO + c * 16, r16);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                r16[i] = __float_as_uint(__uint_as_float(r16[i]) * alpha);
+                            tc::st_32x32b_x16(tO + c * 16, r16);
+                        }
+                    }
+                    if (grow) m_run = m_tile;
+                }
+                const float msub = m_run == kNegInf ? 0.f : m_run;
+                const float psc = ALIBI ? 1.f : sl2;
+                const uint64_t scale2 = f2_pack(psc, psc), neg2 = f2_pack(-msub, -msub);
+                uint64_t ps2[2] = {0ull, 0ull};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float t0, t1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]),
+                                             __uint_as_float(ra[2 * i + 1])),
+                                     scale2, neg2),
+                              t0, t1);
+                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                    ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
+                    ra[i] = pack_bf16(p0, p1);  // packed in place: pair i -> word i
+                }
+                tc::st_32x32b_x16(tmem + lane_off + s_col(b) + hc * 16, ra);
+                float s0, s1, s2, s3;
+                f2_unpack(ps2[0], s0, s1);
+                f2_unpack(ps2[1], s2, s3);
+                l_run += (s0 + s1) + (s2 + s3);
+                tc::wait_st();
+                tc::fence_before_sync();
+                mbar_arrive(bar(Lay::B_PFULL + b));
+            }
+            // epilogue: combine the halves' sums, normalise (sink in the
+            // denominator) and store this warp's 128 output columns
+            bool have_o = t.n > 0 && alive;
+            if (have_o) {
+                // the last PV's commit covers every earlier MMA
+                const int k = pv_base + t.n - 1;
+                have_o = __all_sync(0xffffffffu,
+                                    mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
+                                                      p.dev_error));
+                tc::fence_after_sync();
+            }
+            float *lslot = xl + (x * 128 + row) * 2;
+            lslot[hc] = l_run;
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            const float l_tot = l_run + lslot[hc ^ 1];
+            const float M = fmaxf(m_run, sink_l2);
+            float oscale = 0.f, lse = kNegInf;
+            if (M != kNegInf) {
+                const float f = fast_exp2(m_run - M);
+                const float Z = l_tot * f + fast_exp2(sink_l2 - M);
+                oscale = f / Z;
+                lse = (M + log2f(Z)) * kLn2;
+            }
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) +
+                                  ((int64_t)(geo.q_start + tok) * p.num_qo_heads + head) * kD +
+                                  hc * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r32[32];
+                if (have_o) {  // warp-uniform: every lane takes part in the load
+                    tc::ld_32x32b_x32(tmem + lane_off + Lay::O_COL + hc * 128 + c * 32, r32);
+                    tc::wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r32[i] = 0u;
+                }
+                if (row_valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int e = 8 * i;
+                        dst[i] = make_uint4(
+                            pack_bf16(__uint_as_float(r32[e + 0]) * oscale,
+                                      __uint_as_float(r32[e + 1]) * oscale),
+                            pack_bf16(__uint_as_float(r32[e + 2]) * oscale,
+                                      __uint_as_float(r32[e + 3]) * oscale),
+                            pack_bf16(__uint_as_float(r32[e + 4]) * oscale,
+                                      __uint_as_float(r32[e + 5]) * oscale),
+                            pack_bf16(__uint_as_float(r32[e + 6]) * oscale,
+                                      __uint_as_float(r32[e + 7]) * oscale));
+                    }
+                }
+            }
+            if (row_valid && hc == 0 && p.lse_out)
+                p.lse_out[(int64_t)(geo.q_start + tok) * p.num_qo_heads + head] = lse;
+            if (t.n > 0) {
+                tc::fence_before_sync();
+                mbar_arrive(bar(Lay::B_OFREE));  // O may be overwritten by the next tile
+            }
+            pv_base += t.n;
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, Lay::TMEM_COLS);
+    }
+}
+
+template <typename K>
+cudaError_t set_smem_wide(K kernel, int bytes) {
+    return ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_wide(const PrefillParams &p, const pkv_cache_desc &cache,
+                                bool contiguous, const CUtensorMap *tmap_q,
+                                const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
+                                cudaStream_t stream) {
+    const int grid = p.max_tiles;
+    if (grid <= 0) return cudaSuccess;
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = set_smem_wide(kern, WideLayout::SMEM);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, WideLayout::THREADS, WideLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k,
+                                                                      *tmap_v);
+        return cudaGetLastError();
+    };
+    auto paged = [&](auto alibi_tag) -> cudaError_t {
+        constexpr bool AL = decltype(alibi_tag)::value;
+        if (cache.block_size == 16)
+            return p.hnd ? go(prefill_wide_kernel<16, false, AL, true>)
+                         : go(prefill_wide_kernel<16, false, AL, false>);
+        if (cache.block_size == 32)
+            return p.hnd ? go(prefill_wide_kernel<32, false, AL, true>)
+                         : go(prefill_wide_kernel<32, false, AL, false>);
+        return cudaErrorNotSupported;
+    };
+    if (contiguous)
+        return p.alibi ? go(prefill_wide_kernel<kTileN, true, true, false>)
+                       : go(prefill_wide_kernel<kTileN, true, false, false>);
+    return p.alibi ? paged(std::true_type{}) : paged(std::false_type{});
+}
+
+}  // namespace pkv

@@ -384,13 +384,17 @@ def config3_lengths() -> List[int]:
     return uniform_int(32768, 131072, 8, _gen(seed_for(3))).tolist()
 
 
-def config4_prefill() -> VarlenCase:
+def config4_prefill(num_qo_heads: int = 32, num_kv_heads: int = 8,
+                    head_dim: int = 128) -> VarlenCase:
+    """B16 varlen prefill: q ~ U[1, 2048], prefix ~ U[0, 8192] (the lengths do
+    not depend on the head shape; head_dim 256 with 16 query heads is the
+    same work as 128 with 32)."""
     gen = _gen(seed_for(4))
     ql = uniform_int(1, 2048, 16, gen).tolist()
     pl = uniform_int(0, 8192, 16, gen).tolist()
-    return make_varlen(ql, pl, 32, 8, 128, 16, torch.bfloat16, seed_for(4) + 100,
-                       sink="randn", window_left=-1, sm_scale=1.0 / math.sqrt(128),
-                       name="config4")
+    return make_varlen(ql, pl, num_qo_heads, num_kv_heads, head_dim, 16, torch.bfloat16,
+                       seed_for(4) + 100, sink="randn", window_left=-1,
+                       sm_scale=1.0 / math.sqrt(head_dim), name="config4")
 
 
 @dataclass

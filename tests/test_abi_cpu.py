@@ -123,7 +123,7 @@ def test_reshape_and_cache_validation():
 @nogpu
 @pytest.mark.parametrize("change,expected", [
     (dict(window=-2), 1),
-    (dict(d=256), 2),               # prefill tiles stop at head_dim 128
+    (dict(d=512), 2),               # no prefill kernel for head_dim 512
     (dict(d=72), 2),
     (dict(dtype=0), 2),             # fp32 prefill not in this version
     (dict(hq=24), 2),               # group of 3 (not a power of two)
@@ -148,7 +148,7 @@ def test_prefill_validation(change, expected):
     (dict(dtype=3), 2),
     (dict(dtype=0), 2),             # fp32 prefill not in this version
     (dict(d=72), 2),                # not a multiple of 16
-    (dict(d=256), 2),               # prefill tiles stop at 128
+    (dict(d=512), 2),               # no kernel for head_dim 512
     (dict(hq=24), 2),               # group of 3 (not a power of two)
     (dict(hq=12), 1),               # not a multiple of num_kv_heads
     (dict(k=None), 1),              # keys missing although total_k > 0

@@ -247,6 +247,56 @@ def test_head_sizes_contiguous_non_causal(D):
     _check_contig(case, pad_rows=32)
 
 
+# ---------------------------------------------------------------------------
+# head size 256 (its own kernel: query tiles in sequence, 64-key tiles)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("G,Hkv,bs", [(4, 4, 16), (1, 8, 32), (16, 1, 16), (2, 2, 32)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_size_256(G, Hkv, bs, causal):
+    q_lens = [1, 7, 64, 130, 300, 5]
+    kv_lens = [1, 900, 64, 130, 700, 0]
+    case = W.make_varlen_kv(q_lens, kv_lens, G * Hkv, Hkv, 256, bs, BF16, seed=G * 5 + bs,
+                            sink="randn", causal=causal)
+    _check(case)
+
+
+@pytest.mark.parametrize("window,alibi", [(0, "none"), (100, "uniform"), (-1, "steep")])
+def test_head_size_256_windows_alibi(window, alibi):
+    case = W.make_varlen([1, 33, 129, 250], [0, 300, 128, 1000], 16, 4, 256, 16, BF16,
+                         seed=window + 7, sink="randn", window_left=window, alibi=alibi)
+    _check(case)
+
+
+def test_head_size_256_q_longer_than_kv():
+    """Rows at negative positions in the first query tile attend nothing while
+    the second tile has keys: the tiles of an item run with their own ranges."""
+    case = W.make_varlen_kv([200, 3], [70, 1], 8, 2, 256, 16, BF16, seed=141, sink="randn")
+    _check(case)
+
+
+def test_head_size_256_contiguous_and_hnd():
+    case = W.make_varlen_kv([5, 127, 300], [5, 1000, 300], 16, 4, 256, 16, BF16, seed=142,
+                            sink="randn", alibi="geometric")
+    _check_contig(case, pad_rows=64)
+    got = gpu_prefill(case, layout="HND")
+    assert max_abs(got, oracle_prefill(case)) <= TOL[BF16]
+    assert np.array_equal(got, gpu_prefill(case))
+
+
+def test_head_size_256_decode_equals_prefill():
+    dec = W.make_decode([1, 300, 1024, 2049], 16, 4, 256, 16, BF16, seed=143, sink="randn",
+                        window_left=700)
+    B = dec.batch
+    var = W.VarlenCase("as-prefill", dec.q, dec.k_cache, dec.v_cache, dec.block_table,
+                       W.cumsum0(torch.ones(B, dtype=torch.int32)),
+                       W.cumsum0(dec.cache_seqlens), dec.sink, dec.window_left, dec.sm_scale)
+    a = gpu_decode(dec)
+    b = gpu_prefill(var)
+    assert np.abs(a - b).max() <= 2e-2
+    assert max_abs(b, oracle_decode(dec)) <= TOL[BF16]
+
+
 def test_decode_equals_prefill_with_one_query():
     """Cross-op: paged_decode == varlen_prefill with q_len = 1 per request."""
     dec = W.make_decode([1, 300, 1024, 4097], 32, 8, 128, 16, BF16, seed=23, sink="randn",
