@@ -175,7 +175,7 @@ __device__ __forceinline__ Unit locate(const RopeParams &p, const Geometry &g, u
 // every head of the token and is read (from L1, mostly) while rotating.
 constexpr int kUnits = 1;
 
-template <typename T, bool NEOX>
+template <typename T, bool NEOX, bool HND>
 __global__ void __launch_bounds__(kThreads)
 rope_reshape_cache_kernel(RopeParams p) {
     using VT = Vec<T>;
@@ -232,10 +232,12 @@ rope_reshape_cache_kernel(RopeParams p) {
             // the slot's row of kv head h: NHD slot * row + h * D; HND
             // ((page * Hkv + h) * bs + offset) * D
             const int64_t sl = cache_it ? slot[k] : 0;
-            const int64_t crow_el =
-                p.hnd ? ((sl / p.block_size * p.num_kv_heads + u.h) * p.block_size +
-                         sl % p.block_size) * p.head_dim
-                      : sl * row_kv + (int64_t)u.h * p.head_dim;
+            int64_t crow_el;
+            if constexpr (HND)
+                crow_el = ((sl / p.block_size * p.num_kv_heads + u.h) * p.block_size +
+                           sl % p.block_size) * p.head_dim;
+            else
+                crow_el = sl * row_kv + (int64_t)u.h * p.head_dim;
             uint8_t *crow = (u.kind == kVCopy ? vcb : kcb) + crow_el * ES;
             if (u.kind <= kKRot) {
                 const float4 *cs4 =
@@ -344,18 +346,30 @@ cudaError_t launch_rope_reshape_cache(const RopeParams &p, int dtype, bool neox,
             return cudaGetLastError();
         };
         cudaError_t e;
-        if (dtype == PKV_F32)
-            e = neox ? go(std::integral_constant<decltype(&rope_reshape_cache_kernel<float, true>),
-                                                 &rope_reshape_cache_kernel<float, true>>{})
-                     : go(std::integral_constant<decltype(&rope_reshape_cache_kernel<float, false>),
-                                                 &rope_reshape_cache_kernel<float, false>>{});
-        else
-            e = neox ? go(std::integral_constant<
-                             decltype(&rope_reshape_cache_kernel<__nv_bfloat16, true>),
-                             &rope_reshape_cache_kernel<__nv_bfloat16, true>>{})
-                     : go(std::integral_constant<
-                             decltype(&rope_reshape_cache_kernel<__nv_bfloat16, false>),
-                             &rope_reshape_cache_kernel<__nv_bfloat16, false>>{});
+        if (dtype == PKV_F32) {
+            if (neox)
+                e = p.hnd ? go(std::integral_constant<decltype(&rope_reshape_cache_kernel<float, true, true>),
+                                                      &rope_reshape_cache_kernel<float, true, true>>{})
+                          : go(std::integral_constant<decltype(&rope_reshape_cache_kernel<float, true, false>),
+                                                      &rope_reshape_cache_kernel<float, true, false>>{});
+            else
+                e = p.hnd ? go(std::integral_constant<decltype(&rope_reshape_cache_kernel<float, false, true>),
+                                                      &rope_reshape_cache_kernel<float, false, true>>{})
+                          : go(std::integral_constant<decltype(&rope_reshape_cache_kernel<float, false, false>),
+                                                      &rope_reshape_cache_kernel<float, false, false>>{});
+        } else {
+            using B16 = __nv_bfloat16;
+            if (neox)
+                e = p.hnd ? go(std::integral_constant<decltype(&rope_reshape_cache_kernel<B16, true, true>),
+                                                      &rope_reshape_cache_kernel<B16, true, true>>{})
+                          : go(std::integral_constant<decltype(&rope_reshape_cache_kernel<B16, true, false>),
+                                                      &rope_reshape_cache_kernel<B16, true, false>>{});
+            else
+                e = p.hnd ? go(std::integral_constant<decltype(&rope_reshape_cache_kernel<B16, false, true>),
+                                                      &rope_reshape_cache_kernel<B16, false, true>>{})
+                          : go(std::integral_constant<decltype(&rope_reshape_cache_kernel<B16, false, false>),
+                                                      &rope_reshape_cache_kernel<B16, false, false>>{});
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
