@@ -20,6 +20,7 @@ Definitions followed (page title, section):
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -77,6 +78,14 @@ def _load():
                                         ctypes.c_int, ctypes.c_double, ctypes.c_double,
                                         ctypes.c_int]
             lib.oracle_rope.restype = None
+            lib.oracle_minference_scores.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_double]
+            lib.oracle_minference_scores.restype = None
+            lib.oracle_sparse_attention.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                                    ctypes.c_int, P, ctypes.c_int, ctypes.c_double]
+            lib.oracle_sparse_attention.restype = None
             lib.oracle_online_cores.argtypes = []
             lib.oracle_online_cores.restype = ctypes.c_int
             _ = i32
@@ -206,3 +215,81 @@ def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, sink=None,
     return attention(q, k_cache, v_cache, block_table, cu, cache_seqlens, sink=sink,
                      causal=True, window_left=window_left, sm_scale=sm_scale, rows=rows,
                      threads=threads, with_lse=with_lse, alibi_slopes=alibi_slopes)
+
+
+# ---------------------------------------------------------------------------
+# MInference vertical + slash sparse prefill (nano-vllm minference.py)
+# ---------------------------------------------------------------------------
+
+def minference_sizes(seq_len: int, vertical_size: int = 1000, slash_size: int = 6096,
+                     adaptive_budget=0.3, num_sink_tokens: int = 30,
+                     num_recent_diags: int = 100):
+    """Numbers of vertical and slash indices kept (MInferencePolicy
+    .estimate_pattern): with an adaptive budget b = int(S * budget) they are
+    max(num_sink + 1, int(0.2 b)) and max(num_recent + 1, int(0.8 b)); both
+    are capped at S."""
+    if adaptive_budget is not None:
+        budget = int(seq_len * adaptive_budget)
+        vertical_size = max(num_sink_tokens + 1, int(budget * 0.2))
+        slash_size = max(num_recent_diags + 1, int(budget * 0.8))
+    return min(vertical_size, seq_len), min(slash_size, seq_len)
+
+
+def minference_scores(q, k, last_q: int = 64, scale=None):
+    """(vertical [Hq, S], slash [Hq, S]) fp64 pattern scores of the last
+    min(last_q, S) queries (see oracle_minference_scores)."""
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    lq = min(last_q, S)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    vert = np.zeros((Hq, S), np.float64)
+    sl = np.zeros((Hq, S), np.float64)
+    _load().oracle_minference_scores(_ptr(vert), _ptr(sl), _ptr(q), _ptr(k), _dtype_code(q), S,
+                                     Hq, Hkv, D, lq, sc)
+    return vert, sl
+
+
+def topk_sorted(scores, k: int, n_force: int):
+    """The page's selection: the first n_force entries forced to +inf, the k
+    largest kept (equal values: lower index first), returned in ascending
+    index order.  scores: [H, S]; returns int32 [H, k]."""
+    sc = np.array(scores, np.float64, copy=True)
+    sc[:, :n_force] = np.inf
+    H, S = sc.shape
+    out = np.empty((H, k), np.int32)
+    for h in range(H):
+        order = np.lexsort((np.arange(S), -sc[h]))  # by value descending, then index
+        out[h] = np.sort(order[:k])
+    return out
+
+
+def minference_pattern(q, k, last_q: int = 64, scale=None, vertical_size: int = 1000,
+                       slash_size: int = 6096, adaptive_budget=0.3, num_sink_tokens: int = 30,
+                       num_recent_diags: int = 100):
+    """(vertical_indices [Hq, nv], slash_indices [Hq, ns], vertical_scores,
+    slash_scores): the estimate_pattern steps in fp64."""
+    S = q.shape[0]
+    nv, ns = minference_sizes(S, vertical_size, slash_size, adaptive_budget, num_sink_tokens,
+                              num_recent_diags)
+    vsc, ssc = minference_scores(q, k, last_q, scale)
+    return (topk_sorted(vsc, nv, num_sink_tokens), topk_sorted(ssc, ns, num_recent_diags),
+            vsc, ssc)
+
+
+def sparse_attention(q, k, v, vertical_indices, slash_indices, scale=None):
+    """Vertical + slash sparse causal attention of one sequence, fp64
+    [S, Hq, D] (see oracle_sparse_attention)."""
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    vi = np.ascontiguousarray(vertical_indices, dtype=np.int32)
+    si = np.ascontiguousarray(slash_indices, dtype=np.int32)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    out = np.zeros((S, Hq, D), np.float64)
+    _load().oracle_sparse_attention(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), S, Hq,
+                                    Hkv, D, _ptr(vi), vi.shape[1], _ptr(si), si.shape[1], sc)
+    return out

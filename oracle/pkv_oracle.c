@@ -324,3 +324,105 @@ void oracle_rope(double *out, const void *x, int dtype, int64_t num_tokens, int 
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* MInference vertical + slash sparse prefill                                */
+/* ------------------------------------------------------------------------ */
+
+/* Pattern scores (nano-vllm minference.py, MInferencePolicy.estimate_pattern):
+ * the last `last_q` queries of a sequence of S tokens (positions
+ * S - last_q .. S - 1) attend causally to all keys; each row's softmax
+ * probabilities p_i(j) are summed
+ *   - per key column:   vertical[h][j] = sum_i p_i(j)
+ *   - per diagonal:     slash[h][d]    = sum_i p_i(pos_i - d),  d = pos_i - j.
+ * q: [S, Hq, D], k: [S, Hkv, D] (query head h reads kv head h / (Hq / Hkv));
+ * the logit is scale * <q, k>.  vertical, slash: [Hq, S] fp64 outputs. */
+void oracle_minference_scores(double *vertical, double *slash, const void *q, const void *k,
+                              int dtype, int S, int num_qo_heads, int num_kv_heads,
+                              int head_dim, int last_q, double scale) {
+    const int Hq = num_qo_heads, Hkv = num_kv_heads, D = head_dim;
+    const int group = Hq / Hkv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    for (int h = 0; h < Hq; ++h) {
+        const int kvh = h / group;
+        double *vh = vertical + (int64_t)h * S, *sh = slash + (int64_t)h * S;
+        for (int j = 0; j < S; ++j) vh[j] = sh[j] = 0.0;
+        for (int i = 0; i < last_q; ++i) {
+            const int pos = S - last_q + i;
+            const int64_t qb = ((int64_t)pos * Hq + h) * D;
+            double m = -INFINITY;
+            for (int j = 0; j <= pos; ++j) {
+                const int64_t kb = ((int64_t)j * Hkv + kvh) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += widen(q, dtype, qb + d) * widen(k, dtype, kb + d);
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double z = 0.0;
+            for (int j = 0; j <= pos; ++j) z += exp(s[j] - m);
+            for (int j = 0; j <= pos; ++j) {
+                const double p = exp(s[j] - m) / z;
+                vh[j] += p;
+                sh[pos - j] += p;
+            }
+        }
+    }
+    free(s);
+}
+
+/* Vertical + slash sparse attention of one sequence (the attention the
+ * pattern selects): query row i (position i) keeps key j iff j <= i and
+ * (j is a vertical index of its head, or i - j is a slash index of its
+ * head); softmax over the kept keys, o = sum p v.  A row that keeps no key
+ * gets 0.  vert: [Hq, nv] and slash_idx: [Hq, ns] key / diagonal indices.
+ * out: [S, Hq, D] fp64. */
+void oracle_sparse_attention(double *out, const void *q, const void *k, const void *v, int dtype,
+                             int S, int num_qo_heads, int num_kv_heads, int head_dim,
+                             const int32_t *vert, int nv, const int32_t *slash_idx, int ns,
+                             double scale) {
+    const int Hq = num_qo_heads, Hkv = num_kv_heads, D = head_dim;
+    const int group = Hq / Hkv;
+    uint8_t *isv = (uint8_t *)calloc((size_t)(S > 0 ? S : 1), 1);
+    uint8_t *iss = (uint8_t *)calloc((size_t)(S > 0 ? S : 1), 1);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    for (int h = 0; h < Hq; ++h) {
+        const int kvh = h / group;
+        memset(isv, 0, (size_t)S);
+        memset(iss, 0, (size_t)S);
+        for (int a = 0; a < nv; ++a) {
+            const int j = vert[(int64_t)h * nv + a];
+            if (j >= 0 && j < S) isv[j] = 1;
+        }
+        for (int a = 0; a < ns; ++a) {
+            const int d = slash_idx[(int64_t)h * ns + a];
+            if (d >= 0 && d < S) iss[d] = 1;
+        }
+        for (int i = 0; i < S; ++i) {
+            double *o = out + ((int64_t)i * Hq + h) * D;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            const int64_t qb = ((int64_t)i * Hq + h) * D;
+            double m = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                if (!(isv[j] || iss[i - j])) { s[j] = -INFINITY; continue; }
+                const int64_t kb = ((int64_t)j * Hkv + kvh) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += widen(q, dtype, qb + d) * widen(k, dtype, kb + d);
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            if (m == -INFINITY) continue;
+            double z = 0.0;
+            for (int j = 0; j <= i; ++j)
+                if (s[j] != -INFINITY) z += exp(s[j] - m);
+            for (int j = 0; j <= i; ++j) {
+                if (s[j] == -INFINITY) continue;
+                const double p = exp(s[j] - m) / z;
+                const int64_t vb = ((int64_t)j * Hkv + kvh) * D;
+                for (int d = 0; d < D; ++d) o[d] += p * widen(v, dtype, vb + d);
+            }
+        }
+    }
+    free(isv);
+    free(iss);
+    free(s);
+}

@@ -63,6 +63,12 @@ MUTATIONS = {
     "alibi: bias scaled by sm_scale": (
         "if (J->alibi) s_buf[j] += (double)J->alibi[h]",
         "if (J->alibi) s_buf[j] += J->sm_scale * (double)J->alibi[h]"),
+    "minference: slash summed per key, not per diagonal": (
+        "sh[pos - j] += p;", "sh[j] += p;"),
+    "minference: estimating queries taken from the start": (
+        "const int pos = S - last_q + i;", "const int pos = i;"),
+    "sparse attention: vertical and slash intersected": (
+        "if (!(isv[j] || iss[i - j]))", "if (!(isv[j] && iss[i - j]))"),
     "cache write ignores the skip marker": (
         "if (s < 0) continue;", "if (s < -1) continue;"),
 }

@@ -518,3 +518,132 @@ def test_alibi_identical_keys_give_geometric_weights():
                               alibi_slopes=np.array([slope], np.float32))
     w = np.exp(np.float64(np.float32(slope)) * np.arange(L))
     np.testing.assert_allclose(out[0, 0, :L], w / w.sum(), rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# MInference vertical + slash sparse prefill
+# ---------------------------------------------------------------------------
+
+def _numpy_pattern_scores(q, k, last_q, scale):
+    """Independent dense statement: softmax rows of the last queries (causal),
+    summed per key column and per diagonal pos - j."""
+    S, Hq, D = q.shape
+    G = Hq // k.shape[1]
+    kk = np.repeat(k.astype(np.float64), G, axis=1)
+    lq = min(last_q, S)
+    pos = np.arange(S - lq, S)
+    qk = np.einsum("qhd,khd->hqk", q[S - lq:].astype(np.float64), kk) * scale
+    col = np.arange(S)[None, :]
+    qk = np.where((col <= pos[:, None])[None], qk, -np.inf)
+    p = np.exp(qk - qk.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    vert = p.sum(1)
+    slash = np.zeros((Hq, S))
+    diag = np.broadcast_to(pos[:, None] - col, (lq, S))
+    for h in range(Hq):
+        ok = col.repeat(lq, 0) <= pos[:, None]
+        np.add.at(slash[h], diag[ok], p[h][ok])
+    return vert, slash
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D", [(200, 4, 2, 16), (64, 2, 1, 32), (37, 4, 4, 8),
+                                        (130, 8, 2, 16)])
+def test_minference_scores_match_numpy(S, Hq, Hkv, D):
+    rng = np.random.default_rng(S + Hq)
+    q = rng.standard_normal((S, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((S, Hkv, D)).astype(np.float32)
+    scale = 1.0 / math.sqrt(D)
+    vert, slash = oracle.minference_scores(q, k, 64, scale)
+    rv, rs = _numpy_pattern_scores(q, k, 64, scale)
+    np.testing.assert_allclose(vert, rv, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(slash, rs, rtol=0, atol=1e-12)
+    # each softmax row sums to one: both score vectors sum to the number of
+    # estimating queries
+    np.testing.assert_allclose(vert.sum(1), min(64, S), rtol=1e-12)
+    np.testing.assert_allclose(slash.sum(1), min(64, S), rtol=1e-12)
+
+
+def test_minference_sizes_follow_the_budget():
+    # S = 1000, budget 0.3: b = 300, vertical max(31, 60), slash max(101, 240)
+    assert oracle.minference_sizes(1000) == (60, 240)
+    # S = 100: b = 30; the floors 31 and 101, the latter capped at S
+    assert oracle.minference_sizes(100) == (31, 100)
+    # no adaptive budget: the fixed sizes, capped at S
+    assert oracle.minference_sizes(5000, adaptive_budget=None) == (1000, 5000)
+    assert oracle.minference_sizes(20000, adaptive_budget=None) == (1000, 6096)
+
+
+def test_minference_selection_keeps_sinks_and_recent_diagonals():
+    rng = np.random.default_rng(23)
+    S = 500
+    q = rng.standard_normal((S, 4, 16)).astype(np.float32)
+    k = rng.standard_normal((S, 2, 16)).astype(np.float32)
+    vi, si, vs, ss = oracle.minference_pattern(q, k)
+    nv, ns = oracle.minference_sizes(S)
+    assert vi.shape == (4, nv) and si.shape == (4, ns)
+    for h in range(4):
+        assert np.all(np.diff(vi[h]) > 0) and np.all(np.diff(si[h]) > 0)  # sorted, unique
+        assert set(range(30)) <= set(vi[h].tolist())
+        assert set(range(100)) <= set(si[h].tolist())
+        # every kept (unforced) index scores at least as much as every dropped one
+        free_v = [j for j in vi[h] if j >= 30]
+        drop_v = np.setdiff1d(np.arange(30, S), vi[h])
+        assert vs[h][free_v].min() >= vs[h][drop_v].max()
+        free_s = [d for d in si[h] if d >= 100]
+        drop_s = np.setdiff1d(np.arange(100, S), si[h])
+        assert ss[h][free_s].min() >= ss[h][drop_s].max()
+
+
+def test_sparse_attention_with_every_key_vertical_is_dense_causal():
+    rng = np.random.default_rng(24)
+    S, Hq, Hkv, D = 90, 4, 2, 16
+    q = rng.standard_normal((S, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((S, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((S, Hkv, D)).astype(np.float32)
+    allv = np.tile(np.arange(S, dtype=np.int32), (Hq, 1))
+    none_s = np.zeros((Hq, 0), np.int32)
+    out = oracle.sparse_attention(q, k, v, allv, none_s, scale=0.25)
+    kp, vp, bt = paginate([k], [v], 8, rng)
+    ref = oracle.attention(q, kp, vp, bt, cu([S]), np.array([S], np.int32), causal=True,
+                           sm_scale=0.25)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    # every diagonal as a slash line is the same mask
+    alls = np.tile(np.arange(S, dtype=np.int32), (Hq, 1))
+    out2 = oracle.sparse_attention(q, k, v, np.zeros((Hq, 0), np.int32), alls, scale=0.25)
+    np.testing.assert_allclose(out2, ref, rtol=0, atol=1e-12)
+
+
+def test_sparse_attention_main_diagonal_only_returns_own_value():
+    rng = np.random.default_rng(25)
+    S, Hq, Hkv, D = 40, 4, 2, 8
+    q = rng.standard_normal((S, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((S, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((S, Hkv, D)).astype(np.float32)
+    out = oracle.sparse_attention(q, k, v, np.zeros((Hq, 0), np.int32),
+                                  np.zeros((Hq, 1), np.int32))
+    np.testing.assert_array_equal(out, np.repeat(v.astype(np.float64), 2, axis=1))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_sparse_attention_matches_numpy_bruteforce(seed):
+    rng = np.random.default_rng(30 + seed)
+    S, Hq, Hkv, D = 70, 4, 2, 16
+    q = rng.standard_normal((S, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((S, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((S, Hkv, D)).astype(np.float32)
+    vi = np.sort(np.stack([rng.choice(S, 9, replace=False) for _ in range(Hq)]), 1).astype(np.int32)
+    si = np.sort(np.stack([rng.choice(S, 13, replace=False) for _ in range(Hq)]), 1).astype(np.int32)
+    out = oracle.sparse_attention(q, k, v, vi, si, scale=0.3)
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    kk = np.repeat(k.astype(np.float64), 2, axis=1)
+    vv = np.repeat(v.astype(np.float64), 2, axis=1)
+    for h in range(Hq):
+        keep = (j <= i) & (np.isin(j, vi[h]) | np.isin(i - j, si[h]))
+        s = np.where(keep, q[:, h].astype(np.float64) @ kk[:, h].T * 0.3, -np.inf)
+        m = s.max(1, keepdims=True)
+        m = np.where(np.isfinite(m), m, 0.0)
+        e = np.exp(s - m)
+        z = e.sum(1, keepdims=True)
+        ref = np.where(z > 0, (e @ vv[:, h]) / np.where(z > 0, z, 1), 0.0)
+        np.testing.assert_allclose(out[:, h], ref, rtol=0, atol=1e-12)
