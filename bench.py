@@ -31,6 +31,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -210,6 +212,23 @@ def rope_bytes(num_tokens, Hq, Hkv, D, rotary_dim, elem_bytes):
     position) is not counted."""
     per_token = elem_bytes * (2 * Hq * rotary_dim + Hkv * (2 * D + rotary_dim) + 2 * Hkv * D)
     return num_tokens * (per_token + 16)
+
+
+def sparse_kept_pairs(seq_len, vertical, slash):
+    """Causal (query, key) pairs the vertical + slash pattern keeps, summed
+    over heads: per row i, |V <= i| + |S <= i| - |{j in V: i - j in S}|, the
+    last term a convolution of the two indicator vectors (FFT, rounded)."""
+    S = int(seq_len)
+    total = 0
+    n = 1 << (2 * S - 1).bit_length()
+    for vh, sh in zip(vertical, slash):
+        v = np.zeros(S)
+        v[np.asarray(vh)] = 1.0
+        d = np.zeros(S)
+        d[np.asarray(sh)] = 1.0
+        both = np.rint(np.fft.irfft(np.fft.rfft(v, n) * np.fft.rfft(d, n), n)[:S])
+        total += int(np.cumsum(v).sum() + np.cumsum(d).sum() - both.sum())
+    return total
 
 
 def time_flushed(fn, K, flush):
@@ -477,6 +496,35 @@ def extra_configs(dev, K, peaks):
     out["config4_prefill_B16_D256"] = {"ms": round(ms, 4), "flops": flw, "TFLOP/s": round(tf, 1),
                                        "frac_bf16_measured_burst": round(tf / peaks["bf16_tflops"], 3)}
     del qw, kcw, vcw, outw, wsw
+    torch.cuda.empty_cache()
+
+    # MInference vertical + slash sparse prefill of one 32K-token sequence
+    # whose attention has local (slash) and stripe (vertical) structure
+    # (default budget 0.3), against the dense causal prefill of the same one
+    S = 32768
+    qm, km, vm = (t.to(dev) for t in W.make_long_sequence(S, 32, 8, 128, W.seed_for(6)))
+    outm = torch.empty_like(qm)
+    wsm = torch.empty(pkv.lib_minference_workspace(S, 32, 8), dtype=torch.uint8, device=dev)
+    _, vim, sim = pkv.minference_prefill(qm, km, vm, out=outm, workspace=wsm,
+                                         return_pattern=True)
+    cum = torch.tensor([0, S], dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ms_sparse = time_flushed(lambda: pkv.minference_prefill(qm, km, vm, out=outm, workspace=wsm),
+                             max(3, K // 10), flush)
+    ms_dense = time_flushed(lambda: pkv.varlen_prefill_contiguous(qm, km, vm, cum, cum, S, S,
+                                                                  out=outm),
+                            max(3, K // 10), flush)
+    kept = sparse_kept_pairs(S, vim.cpu().numpy(), sim.cpu().numpy())
+    fl_kept = 4 * 128 * kept  # per kept (query, key) pair of a head: QK^T and PV
+    fl_dense = 4 * 128 * 32 * (S * (S + 1) // 2)
+    out["minference_prefill_S32K_Hq32_D128"] = {
+        "ms": round(ms_sparse, 4), "dense_ms": round(ms_dense, 4),
+        "speedup_vs_dense": round(ms_dense / ms_sparse, 3),
+        "kept_pair_fraction": round(kept / (32 * S * (S + 1) // 2), 4),
+        "TFLOP/s_on_kept_pairs": round(fl_kept / (ms_sparse * 1e-3) / 1e12, 1),
+        "dense_TFLOP/s": round(fl_dense / (ms_dense * 1e-3) / 1e12, 1),
+        "l2": "256 MB buffer written before each timed launch"}
+    del qm, km, vm, outm, wsm, flush
     torch.cuda.empty_cache()
 
     # rotary embedding fused with the cache write, on the mixed step's 8448 new

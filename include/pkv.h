@@ -11,6 +11,8 @@
  *   pkv_rope_reshape_and_cache  the same write preceded by the rotary
  *                          position embedding of query and key
  *                          (vLLM attention.py, PagedAttentionWithRoPE);
+ *   pkv_minference_prefill vertical + slash sparse prefill of one sequence
+ *                          (nano-vllm minference.py);
  *   pkv_paged_decode       one query token per sequence, attending to positions
  *                          0 .. cache_seqlens[b]-1 gathered through block_table
  *                          (transformers docs "paged_attention", decode path;
@@ -286,6 +288,51 @@ PKV_API pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const
                                                  float sm_scale, float *lse_out,
                                                  void *workspace, size_t workspace_bytes,
                                                  int32_t *dev_error, void *stream);
+
+/*
+ * MInference vertical + slash sparse prefill of one sequence (nano-vllm
+ * minference.py, MInferencePolicy).  Two steps, both on the GPU:
+ *   1. the pattern (estimate_pattern): the last min(64, S) queries attend
+ *      causally to every key with logits sm_scale * <q, k>; each row's softmax
+ *      probabilities are summed per key column (vertical scores) and per
+ *      diagonal d = position - key (slash scores); the first num_sink_tokens
+ *      columns and num_recent_diags diagonals count as +inf; the nv highest
+ *      columns and ns highest diagonals of every query head are kept (equal
+ *      scores: lower index first), in ascending order.  nv, ns: see
+ *      pkv_minference_sizes.  Scores and sums in fp32.
+ *   2. the attention: query row i (position i) keeps key j iff j <= i and
+ *      (j is a kept column of its head, or i - j a kept diagonal); softmax
+ *      over the kept keys; o = sum p v (a row keeping nothing gets 0).  The
+ *      pages leave the sparse kernel itself to a library they do not show;
+ *      this is the element-wise reading of "vertical + slash".
+ *   q, out [S, num_qo_heads, head_dim], k, v [S, num_kv_heads, head_dim]:
+ *   bf16, contiguous; head_dim 64..128 (multiple of 16); S <= 131072;
+ *   num_qo_heads / num_kv_heads a power of two <= 16.
+ *   vertical_indices [num_qo_heads, nv], slash_indices [num_qo_heads, ns]:
+ *   optional int32 device outputs (NULL: kept in the workspace).
+ *   workspace: pkv_minference_workspace_size bytes, 256-byte aligned.
+ */
+PKV_API pkv_status pkv_minference_sizes(int seq_len, int vertical_size, int slash_size,
+                                        double adaptive_budget, int num_sink_tokens,
+                                        int num_recent_diags, int *nv, int *ns);
+/* nv, ns: with adaptive_budget > 0, b = (int)(S * adaptive_budget),
+ * nv = max(num_sink + 1, (int)(0.2 b)), ns = max(num_recent + 1, (int)(0.8 b));
+ * otherwise vertical_size, slash_size; both capped at S. */
+
+PKV_API size_t pkv_minference_workspace_size(int seq_len, int num_qo_heads, int num_kv_heads,
+                                             int vertical_size, int slash_size,
+                                             double adaptive_budget, int num_sink_tokens,
+                                             int num_recent_diags);
+
+PKV_API pkv_status pkv_minference_prefill(void *out, const void *q, const void *k,
+                                          const void *v, int seq_len, int num_qo_heads,
+                                          int num_kv_heads, int head_dim, int dtype,
+                                          int vertical_size, int slash_size,
+                                          double adaptive_budget, int num_sink_tokens,
+                                          int num_recent_diags, float sm_scale,
+                                          int32_t *vertical_indices, int32_t *slash_indices,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t *dev_error, void *stream);
 
 /*
  * paged_decode_noalloc: paged_decode for callers that cannot allocate device

@@ -33,6 +33,7 @@ __all__ = [
     "varlen_prefill", "varlen_prefill_contiguous", "paged_decode_noalloc",
     "paged_decode_workspace_size", "varlen_prefill_workspace_size",
     "rope_cos_sin_table", "rope_reshape_and_cache", "ntk_scaled_base",
+    "minference_sizes", "minference_prefill",
     "DEVERR_BLOCK_ID", "DEVERR_SLOT", "DEVERR_SEQLEN", "DEVERR_TIMEOUT", "DEVERR_POSITION",
     "EXPORTED_SYMBOLS",
 ]
@@ -50,6 +51,7 @@ EXPORTED_SYMBOLS = (
     "pkv_paged_decode_workspace_size", "pkv_paged_decode",
     "pkv_varlen_prefill_workspace_size", "pkv_varlen_prefill",
     "pkv_varlen_prefill_contiguous", "pkv_rope_cos_sin_table", "pkv_rope_reshape_and_cache",
+    "pkv_minference_sizes", "pkv_minference_workspace_size", "pkv_minference_prefill",
 )
 
 
@@ -118,6 +120,13 @@ def load_library(path: Optional[str] = None):
         lib.pkv_rope_reshape_and_cache.argtypes = [P, P, P, P, P, P, P, i64, i32, CacheDesc, P,
                                                    i32, i32, i32, P, P]
         lib.pkv_rope_reshape_and_cache.restype = i32
+        lib.pkv_minference_sizes.argtypes = [i32, i32, i32, f64, i32, i32, P, P]
+        lib.pkv_minference_sizes.restype = i32
+        lib.pkv_minference_workspace_size.argtypes = [i32, i32, i32, i32, i32, f64, i32, i32]
+        lib.pkv_minference_workspace_size.restype = sz
+        lib.pkv_minference_prefill.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64,
+                                               i32, i32, f32, P, P, P, sz, P, P]
+        lib.pkv_minference_prefill.restype = i32
         _lib = lib
         return lib
 
@@ -442,6 +451,70 @@ def varlen_prefill_contiguous(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_seqlen_
         ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill_contiguous", st)
     return out
+
+
+def minference_sizes(seq_len: int, vertical_size: int = 1000, slash_size: int = 6096,
+                     adaptive_budget: Optional[float] = 0.3, num_sink_tokens: int = 30,
+                     num_recent_diags: int = 100):
+    """(nv, ns): how many vertical columns and slash diagonals are kept."""
+    nv, ns = ctypes.c_int(), ctypes.c_int()
+    st = load_library().pkv_minference_sizes(
+        int(seq_len), int(vertical_size), int(slash_size),
+        float(adaptive_budget) if adaptive_budget is not None else 0.0, int(num_sink_tokens),
+        int(num_recent_diags), ctypes.byref(nv), ctypes.byref(ns))
+    _check("pkv_minference_sizes", st)
+    return nv.value, ns.value
+
+
+def lib_minference_workspace(seq_len: int, num_qo_heads: int, num_kv_heads: int,
+                             vertical_size: int = 1000, slash_size: int = 6096,
+                             adaptive_budget: Optional[float] = 0.3, num_sink_tokens: int = 30,
+                             num_recent_diags: int = 100) -> int:
+    """Workspace bytes minference_prefill needs."""
+    return int(load_library().pkv_minference_workspace_size(
+        int(seq_len), int(num_qo_heads), int(num_kv_heads), int(vertical_size), int(slash_size),
+        float(adaptive_budget) if adaptive_budget is not None else 0.0, int(num_sink_tokens),
+        int(num_recent_diags)))
+
+
+def minference_prefill(q, k, v, vertical_size: int = 1000, slash_size: int = 6096,
+                       adaptive_budget: Optional[float] = 0.3, num_sink_tokens: int = 30,
+                       num_recent_diags: int = 100, sm_scale: Optional[float] = None, out=None,
+                       return_pattern: bool = False, workspace=None, dev_error=None,
+                       stream=None):
+    """MInference vertical + slash sparse prefill of one sequence: q [S, Hq, D],
+    k, v [S, Hkv, D] bf16.  Returns out [S, Hq, D] (and, with
+    return_pattern, the kept vertical [Hq, nv] and slash [Hq, ns] indices)."""
+    torch = _torch()
+    _cuda_contig("q", q, torch.bfloat16, 3)
+    _cuda_contig("k", k, torch.bfloat16, 3)
+    _cuda_contig("v", v, torch.bfloat16, 3)
+    S, Hq, D = q.shape
+    _require(k.shape == v.shape and k.shape[0] == S and k.shape[2] == D,
+             "k and v must be [S, num_kv_heads, head_dim] like q")
+    Hkv = k.shape[1]
+    budget = float(adaptive_budget) if adaptive_budget is not None else 0.0
+    nv, ns = minference_sizes(S, vertical_size, slash_size, adaptive_budget, num_sink_tokens,
+                              num_recent_diags)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_contig("out", out, q.dtype, 3)
+        _require(out.shape == q.shape, "out must be shaped like q")
+    vi = torch.empty(Hq, nv, dtype=torch.int32, device=q.device) if return_pattern else None
+    si = torch.empty(Hq, ns, dtype=torch.int32, device=q.device) if return_pattern else None
+    need = int(load_library().pkv_minference_workspace_size(
+        S, Hq, Hkv, int(vertical_size), int(slash_size), budget, int(num_sink_tokens),
+        int(num_recent_diags)))
+    ws = _workspace(need, q.device, workspace)
+    scale = float(sm_scale) if sm_scale is not None else D ** -0.5
+    st = load_library().pkv_minference_prefill(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), S, Hq, Hkv, D, PKV_BF16, int(vertical_size),
+        int(slash_size), budget, int(num_sink_tokens), int(num_recent_diags), scale, _ptr(vi),
+        _ptr(si), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_error),
+        _stream_handle(stream))
+    _check("pkv_minference_prefill", st)
+    return (out, vi, si) if return_pattern else out
 
 
 def paged_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,

@@ -3,6 +3,7 @@
 // memory from the host or synchronises a stream.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -193,7 +194,7 @@ const char *pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 300; }
+int pkv_version(void) { return 400; }
 
 pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                  void *v_cache, const int64_t *slot_mapping, int64_t num_tokens,
@@ -376,6 +377,13 @@ namespace {
 // Shared by the paged and the contiguous prefill entry points.  kv_rows: the
 // rows of the K/V views the tensor maps cover; kv_box_rows: rows per box (the
 // page size, or 128 for contiguous rows).
+// The bitmaps of the MInference sparse form (nullptr: dense attention).
+struct SparseMask {
+    const uint32_t *vbits, *sbits;
+    const int32_t *vcnt, *scnt;
+    int words;
+};
+
 pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
                        const pkv_cache_desc &cache, bool contiguous, int64_t kv_rows,
                        const int32_t *block_table, int max_blocks_per_seq,
@@ -384,7 +392,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
                        const float *alibi_slopes, int batch, int num_qo_heads, int causal,
                        int window_left, float sm_scale,
                        float *lse_out, void *workspace, size_t workspace_bytes,
-                       int32_t *dev_error, void *stream) {
+                       int32_t *dev_error, void *stream, const SparseMask *sparse = nullptr) {
     if (cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (cache.head_dim % 16 != 0 || (cache.head_dim > 128 && cache.head_dim != 256))
         return PKV_ERR_UNSUPPORTED;
@@ -431,6 +439,13 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
     p.window_left = window_left;
     p.head_dim = cache.head_dim;
     p.hnd = (!contiguous && cache.layout == PKV_HND) ? 1 : 0;
+    if (sparse) {
+        p.vbits = sparse->vbits;
+        p.sbits = sparse->sbits;
+        p.vcnt = sparse->vcnt;
+        p.scnt = sparse->scnt;
+        p.bit_words = sparse->words;
+    }
     p.causal = causal ? 1 : 0;
     p.total_k = contiguous ? (int)kv_rows : 0;
     p.rows_per_head = 128 / G;
@@ -511,6 +526,148 @@ pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k
                        max_seqlen_q, max_seqlen_k, total_q, sink, alibi_slopes, batch,
                        num_qo_heads, causal, window_left, sm_scale, lse_out, workspace,
                        workspace_bytes, dev_error, stream);
+}
+
+
+pkv_status pkv_minference_sizes(int seq_len, int vertical_size, int slash_size,
+                                double adaptive_budget, int num_sink_tokens,
+                                int num_recent_diags, int *nv, int *ns) {
+    if (seq_len <= 0 || num_sink_tokens < 0 || num_recent_diags < 0 || !nv || !ns)
+        return PKV_ERR_INVALID_ARG;
+    if (adaptive_budget > 0.0) {
+        const int budget = (int)(seq_len * adaptive_budget);
+        vertical_size = std::max(num_sink_tokens + 1, (int)(budget * 0.2));
+        slash_size = std::max(num_recent_diags + 1, (int)(budget * 0.8));
+    }
+    if (vertical_size <= 0 || slash_size <= 0) return PKV_ERR_INVALID_ARG;
+    *nv = std::min(vertical_size, seq_len);
+    *ns = std::min(slash_size, seq_len);
+    return PKV_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct MinferenceLayout {
+    size_t stat, lse, vscore, sscore, spart, vidx, sidx, vbits, sbits, vcnt, scnt, cu, tiles,
+        total;
+};
+
+MinferenceLayout minference_layout(int S, int Hq, int Hkv, int nv, int ns) {
+    MinferenceLayout L;
+    const size_t nblk = (size_t)(S + 127) / 128, W = (size_t)(S + 31) / 32;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    L.stat = take((size_t)Hq * nblk * 64 * 4 * 2);
+    L.lse = take((size_t)Hq * 64 * 4);
+    L.vscore = take((size_t)Hq * S * 4);
+    L.sscore = take((size_t)Hq * S * 4);
+    L.spart = take((size_t)Hq * nblk * 192 * 4);
+    L.vidx = take((size_t)Hq * nv * 4);
+    L.sidx = take((size_t)Hq * ns * 4);
+    L.vbits = take((size_t)Hq * W * 4);
+    L.sbits = take((size_t)Hq * W * 4);
+    L.vcnt = take((size_t)Hq * (W + 1) * 4);
+    L.scnt = take((size_t)Hq * (W + 1) * 4);
+    L.cu = take(16);
+    const int G = Hkv > 0 ? Hq / Hkv : 1;
+    L.tiles = take(prefill_layout(1, G, Hkv, S).total);
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_minference_workspace_size(int seq_len, int num_qo_heads, int num_kv_heads,
+                                     int vertical_size, int slash_size, double adaptive_budget,
+                                     int num_sink_tokens, int num_recent_diags) {
+    int nv = 0, ns = 0;
+    if (num_qo_heads <= 0 || num_kv_heads <= 0 ||
+        pkv_minference_sizes(seq_len, vertical_size, slash_size, adaptive_budget,
+                             num_sink_tokens, num_recent_diags, &nv, &ns) != PKV_OK)
+        return 256;
+    return minference_layout(seq_len, num_qo_heads, num_kv_heads, nv, ns).total;
+}
+
+pkv_status pkv_minference_prefill(void *out, const void *q, const void *k, const void *v,
+                                  int seq_len, int num_qo_heads, int num_kv_heads, int head_dim,
+                                  int dtype, int vertical_size, int slash_size,
+                                  double adaptive_budget, int num_sink_tokens,
+                                  int num_recent_diags, float sm_scale,
+                                  int32_t *vertical_indices, int32_t *slash_indices,
+                                  void *workspace, size_t workspace_bytes, int32_t *dev_error,
+                                  void *stream) {
+    int nv = 0, ns = 0;
+    pkv_status st = pkv_minference_sizes(seq_len, vertical_size, slash_size, adaptive_budget,
+                                         num_sink_tokens, num_recent_diags, &nv, &ns);
+    if (st != PKV_OK) return st;
+    if (num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0 ||
+        !std::isfinite(sm_scale))
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (head_dim % 16 != 0 || head_dim < 64 || head_dim > 128) return PKV_ERR_UNSUPPORTED;
+    if (seq_len > kMaxSparseKeys) return PKV_ERR_UNSUPPORTED;
+    if (!out || !q || !k || !v) return PKV_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+        (vertical_indices && !aligned(vertical_indices, 4)) ||
+        (slash_indices && !aligned(slash_indices, 4)))
+        return PKV_ERR_INVALID_ARG;
+    const MinferenceLayout L =
+        minference_layout(seq_len, num_qo_heads, num_kv_heads, nv, ns);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total)
+        return PKV_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    MinferenceParams m;
+    std::memset(&m, 0, sizeof m);
+    m.q = q;
+    m.k = k;
+    m.seq_len = seq_len;
+    m.last_q = std::min(64, seq_len);
+    m.num_qo_heads = num_qo_heads;
+    m.num_kv_heads = num_kv_heads;
+    m.head_dim = head_dim;
+    m.num_blocks = (seq_len + 127) / 128;
+    m.scale = sm_scale;
+    const size_t nblk = (size_t)m.num_blocks;
+    m.stat_m = reinterpret_cast<float *>(ws + L.stat);
+    m.stat_l = m.stat_m + (size_t)num_qo_heads * nblk * 64;
+    m.lse = reinterpret_cast<float *>(ws + L.lse);
+    m.vscore = reinterpret_cast<float *>(ws + L.vscore);
+    m.sscore = reinterpret_cast<float *>(ws + L.sscore);
+    m.spart = reinterpret_cast<float *>(ws + L.spart);
+    m.nv = nv;
+    m.ns = ns;
+    m.num_sink = num_sink_tokens;
+    m.num_recent = num_recent_diags;
+    m.vidx = vertical_indices ? vertical_indices : reinterpret_cast<int32_t *>(ws + L.vidx);
+    m.sidx = slash_indices ? slash_indices : reinterpret_cast<int32_t *>(ws + L.sidx);
+    m.words = (seq_len + 31) / 32;
+    m.vbits = reinterpret_cast<uint32_t *>(ws + L.vbits);
+    m.sbits = reinterpret_cast<uint32_t *>(ws + L.sbits);
+    m.vcnt = reinterpret_cast<int32_t *>(ws + L.vcnt);
+    m.scnt = reinterpret_cast<int32_t *>(ws + L.scnt);
+    m.cu = reinterpret_cast<int32_t *>(ws + L.cu);
+    cudaError_t e = launch_minference_pattern(m, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    pkv_cache_desc cache;
+    cache.num_blocks = 1;
+    cache.block_size = 128;
+    cache.num_kv_heads = num_kv_heads;
+    cache.head_dim = head_dim;
+    cache.dtype = dtype;
+    cache.layout = PKV_NHD;
+    const SparseMask mask{m.vbits, m.sbits, m.vcnt, m.scnt, m.words};
+    return prefill_run(out, q, k, v, cache, true, seq_len, nullptr, seq_len / 64 + 2, m.cu,
+                       m.cu, seq_len, seq_len, seq_len, nullptr, nullptr, 1, num_qo_heads, 1, -1,
+                       sm_scale, nullptr, ws + L.tiles, L.total - L.tiles, dev_error, stream,
+                       &mask);
 }
 
 }  // extern "C"

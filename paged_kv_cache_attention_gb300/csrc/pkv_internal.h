@@ -57,6 +57,12 @@ struct PrefillParams {
     int head_dim;                  // D <= 128 (tiles padded to 128 with zeros), or 256
     int hnd;                       // paged pools in the HND layout (else NHD)
     int total_k;                   // contiguous K/V: rows in the arrays (unused when paged)
+    // MInference sparse form (contiguous K/V only): [Hq][bit_words] bitmaps of
+    // the kept key columns and diagonals, and their per-word prefix counts
+    // ([Hq][bit_words + 1]); vbits == nullptr for dense attention
+    const uint32_t *vbits, *sbits;
+    const int32_t *vcnt, *scnt;
+    int bit_words;
     int rows_per_head;             // query tokens per 128-row tile (128 / group)
     int max_tiles;                 // capacity of the work list
     float scale_log2;
@@ -74,6 +80,33 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
 cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
                           const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                           cudaStream_t stream);
+
+// MInference: the longest sequence the sparse prefill takes (its per-CTA
+// list of 128-key tiles has 16-bit entries in 2 KB of shared memory).
+constexpr int kMaxSparseKeys = 131072;
+
+// MInference vertical + slash pattern of one sequence (minference.cu).
+struct MinferenceParams {
+    const void *q, *k;             // [S, Hq, D], [S, Hkv, D]
+    int seq_len, last_q, num_qo_heads, num_kv_heads, head_dim;
+    int num_blocks;                // ceil(S / 128) score blocks
+    float scale;                   // logit = scale * <q, k>
+    // workspace
+    float *stat_m, *stat_l;        // [Hq][num_blocks][64] per-block row max, sum exp
+    float *lse;                    // [Hq][64]
+    float *vscore, *sscore;        // [Hq][S]
+    float *spart;                  // [Hq][num_blocks][192] diagonal partials
+    // selection
+    int nv, ns, num_sink, num_recent;
+    int32_t *vidx, *sidx;          // [Hq][nv], [Hq][ns], ascending
+    // bitmaps for the attention
+    int words;                     // ceil(S / 32)
+    uint32_t *vbits, *sbits;       // [Hq][words]
+    int32_t *vcnt, *scnt;          // [Hq][words + 1]
+    int32_t *cu;                   // [2]: cu_seq_lens {0, S} of the one sequence
+};
+
+cudaError_t launch_minference_pattern(const MinferenceParams &p, int dtype, cudaStream_t stream);
 
 // Rotary embedding fused with the cache write.
 struct RopeParams {

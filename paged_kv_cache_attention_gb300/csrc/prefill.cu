@@ -50,6 +50,7 @@ constexpr int kNQ = 2;        // query tiles per CTA
 constexpr int kStages = 2;    // K and V ring depth
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxSparseTiles = kMaxSparseKeys / kTileN;
 
 struct PfLayout {
     static constexpr int Q_BYTES = kTileM * kHeadDim * 2;   // 32 KB
@@ -76,7 +77,11 @@ struct PfLayout {
     // ([kNQ][128][2])
     static constexpr int OFF_XMAX = OFF_TMEM + 16;
     static constexpr int OFF_XL = OFF_XMAX + 2 * kNQ * 128 * 2 * 4;
-    static constexpr int SMEM = 1024 + OFF_XL + kNQ * 128 * 2 * 4;
+    // sparse form: the key tiles the item attends ([kMaxSparseTiles] uint16)
+    // and their number
+    static constexpr int OFF_LIST = OFF_XL + kNQ * 128 * 2 * 4;
+    static constexpr int OFF_NLIST = OFF_LIST + kMaxSparseTiles * 2;
+    static constexpr int SMEM = 1024 + OFF_NLIST + 16;
     static constexpr int SOFT_WARPS = 8;  // per query tile: 2 per TMEM lane quarter
     static constexpr int THREADS = 64 + kNQ * SOFT_WARPS * 32;
     static constexpr int TMEM_COLS = 512;  // O_0, O_1, S_0, S_1: 128 columns each
@@ -219,13 +224,46 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
 }
 
 // ---------------------------------------------------------------------------
+// bitmaps of the sparse form
+// ---------------------------------------------------------------------------
+// Bits [lo, lo + 64) of a bitmap of `words` 32-bit words (bit j of the map is
+// bit j & 31 of word j >> 5); bits outside the map read 0.
+__device__ __forceinline__ uint64_t bits64(const uint32_t *bits, int words, int lo) {
+    const int w = lo >> 5;  // floor, also for negative lo
+    const int off = lo & 31;
+    auto word = [&](int i) -> uint64_t {
+        return (i >= 0 && i < words) ? (uint64_t)__ldg(bits + i) : 0ull;
+    };
+    const uint64_t a = word(w) | (word(w + 1) << 32);
+    const uint64_t b = word(w + 2);
+    return off ? (a >> off) | (b << (64 - off)) : a;
+}
+
+// Is any bit of [lo, hi] (inclusive, clipped to the map) set?  cnt[w] is the
+// number of set bits in words [0, w).
+__device__ __forceinline__ bool bit_range_any(const uint32_t *bits, const int32_t *cnt, int lo,
+                                              int hi) {
+    if (lo < 0) lo = 0;
+    if (hi < lo) return false;
+    const int wl = lo >> 5, wh = hi >> 5;
+    const uint32_t ml = ~0u << (lo & 31), mh = ~0u >> (31 - (hi & 31));
+    if (wl == wh) return (__ldg(bits + wl) & ml & mh) != 0;
+    if (__ldg(bits + wl) & ml) return true;
+    if (__ldg(bits + wh) & mh) return true;
+    return __ldg(cnt + wh) - __ldg(cnt + wl + 1) > 0;
+}
+
+// ---------------------------------------------------------------------------
 // the attention kernel
 // ---------------------------------------------------------------------------
 // BS: rows per page of the paged pools; CONTIG: K/V are contiguous rows
 // addressed by cu_k (then BS = 128, one box per 64-dim half per tile);
 // ALIBI: the logits gain slope[head] * (key - position); HND: paged pools in
-// the HND layout.
-template <int BS, bool CONTIG, bool ALIBI, bool HND>
+// the HND layout; SPARSE: MInference vertical + slash attention of one
+// contiguous sequence (key j kept for the row at position i iff j <= i and
+// the vertical bitmap of its head has j or the slash bitmap has i - j); key
+// tiles holding no kept key of the item's heads are skipped.
+template <int BS, bool CONTIG, bool ALIBI, bool HND, bool SPARSE = false>
 __global__ void __launch_bounds__(PfLayout::THREADS, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -263,14 +301,60 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int ntiles = geo.ntiles;
-    const int last_key_end = (geo.kt_lo + ntiles) * kTileN;
-    const bool tail = ntiles > 0 && last_key_end > geo.kv_len;
-    // Key tiles in processing order.  With ALiBi they run from the query's end
-    // backwards: the nearest keys carry the largest bias, so the first tile
-    // usually holds the row maximum and its P = 2^0 is exact in bf16.
-    auto tile_of = [&](int j) { return ALIBI ? ntiles - 1 - j : j; };  // offset from kt_lo
-    auto is_tail = [&](int j) { return tail && tile_of(j) == ntiles - 1; };
+    uint16_t *s_list = reinterpret_cast<uint16_t *>(smem + Lay::OFF_LIST);
+    int *s_nlist = reinterpret_cast<int *>(smem + Lay::OFF_NLIST);
+    if constexpr (SPARSE) {
+        // the key tiles with at least one kept key for some row of the item
+        // (a superset is harmless: every key of a tile is masked per element)
+        if (threadIdx.x == 0) *s_nlist = 0;
+        __syncthreads();
+        const int G = p.group;
+        const int t_end = min(geo.t0 + kNQ * p.rows_per_head, geo.q_len);
+        const int pos_lo = geo.kv_len - geo.q_len + geo.t0;
+        const int pos_hi = geo.kv_len - geo.q_len + t_end - 1;
+        for (int jt = threadIdx.x; jt < geo.ntiles; jt += blockDim.x) {
+            const int k0 = (geo.kt_lo + jt) * kTileN;
+            const int k1 = min(k0 + kTileN - 1, pos_hi);  // causal
+            bool need = false;
+            for (int hl = 0; hl < G && !need; ++hl) {
+                const int head = geo.g * G + hl;
+                need = bit_range_any(p.vbits + (int64_t)head * p.bit_words,
+                                     p.vcnt + (int64_t)head * (p.bit_words + 1), k0, k1) ||
+                       bit_range_any(p.sbits + (int64_t)head * p.bit_words,
+                                     p.scnt + (int64_t)head * (p.bit_words + 1),
+                                     max(pos_lo - (k0 + kTileN - 1), 0), pos_hi - k0);
+            }
+            if (need) s_list[jt] = 1; else s_list[jt] = 0;
+        }
+        __syncthreads();
+        if (warp == 0) {  // compact the flags, in order
+            int base = 0;
+            for (int c0 = 0; c0 < geo.ntiles; c0 += 32) {
+                const int jt = c0 + lane;
+                const bool f = jt < geo.ntiles && s_list[jt];
+                const uint32_t m = __ballot_sync(0xffffffffu, f);
+                __syncwarp();
+                if (f) s_list[base + __popc(m & ((1u << lane) - 1))] = (uint16_t)jt;
+                __syncwarp();
+                base += __popc(m);
+            }
+            if (lane == 0) *s_nlist = base;
+        }
+        __syncthreads();
+    }
+    const int ntiles = SPARSE ? *s_nlist : geo.ntiles;
+    const int last_key_end = (geo.kt_lo + geo.ntiles) * kTileN;
+    const bool tail = geo.ntiles > 0 && last_key_end > geo.kv_len;
+    // Key tiles in processing order (offsets from kt_lo).  With ALiBi they run
+    // from the query's end backwards: the nearest keys carry the largest
+    // bias, so the first tile usually holds the row maximum and its P = 2^0
+    // is exact in bf16.  The sparse form runs its list of tiles, also from the
+    // end: its rows are dominated by their nearest (slash) keys.
+    auto tile_of = [&](int j) {
+        if constexpr (SPARSE) return (int)s_list[ntiles - 1 - j];
+        return ALIBI ? ntiles - 1 - j : j;
+    };
+    auto is_tail = [&](int j) { return tail && tile_of(j) == geo.ntiles - 1; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -463,12 +547,21 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         float m_run = kNegInf, l_run = 0.f;
         bool alive = true;
         for (int j = 0; j < ntiles; ++j) {
+            const int key0 = (geo.kt_lo + tile_of(j)) * kTileN + hc * 64;  // first key of this half
+            uint64_t keep = ~0ull;  // sparse form: bit c keeps key key0 + c
+            if constexpr (SPARSE) {
+                // vertical bits of keys [key0, key0 + 64) and slash bits of the
+                // diagonals qpos - key0 - c, c = 0..63 (reversed into key
+                // order); loaded before the wait for S so the two overlap
+                keep = bits64(p.vbits + (int64_t)head * p.bit_words, p.bit_words, key0) |
+                       __brevll(bits64(p.sbits + (int64_t)head * p.bit_words, p.bit_words,
+                                       qpos - key0 - 63));
+            }
             alive = __all_sync(0xffffffffu,
                                mbar_wait_bounded(bar(Lay::B_SFULL + x), j & 1, p.dev_error));
             if (!alive) break;
             tc::fence_after_sync();
-            const int key0 = (geo.kt_lo + tile_of(j)) * kTileN + hc * 64;  // first key of this half
-            const bool full = (key0 + 63 <= cpos) && (key0 + 64 <= geo.kv_len) &&
+            const bool full = !SPARSE && (key0 + 63 <= cpos) && (key0 + 64 <= geo.kv_len) &&
                               (wl < 0 || key0 >= qpos - wl);
             // keys this row keeps: [klo, khi] (inclusive), relative to key0
             const int khi = min(cpos, geo.kv_len - 1) - key0;
@@ -479,7 +572,22 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             tc::wait_ld();
             // ALiBi bias of this half's first key, log2 units
             const float b0 = ALIBI ? al2 * (float)(key0 - qpos) : 0.f;
-            if (!full) {
+            if constexpr (SPARSE) {
+                // fold the causal / length range [klo, khi] into the keep bits,
+                // then one bit test per element (none when every key is kept)
+                const int lo = max(klo, 0), hi = min(khi, 63);
+                const uint64_t range = hi < lo ? 0ull
+                                               : ((~0ull) >> (63 - hi)) & ((~0ull) << lo);
+                keep &= range;
+                if (keep != ~0ull) {
+                    const uint32_t keep_a = (uint32_t)keep, keep_b = (uint32_t)(keep >> 32);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        if (!((keep_a >> i) & 1u)) ra[i] = __float_as_uint(kNegInf);
+                        if (!((keep_b >> i) & 1u)) rb[i] = __float_as_uint(kNegInf);
+                    }
+                }
+            } else if (!full) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     if (!(i <= khi && i >= klo)) ra[i] = __float_as_uint(kNegInf);
@@ -530,9 +638,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             const float mx = fmaxf(mine, slot[hc ^ 1]);
             const float m_tile = ALIBI ? mx : mx * sl2;  // ALiBi rows hold scaled x already
             // Lazy rescale: O is rescaled only when the maximum grows by more
-            // than the threshold.  ALiBi rescales on any growth, so the row's
-            // largest P stays 2^0 (see the tile order above).
-            const bool grow = m_tile > m_run + (ALIBI ? 0.f : kRescaleThreshold);
+            // than the threshold.  ALiBi and the sparse form rescale on any
+            // growth, so the row's largest P stays 2^0 (see the tile order
+            // above).
+            const bool grow = m_tile > m_run + ((ALIBI || SPARSE) ? 0.f : kRescaleThreshold);
             // tcgen05.ld/st are warp-collective: the warp rescales together,
             // lanes whose maximum did not grow enough multiply by 1
             if (__any_sync(0xffffffffu, grow)) {
@@ -681,6 +790,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, 
                          : go(prefill_tc_kernel<32, false, AL, false>);
         return cudaErrorNotSupported;
     };
+    if (contiguous && p.vbits) return go(prefill_tc_kernel<kTileN, true, false, false, true>);
     if (contiguous)
         return p.alibi ? go(prefill_tc_kernel<kTileN, true, true, false>)
                        : go(prefill_tc_kernel<kTileN, true, false, false>);

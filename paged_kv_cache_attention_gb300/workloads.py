@@ -329,6 +329,50 @@ def make_rope(num_tokens: int, num_qo_heads: int, num_kv_heads: int, head_dim: i
                     float(position_scale), bool(neox), int(max_position))
 
 
+def make_long_sequence(seq_len: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                       seed: int, n_stripes: int = 32, n_sinks: int = 4, dtype=torch.bfloat16):
+    """One long sequence whose attention has the structure MInference's
+    vertical + slash pattern targets (long-context LLM prefill): q and k share
+    a component rotated by position (RoFormer rotation of the first half of
+    the dims, frequencies 10000^(-2f/half)), so q_i . k_j peaks near i = j and
+    decays with the distance (slash lines); the unrotated half of the query
+    is a common direction that a few keys (the first n_sinks and n_stripes
+    seeded columns) carry strongly (vertical lines); plus N(0, 1) noise.
+    Returns q [S, Hq, D], k, v [S, Hkv, D] in dtype."""
+    gen = _gen(seed)
+    S, D = int(seq_len), int(head_dim)
+    half = D // 2
+    pos = torch.arange(S, dtype=torch.float64)[:, None]
+    freq = torch.pow(10000.0, -2.0 * torch.arange(half // 2, dtype=torch.float64) / half)
+    ang = pos * freq[None, :]
+    cos, sin = torch.cos(ang), torch.sin(ang)  # [S, half/2]
+
+    def rotate(x):  # x [S, H, half]: pairs (f, f + half/2) turned by pos * freq_f
+        a, b = x[..., : half // 2], x[..., half // 2:]
+        c, s_ = cos[:, None, :], sin[:, None, :]
+        return torch.cat([a * c - b * s_, b * c + a * s_], dim=-1)
+
+    base = torch.randn(num_kv_heads, half, generator=gen, dtype=torch.float64) * 1.5
+    qdir = torch.randn(num_kv_heads, D - half, generator=gen, dtype=torch.float64)
+    qdir = qdir / qdir.norm(dim=-1, keepdim=True) * 3.0
+    G = num_qo_heads // num_kv_heads
+    qr = base.repeat_interleave(G, 0)[None] + 0.5 * torch.randn(S, num_qo_heads, half,
+                                                                 generator=gen,
+                                                                 dtype=torch.float64)
+    kr = base[None] + 0.5 * torch.randn(S, num_kv_heads, half, generator=gen,
+                                        dtype=torch.float64)
+    qu = qdir.repeat_interleave(G, 0)[None].expand(S, -1, -1) + 0.5 * torch.randn(
+        S, num_qo_heads, D - half, generator=gen, dtype=torch.float64)
+    ku = 0.5 * torch.randn(S, num_kv_heads, D - half, generator=gen, dtype=torch.float64)
+    cols = torch.cat([torch.arange(min(n_sinks, S)),
+                      torch.randperm(S, generator=gen)[:n_stripes]]).unique()
+    ku[cols] += qdir[None] * 12.0
+    q = torch.cat([rotate(qr), qu], dim=-1)
+    k = torch.cat([rotate(kr), ku], dim=-1)
+    v = torch.randn(S, num_kv_heads, D, generator=gen, dtype=torch.float64)
+    return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
 # ---------------------------------------------------------------------------
 # the five serving configurations
 # ---------------------------------------------------------------------------

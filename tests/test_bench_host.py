@@ -46,6 +46,18 @@ def test_rope_bytes_by_hand():
     assert bench.rope_bytes(3, 2, 1, 8, 4, 2) == 360
 
 
+def test_sparse_kept_pairs_by_brute_force():
+    rng = np.random.default_rng(3)
+    S = 97
+    vert = [np.sort(rng.choice(S, 11, replace=False)) for _ in range(3)]
+    slash = [np.sort(rng.choice(S, 17, replace=False)) for _ in range(3)]
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    want = sum(int(((j <= i) & (np.isin(j, v) | np.isin(i - j, d))).sum())
+               for v, d in zip(vert, slash))
+    assert bench.sparse_kept_pairs(S, vert, slash) == want
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
