@@ -572,28 +572,32 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             tc::wait_ld();
             // ALiBi bias of this half's first key, log2 units
             const float b0 = ALIBI ? al2 * (float)(key0 - qpos) : 0.f;
-            if constexpr (SPARSE) {
-                // fold the causal / length range [klo, khi] into the keep bits,
-                // then one bit test per element (none when every key is kept)
-                const int lo = max(klo, 0), hi = min(khi, 63);
-                const uint64_t range = hi < lo ? 0ull
-                                               : ((~0ull) >> (63 - hi)) & ((~0ull) << lo);
-                keep &= range;
-                if (keep != ~0ull) {
-                    const uint32_t keep_a = (uint32_t)keep, keep_b = (uint32_t)(keep >> 32);
+            auto apply_mask = [&]() {
+                if constexpr (SPARSE) {
+                    // fold the causal / length range [klo, khi] into the keep bits,
+                    // then one bit test per element (none when every key is kept)
+                    const int lo = max(klo, 0), hi = min(khi, 63);
+                    const uint64_t range = hi < lo ? 0ull
+                                                   : ((~0ull) >> (63 - hi)) & ((~0ull) << lo);
+                    keep &= range;
+                    if (keep != ~0ull) {
+                        const uint32_t keep_a = (uint32_t)keep, keep_b = (uint32_t)(keep >> 32);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            if (!((keep_a >> i) & 1u)) ra[i] = __float_as_uint(kNegInf);
+                            if (!((keep_b >> i) & 1u)) rb[i] = __float_as_uint(kNegInf);
+                        }
+                    }
+                } else if (!full) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        if (!((keep_a >> i) & 1u)) ra[i] = __float_as_uint(kNegInf);
-                        if (!((keep_b >> i) & 1u)) rb[i] = __float_as_uint(kNegInf);
+                        if (!(i <= khi && i >= klo)) ra[i] = __float_as_uint(kNegInf);
+                        if (!(i + 32 <= khi && i + 32 >= klo)) rb[i] = __float_as_uint(kNegInf);
                     }
                 }
-            } else if (!full) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (!(i <= khi && i >= klo)) ra[i] = __float_as_uint(kNegInf);
-                    if (!(i + 32 <= khi && i + 32 >= klo)) rb[i] = __float_as_uint(kNegInf);
-                }
-            }
+            };
+            apply_mask();
+            uint64_t ps2[2] = {0ull, 0ull};
             float mine;
             if constexpr (ALIBI) {
                 // x = s * scale + slope * (key - position) in place, log2
@@ -661,28 +665,29 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 }
                 if (grow) m_run = m_tile;
             }
-            // P = 2^(s * scale - m) as bf16 (masked keys hold -inf:
-            // 2^-inf = 0); with ALiBi the row already holds x = s * scale +
-            // bias, so the multiplier is 1.
-            const float msub = m_run == kNegInf ? 0.f : m_run;
-            const float psc = ALIBI ? 1.f : sl2;
-            const uint64_t scale2 = f2_pack(psc, psc), neg2 = f2_pack(-msub, -msub);
-            uint64_t ps2[2] = {0ull, 0ull};
+            {
+                // P = 2^(s * scale - m) as bf16 (masked keys hold -inf:
+                // 2^-inf = 0); with ALiBi the row already holds x = s * scale +
+                // bias, so the multiplier is 1.
+                const float msub = m_run == kNegInf ? 0.f : m_run;
+                const float psc = ALIBI ? 1.f : sl2;
+                const uint64_t scale2 = f2_pack(psc, psc), neg2 = f2_pack(-msub, -msub);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t *src = h ? rb : ra;  // packed in place: pair i -> word i
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t *src = h ? rb : ra;  // packed in place: pair i -> word i
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float t0, t1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * i]),
-                                             __uint_as_float(src[2 * i + 1])),
-                                     scale2, neg2),
-                              t0, t1);
-                    const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-                    ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
-                    src[i] = pack_bf16(p0, p1);
+                    for (int i = 0; i < 16; ++i) {
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * i]),
+                                                 __uint_as_float(src[2 * i + 1])),
+                                         scale2, neg2),
+                                  t0, t1);
+                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                        ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
+                        src[i] = pack_bf16(p0, p1);
+                    }
+                    tc::st_32x32b_x16(tP + h * 16, src);
                 }
-                tc::st_32x32b_x16(tP + h * 16, src);
             }
             float s0, s1, s2, s3;
             f2_unpack(ps2[0], s0, s1);
