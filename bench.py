@@ -266,15 +266,16 @@ def source_sha(*names):
 class MixedStep:
     """Device-resident inputs and the three C-ABI calls of one step."""
 
-    def __init__(self, case, dev):
+    def __init__(self, case, dev, pool=None):
         import torch
         import paged_kv_cache_attention_gb300 as pkv
         self.pkv = pkv
         self.case = case
         self.dev = dev
         d, p = case.decode, case.prefill
-        self.kc = case.k_cache.to(dev)
-        self.vc = case.v_cache.to(dev)
+        # the KV pool is the serving state: a second stepper may share it
+        self.kc, self.vc = pool if pool is not None else (case.k_cache.to(dev),
+                                                          case.v_cache.to(dev))
         self.key = case.key.to(dev)
         self.value = case.value.to(dev)
         self.slots = case.slot_mapping.to(dev)
@@ -349,37 +350,66 @@ def time_device(stepper, K, W, dist):
 
 
 def time_e2e(stepper, K, W, dist):
-    """The same step through pinned host buffers: per-step inputs (queries, new
-    K/V, slot mapping, block tables, lengths) copied in and outputs copied out
-    inside the timed region; the page pool stays resident (it is the cache)."""
+    """The same step through pinned host buffers: every step's inputs (queries,
+    new K/V, slot mapping, block tables, lengths) are copied in from pinned
+    host memory and its outputs copied out, all inside the timed region; the
+    page pool stays resident (it is the cache).  The copies are pipelined the
+    way a serving loop would run them: two device buffer sets, a copy stream
+    uploading step k+1's inputs and downloading step k-1's outputs while the
+    compute stream runs step k (the kernels themselves stay in order on the
+    compute stream, so every step sees the cache writes of the ones before)."""
     import torch
     dev = stepper.dev
-    dev_in = [stepper.q_dec, stepper.q_pre, stepper.key, stepper.value, stepper.slots,
-              stepper.bt_dec, stepper.sl_dec, stepper.bt_pre, stepper.cuq, stepper.cuk]
-    host_in = [t.cpu().pin_memory() for t in dev_in]
-    dev_out = [stepper.out_dec, stepper.out_pre]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+    other = MixedStep(stepper.case, dev, pool=(stepper.kc, stepper.vc))
+    sets = [stepper, other]
+
+    def ins(st):
+        return [st.q_dec, st.q_pre, st.key, st.value, st.slots, st.bt_dec, st.sl_dec,
+                st.bt_pre, st.cuq, st.cuk]
+
+    def outs(st):
+        return [st.out_dec, st.out_pre]
+
+    host_in = [t.cpu().pin_memory() for t in ins(stepper)]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs(stepper)]
+                for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
 
-    def one():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        stepper.step()
-        for h, d in zip(host_out, dev_out):
-            h.copy_(d, non_blocking=True)
+    def run(n):
+        h2d_done = [torch.cuda.Event() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
 
-    for _ in range(W):
-        one()
-    torch.cuda.synchronize()
+        def upload(k):
+            with torch.cuda.stream(copy):
+                if k >= 2:
+                    copy.wait_event(done[k - 2])  # step k-2 no longer reads set k % 2
+                for h, d in zip(host_in, ins(sets[k % 2])):
+                    d.copy_(h, non_blocking=True)
+                h2d_done[k].record(copy)
+
+        upload(0)
+        for k in range(n):
+            if k + 1 < n:
+                upload(k + 1)
+            compute.wait_event(h2d_done[k])
+            sets[k % 2].step()
+            done[k].record(compute)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[k])
+                for h, d in zip(host_out[k % 2], outs(sets[k % 2])):
+                    h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize()
+
+    run(W)
     dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(K):
-        one()
-    torch.cuda.synchronize()
+    run(K)
     dist.barrier()
     ms = (time.perf_counter() - t0) * 1e3
-    _ = dev
+    del other
     return ms, h2d, d2h
 
 
