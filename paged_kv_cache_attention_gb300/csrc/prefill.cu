@@ -450,14 +450,31 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
             const int ksteps = p.head_dim / 16;  // k-steps past the head size multiply zeros
+            // The issuing thread shares its SM sub-partition with four busy
+            // softmax warps, so every instruction it spends per MMA delays
+            // the tensor pipe: the descriptors are built once, and per tile,
+            // stage and k-step only their start-address field (bytes / 16,
+            // bits 0-13, never carrying out) moves by a constant.
+            const uint64_t dq0 = tc::smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t dk0 = tc::smem_desc_sw128(sK, 16, 1024);
+            const uint64_t dv0 = tc::smem_desc_sw128(sV, Lay::HALF, 1024);
             auto issue_s = [&](int x, int s) {
+                const uint64_t dq = dq0 + (uint64_t)((x * Lay::Q_BYTES) >> 4);
+                const uint64_t dk = dk0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
+                const uint32_t d = tmem + s_col(x);
+                auto kstep = [&](int kk) {
+                    const uint32_t koff = ((kk >> 2) * Lay::HALF + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(d, dq + koff, dk + koff, idS, kk > 0 ? 1u : 0u);
+                };
+                if (ksteps == kHeadDim / 16) {
 #pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    if (kk >= ksteps) break;
-                    const uint32_t koff = (kk >> 2) * Lay::HALF + (kk & 3) * 32;
-                    const uint64_t a = tc::smem_desc_sw128(sQ + x * Lay::Q_BYTES + koff, 16, 1024);
-                    const uint64_t b = tc::smem_desc_sw128(sK + s * Lay::T_BYTES + koff, 16, 1024);
-                    tc::mma_ss(tmem + s_col(x), a, b, idS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk) kstep(kk);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                        if (kk >= ksteps) break;
+                        kstep(kk);
+                    }
                 }
                 tc::commit(bar(Lay::B_SFULL + x));
             };
@@ -486,12 +503,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                         if (!alive) break;
                         tc::fence_after_sync();
                     }
+                    {
+                        const uint64_t dv = dv0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
+                        const uint32_t dO = tmem + o_col(x), aP = tmem + s_col(x);
+                        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-                    for (int kk = 0; kk < kTileN / 16; ++kk) {
-                        const uint64_t b =
-                            tc::smem_desc_sw128(sV + s * Lay::T_BYTES + kk * 2048, Lay::HALF, 1024);
-                        tc::mma_ts(tmem + o_col(x), tmem + s_col(x) + kk * 8, b, idO,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kTileN / 16; ++kk)
+                            tc::mma_ts(dO, aP + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idO,
+                                       kk > 0 ? 1u : acc0);
                     }
                     tc::commit(bar(Lay::B_ODONE + x));
                     if (more) {
