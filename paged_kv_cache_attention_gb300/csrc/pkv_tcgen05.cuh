@@ -91,6 +91,75 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// Eight back-to-back MMAs into one accumulator, issued from one asm block so
+// that the issuing thread spends as few instructions per MMA as it can: the
+// accumulate predicate is set once (the first MMA takes `accumulate`, the rest
+// accumulate), and per MMA only the low word of a descriptor moves.  A start
+// address (bytes / 16) stays below 2^14 in shared memory, so the low word
+// never carries into the high one.
+//
+// mma_ss8: k-steps of a 128-byte-swizzled K-major pair of operands (A and B
+// alike): 16 elements = 32 bytes per step inside a 64-element block, the
+// second block one `half_bytes` further.
+template <int HALF_BYTES>
+__device__ __forceinline__ void mma_ss8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    constexpr int H = HALF_BYTES >> 4;
+    static_assert(H > 6, "half block");
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 al, ah, bl, bh, t0, t1;\n\t.reg .b64 a, b;\n\t"
+        "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "setp.eq.b32 p, %4, %4;\n\t"
+        "add.s32 t0, al, 2;\n\tadd.s32 t1, bl, 2;\n\tmov.b64 a, {t0, ah};\n\tmov.b64 b, {t1, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t"
+        "add.s32 t0, al, 4;\n\tadd.s32 t1, bl, 4;\n\tmov.b64 a, {t0, ah};\n\tmov.b64 b, {t1, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t"
+        "add.s32 t0, al, 6;\n\tadd.s32 t1, bl, 6;\n\tmov.b64 a, {t0, ah};\n\tmov.b64 b, {t1, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t"
+        "add.s32 t0, al, %5;\n\tadd.s32 t1, bl, %5;\n\tmov.b64 a, {t0, ah};\n\tmov.b64 b, {t1, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t"
+        "add.s32 t0, al, %6;\n\tadd.s32 t1, bl, %6;\n\tmov.b64 a, {t0, ah};\n\tmov.b64 b, {t1, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t"
+        "add.s32 t0, al, %7;\n\tadd.s32 t1, bl, %7;\n\tmov.b64 a, {t0, ah};\n\tmov.b64 b, {t1, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t"
+        "add.s32 t0, al, %8;\n\tadd.s32 t1, bl, %8;\n\tmov.b64 a, {t0, ah};\n\tmov.b64 b, {t1, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(H), "n"(H + 2), "n"(H + 4),
+        "n"(H + 6)
+        : "memory");
+}
+
+// mma_ts8: A from tensor memory (8 columns = 16 bf16 elements per step), B an
+// MN-major 128-byte-swizzled operand whose K index advances 16 rows of 128
+// bytes (2 KB) per step.
+__device__ __forceinline__ void mma_ts8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 bl, bh, t, ta;\n\t.reg .b64 b;\n\t"
+        "mov.b64 {bl, bh}, %2;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "setp.eq.b32 p, %4, %4;\n\t"
+        "add.s32 ta, %1, 8;\n\tadd.s32 t, bl, 128;\n\tmov.b64 b, {t, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, p;\n\t"
+        "add.s32 ta, %1, 16;\n\tadd.s32 t, bl, 256;\n\tmov.b64 b, {t, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, p;\n\t"
+        "add.s32 ta, %1, 24;\n\tadd.s32 t, bl, 384;\n\tmov.b64 b, {t, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, p;\n\t"
+        "add.s32 ta, %1, 32;\n\tadd.s32 t, bl, 512;\n\tmov.b64 b, {t, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, p;\n\t"
+        "add.s32 ta, %1, 40;\n\tadd.s32 t, bl, 640;\n\tmov.b64 b, {t, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, p;\n\t"
+        "add.s32 ta, %1, 48;\n\tadd.s32 t, bl, 768;\n\tmov.b64 b, {t, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, p;\n\t"
+        "add.s32 ta, %1, 56;\n\tadd.s32 t, bl, 896;\n\tmov.b64 b, {t, bh};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier when every MMA this thread issued so far is done.
 __device__ __forceinline__ void commit(uint32_t bar) {
     asm volatile(

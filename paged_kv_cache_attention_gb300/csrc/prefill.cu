@@ -51,6 +51,7 @@ constexpr int kStages = 2;    // K and V ring depth
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxSparseTiles = kMaxSparseKeys / kTileN;
+static_assert(kTileN / 16 == 8 && kHeadDim / 16 == 8, "MMA groups of 8 k-steps");
 
 struct PfLayout {
     static constexpr int Q_BYTES = kTileM * kHeadDim * 2;   // 32 KB
@@ -467,8 +468,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                     tc::mma_ss(d, dq + koff, dk + koff, idS, kk > 0 ? 1u : 0u);
                 };
                 if (ksteps == kHeadDim / 16) {
-#pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 16; ++kk) kstep(kk);
+                    tc::mma_ss8<Lay::HALF>(d, dq, dk, idS, 0u);
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < kHeadDim / 16; ++kk) {
@@ -506,11 +506,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                     {
                         const uint64_t dv = dv0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
                         const uint32_t dO = tmem + o_col(x), aP = tmem + s_col(x);
-                        const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-                        for (int kk = 0; kk < kTileN / 16; ++kk)
-                            tc::mma_ts(dO, aP + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idO,
-                                       kk > 0 ? 1u : acc0);
+                        tc::mma_ts8(dO, aP, dv, idO, j > 0 ? 1u : 0u);
                     }
                     tc::commit(bar(Lay::B_ODONE + x));
                     if (more) {
