@@ -46,11 +46,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of the same launch as the bench step's call, valid
-# only while the kernel source is unchanged (sha256 prefix of the .cu file).
+# only while the kernel source is unchanged (sha256 prefix of the files it is
+# compiled from).
 NCU_TRAFFIC = {
-    # prefill launch of the mixed step: 664.8 MB read + 83.9 MB written
+    # prefill launch of the mixed step: 665.2 MB read + 85.8 MB written
     # (mean of two launches)
-    "prefill": {"bytes": 748737536, "sha": "2b31f4cc654e5775"},
+    "prefill": {"bytes": 750969216, "sha": "ce9a580f6268023d"},
 }
 
 
@@ -249,6 +250,11 @@ def time_flushed(fn, K, flush):
         evs.append((a, b))
     torch.cuda.synchronize()
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+# the files the dense prefill kernel is compiled from
+PREFILL_SOURCES = ("prefill.cu", "prefill_common.cuh", "pkv_tcgen05.cuh", "pkv_device.cuh",
+                   "pkv_internal.h")
 
 
 def source_sha(*names):
@@ -651,7 +657,7 @@ def run_ours(args, dist):
               "bound": "tensor", "achieved": round(pre_tf, 1), "peak": bf16, "unit": "TFLOP/s",
               "frac": round(pre_tf / bf16, 4),
               "traffic": NCU_TRAFFIC.get("prefill", {}).get("bytes")
-              if NCU_TRAFFIC.get("prefill", {}).get("sha") == source_sha("prefill.cu") else None,
+              if NCU_TRAFFIC.get("prefill", {}).get("sha") == source_sha(*PREFILL_SOURCES) else None,
               "algorithmic_flops": pre_flops, "ms": round(calls["varlen_prefill"], 4),
               "peak_source": f"{peak_src} bf16_tflops_sustained (timed inside the step)"}
     dominant = rl_dec if calls["paged_decode"] >= calls["varlen_prefill"] else rl_pre
