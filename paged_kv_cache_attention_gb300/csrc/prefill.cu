@@ -203,14 +203,31 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
         atomicAdd(&hist[c], p.num_kv_heads);
     }
     __syncthreads();
-    // 3. exclusive scan from the heaviest bucket down (sequential: 1024 buckets)
-    if (tid == 0) {
-        int acc = 0;
-        for (int b = kBuckets - 1; b >= 0; --b) {
-            const int h = hist[b];
-            hist[b] = acc;
-            acc += h;
+    // 3. exclusive scan from the heaviest bucket down: thread t takes bucket
+    //    kBuckets - 1 - t (warp scans, then a scan of the warp totals)
+    {
+        static_assert(kBuckets == kSchedThreads, "one bucket per thread");
+        const int bk = kBuckets - 1 - tid, lane = tid & 31, wid = tid >> 5;
+        const int h = hist[bk];
+        int v = h;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += o;
         }
+        if (lane == 31) wsum[wid] = v;
+        __syncthreads();
+        if (tid < 32) {
+            int w = wsum[tid];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, w, off);
+                if (tid >= off) w += o;
+            }
+            wsum[tid] = w;
+        }
+        __syncthreads();
+        hist[bk] = v - h + (wid ? wsum[wid - 1] : 0);
     }
     __syncthreads();
     // 4. scatter
