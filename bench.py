@@ -51,6 +51,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # prefill launch of the mixed step: 665.2 MB read + 85.8 MB written
     # (mean of two launches)
+    # decode call of the mixed step (split-KV kernel + merge): 3157.7 MB read
+    # and 7.2 MB of partials written by the partition kernel, 27.8 MB of
+    # partials read back by the merge (cold caches under ncu; live they are
+    # L2 hits); mean of two calls
+    "decode": {"bytes": 3192652800, "sha": "5be47219c2ce090e"},
     "prefill": {"bytes": 750969216, "sha": "ce9a580f6268023d"},
 }
 
@@ -65,8 +70,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-configuration decode / prefill lines")
-    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_mixed",
-                                          "write", "rope"],
+    ap.add_argument("--profile", choices=["decode", "decode_long", "decode_mixed", "prefill",
+                                          "prefill_mixed", "write", "rope"],
                     default=None,
                     help="run a few launches of one call on a mid-size case (for ncu)")
     return ap.parse_args()
@@ -252,9 +257,10 @@ def time_flushed(fn, K, flush):
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
-# the files the dense prefill kernel is compiled from
+# the files the dense prefill and the bf16 decode kernels are compiled from
 PREFILL_SOURCES = ("prefill.cu", "prefill_common.cuh", "pkv_tcgen05.cuh", "pkv_device.cuh",
                    "pkv_internal.h")
+DECODE_SOURCES = ("decode.cu", "pkv_device.cuh", "pkv_internal.h")
 
 
 def source_sha(*names):
@@ -650,7 +656,7 @@ def run_ours(args, dist):
               "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
               "frac": round(dec_gbs / hbm, 4),
               "traffic": NCU_TRAFFIC.get("decode", {}).get("bytes")
-              if NCU_TRAFFIC.get("decode", {}).get("sha") == source_sha("decode.cu") else None,
+              if NCU_TRAFFIC.get("decode", {}).get("sha") == source_sha(*DECODE_SOURCES) else None,
               "algorithmic_bytes": dec_bytes, "ms": round(calls["paged_decode"], 4),
               "peak_source": f"{peak_src} hbm_gbs"}
     rl_pre = {"call": "varlen_prefill (work-list kernel + tcgen05 attention kernel)",
@@ -729,16 +735,18 @@ def run_reference(args, dist):
 
 def run_profile(which: str):
     """A few launches of one call on a case larger than L2 but a few GB at
-    most: decode = the B64 / L512-4096 decode batch (~0.6 GB of KV), prefill =
-    the B16 varlen prefill batch, write = the mixed step's cache write, rope =
-    the rotary step fused with the write for 8448 tokens."""
+    most: decode = the B64 / L512-4096 decode batch (~0.6 GB of KV),
+    decode_mixed = the mixed step's decode call (256 sequences, ~3.2 GB of KV),
+    prefill = the B16 varlen prefill batch, write = the mixed step's cache
+    write, rope = the rotary step fused with the write for 8448 tokens."""
     import torch
     import paged_kv_cache_attention_gb300 as pkv
     from paged_kv_cache_attention_gb300 import workloads as W
     dev = torch.device("cuda", torch.cuda.current_device())
     pkv.load_library()
-    if which in ("decode", "decode_long"):
-        c = W.config2_decode() if which == "decode" else W.config3_long(1)
+    if which in ("decode", "decode_long", "decode_mixed"):
+        c = (W.config2_decode() if which == "decode" else
+             W.config3_long(1) if which == "decode_long" else W.config5_mixed().decode)
         q, kc, vc = c.q.to(dev), c.k_cache.to(dev), c.v_cache.to(dev)
         bt, sl = c.block_table.to(dev), c.cache_seqlens.to(dev)
         ws = torch.empty(pkv.paged_decode_workspace_size(c.batch, c.num_qo_heads, q.shape[2],
