@@ -613,10 +613,13 @@ def cpu_baseline(case, n_dec_every=2, n_pre_every=2, threads=0):
     dt = time.perf_counter() - t0
     tokens = len(dec_rows) + len(pre_rows)
     cores = threads if threads > 0 else oracle.online_cores()
-    desc = (f"full cache write of {case.num_new_tokens} tokens + every {n_dec_every}th decode "
-            f"sequence ({len(dec_rows)}) + every {n_pre_every}th prefill row ({len(pre_rows)}); "
+
+    def every(n):
+        return "every" if n == 1 else f"one in {n} of the"
+
+    desc = (f"full cache write of {case.num_new_tokens} tokens + {every(n_dec_every)} decode "
+            f"sequences ({len(dec_rows)}) + {every(n_pre_every)} prefill rows ({len(pre_rows)}); "
             f"value = sampled query tokens / wall time")
-    _ = np
     return tokens / dt, cores, desc, dt
 
 
