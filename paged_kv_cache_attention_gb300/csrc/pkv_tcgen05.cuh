@@ -56,6 +56,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr, uint32_t
     return d;
 }
 
+// Shared-memory descriptor of a K-major operand without swizzle, made of 8x8
+// core matrices (8 rows of 16 bytes, 128 bytes each): lbo = bytes between the
+// core matrices adjacent along K, sbo = bytes between 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t smem_addr, uint32_t lbo,
+                                                    uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for tcgen05; layout type 0: no swizzle
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D.
 //   a_mn_major / b_mn_major: 0 = K-major, 1 = MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major,

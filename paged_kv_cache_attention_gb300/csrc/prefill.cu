@@ -60,7 +60,16 @@ struct PfLayout {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + kNQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + kStages * T_BYTES;
-    static constexpr int OFF_BAR = OFF_V + kStages * T_BYTES;
+    // ALiBi as one more k-step of S = Q K^T: 16-wide K-major blocks without
+    // swizzle (8x8 core matrices: 128 bytes between the two k-halves, 256
+    // bytes between 8-row groups).  Row r of the Q block holds the head's
+    // slope / scale split into three bf16 parts; key row n of the K block holds
+    // n (the key's offset in its tile) three times, so the extra k-step adds
+    // slope / scale * n to every score.
+    static constexpr int AB_BYTES = 128 * 16 * 2;
+    static constexpr int OFF_QA = OFF_V + kStages * T_BYTES;
+    static constexpr int OFF_KA = OFF_QA + AB_BYTES;
+    static constexpr int OFF_BAR = OFF_KA + AB_BYTES;
     // barriers
     static constexpr int B_Q = 0;
     static constexpr int B_KFULL = 1;
@@ -295,6 +304,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     uint8_t *smem = align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + Lay::OFF_Q, sK = sbase + Lay::OFF_K, sV = sbase + Lay::OFF_V;
+    const uint32_t sQA = sbase + Lay::OFF_QA, sKA = sbase + Lay::OFF_KA;
     const uint32_t bars = sbase + Lay::OFF_BAR;
     auto bar = [&](int i) { return bars + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
@@ -314,6 +324,27 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     if (warp == 1) {
         tc::tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
         tc::tmem_relinquish();
+    }
+    if constexpr (ALIBI) {
+        // the ALiBi blocks (see PfLayout): element (row r, k) at byte
+        // (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.  The Q
+        // block serves both query tiles: row r's head is g * G + r % G in each.
+        for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+            const int r = i >> 4, k = i & 15;
+            const int off = (r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+            float qa = 0.f;
+            if (k < 3) {
+                // slope / scale = hi + mid + lo to about 2^-24 relative
+                const float a = p.alibi[geo.g * G + r % G] * kLog2e / p.scale_log2;
+                const float hi = __bfloat162float(__float2bfloat16_rn(a));
+                const float mid = __bfloat162float(__float2bfloat16_rn(a - hi));
+                qa = k == 0 ? hi : k == 1 ? mid : a - hi - mid;
+            }
+            *reinterpret_cast<__nv_bfloat16 *>(smem + Lay::OFF_QA + off) = __float2bfloat16_rn(qa);
+            *reinterpret_cast<__nv_bfloat16 *>(smem + Lay::OFF_KA + off) =
+                __float2bfloat16_rn(k < 3 ? (float)r : 0.f);
+        }
+        fence_proxy_async_smem();
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -476,6 +507,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             const uint64_t dq0 = tc::smem_desc_sw128(sQ, 16, 1024);
             const uint64_t dk0 = tc::smem_desc_sw128(sK, 16, 1024);
             const uint64_t dv0 = tc::smem_desc_sw128(sV, Lay::HALF, 1024);
+            const uint64_t dqa = tc::smem_desc_noswz(sQA, 128, 256);
+            const uint64_t dka = tc::smem_desc_noswz(sKA, 128, 256);
             auto issue_s = [&](int x, int s) {
                 const uint64_t dq = dq0 + (uint64_t)((x * Lay::Q_BYTES) >> 4);
                 const uint64_t dk = dk0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
@@ -493,6 +526,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                         kstep(kk);
                     }
                 }
+                if constexpr (ALIBI) tc::mma_ss(d, dqa, dka, idS, 1u);
                 tc::commit(bar(Lay::B_SFULL + x));
             };
             bool alive = mbar_wait_bounded(bar(Lay::B_Q), 0, p.dev_error) &&
@@ -602,8 +636,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             tc::ld_32x32b_x32(tS, ra);
             tc::ld_32x32b_x32(tS + 32, rb);
             tc::wait_ld();
-            // ALiBi bias of this half's first key, log2 units
-            const float b0 = ALIBI ? al2 * (float)(key0 - qpos) : 0.f;
+            // ALiBi: the extra k-step of S added slope / scale * (key - kt0),
+            // kt0 = the tile's first key; the row's part slope * (kt0 - qpos)
+            // joins here (log2 units)
+            const float ct = ALIBI ? al2 * (float)(key0 - hc * 64 - qpos) : 0.f;
             auto apply_mask = [&]() {
                 if constexpr (SPARSE) {
                     // fold the causal / length range [klo, khi] into the keep bits,
@@ -631,33 +667,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             apply_mask();
             uint64_t ps2[2] = {0ull, 0ull};
             float mine;
-            if constexpr (ALIBI) {
-                // x = s * scale + slope * (key - position) in place, log2
-                // units, as packed pairs: the bias pairs of columns (4k, 4k+1)
-                // and (4k+2, 4k+3) come from two chains stepping by 4 slope.
-                // The maximum is then exact (the row's largest P is 2^0 when
-                // it sets a fresh maximum, exact in bf16).
-                const uint64_t sc2 = f2_pack(sl2, sl2), step2 = f2_pack(4.f * al2, 4.f * al2);
-                uint64_t bc[2] = {f2_pack(b0, b0 + al2), f2_pack(b0 + 2.f * al2, b0 + 3.f * al2)};
-                float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t *src = hh ? rb : ra;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * i]),
-                                                 __uint_as_float(src[2 * i + 1])),
-                                         sc2, bc[i & 1]),
-                                  x0, x1);
-                        bc[i & 1] = f2_add(bc[i & 1], step2);
-                        src[2 * i] = __float_as_uint(x0);
-                        src[2 * i + 1] = __float_as_uint(x1);
-                        mx4[2 * hh + (i & 1)] = fmax3(mx4[2 * hh + (i & 1)], x0, x1);
-                    }
-                }
-                mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
-            } else {
+            {
                 float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -672,7 +682,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             slot[hc] = mine;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             const float mx = fmaxf(mine, slot[hc ^ 1]);
-            const float m_tile = ALIBI ? mx : mx * sl2;  // ALiBi rows hold scaled x already
+            const float m_tile = fmaf(mx, sl2, ct);
             // Lazy rescale: O is rescaled only when the maximum grows by more
             // than the threshold.  ALiBi and the sparse form rescale on any
             // growth, so the row's largest P stays 2^0 (see the tile order
@@ -698,12 +708,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 if (grow) m_run = m_tile;
             }
             {
-                // P = 2^(s * scale - m) as bf16 (masked keys hold -inf:
-                // 2^-inf = 0); with ALiBi the row already holds x = s * scale +
-                // bias, so the multiplier is 1.
+                // P = 2^(s * scale + ct - m) as bf16 (masked keys hold -inf:
+                // 2^-inf = 0).  With ALiBi the row's largest P, where it sets a
+                // fresh maximum, is 2^0 up to rounding far below bf16's step.
                 const float msub = m_run == kNegInf ? 0.f : m_run;
-                const float psc = ALIBI ? 1.f : sl2;
-                const uint64_t scale2 = f2_pack(psc, psc), neg2 = f2_pack(-msub, -msub);
+                const uint64_t scale2 = f2_pack(sl2, sl2), neg2 = f2_pack(ct - msub, ct - msub);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t *src = h ? rb : ra;  // packed in place: pair i -> word i

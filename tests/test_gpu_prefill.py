@@ -374,3 +374,18 @@ def test_config5_prefill_half_after_cache_write():
     pre = case.prefill
     pre.k_cache, pre.v_cache = kc.cpu(), vc.cpu()
     _check(pre, rows=_sample_rows(pre, 3), lse=False)
+
+
+def test_many_requests_work_list():
+    """1500 requests: more than the work-list kernel takes in one pass of its
+    1024 threads, with lengths spread over many cost buckets; every 7th
+    request has no queries.  Sampled rows of every request against the
+    oracle."""
+    g = np.random.default_rng(31)
+    n = 1500
+    q_lens = g.integers(1, 48, n)
+    q_lens[::7] = 0
+    prefix = g.integers(0, 600, n)
+    case = W.make_varlen(q_lens.tolist(), prefix.tolist(), 8, 2, 128, 16, BF16, seed=32,
+                         sink="randn")
+    _check(case, rows=_sample_rows(case, 2))
