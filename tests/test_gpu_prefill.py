@@ -365,6 +365,20 @@ def test_config4_prefill_full_size_sampled():
     _check(case, rows=_sample_rows(case))
 
 
+def test_config4_prefill_alibi_full_size_sampled():
+    # the B16 batch with geometric slopes: prefixes up to ~10K keys, so the
+    # per-tile ALiBi constant slope * (tile start - position) reaches its
+    # largest magnitudes; sampled rows of every request
+    case = W.config4_prefill()
+    case.alibi = W.alibi_slopes("geometric", case.q.shape[1], None)
+    _check(case, rows=_sample_rows(case))
+
+
+def test_config4_prefill_head_size_256_full_size_sampled():
+    case = W.config4_prefill(16, 8, 256)
+    _check(case, rows=_sample_rows(case, 3))
+
+
 def test_config5_prefill_half_after_cache_write():
     case = W.config5_mixed()
     d = dev()
