@@ -10,14 +10,24 @@ fails, an exception is raised.
 Operations (same names as the C ABI):
   * ``reshape_and_cache`` -- write new K/V rows into the paged pools at
     ``slot_mapping`` (vLLM attention.py, PagedAttention.forward);
-  * ``paged_decode`` -- one query per sequence over its pages through
-    ``block_table`` / ``cache_seqlens`` (transformers docs "paged_attention",
-    decode path), split-KV with 512-token partitions;
-  * ``varlen_prefill`` -- causal varlen / chunk prefill addressed by
-    ``cu_seq_lens_q`` / ``cu_seq_lens_k`` (transformers docs "paged_attention",
-    varlen path), keys read from the pages.
-All three support GQA, ``window_left`` and the per-head attention sink of
-FlashInfer's sink_attention_reference.py.
+  * ``rope_reshape_and_cache`` -- the rotary embedding of q and k by position
+    (neox or GPT-J pairing, partial rotary_dim, scaled tables from
+    ``rope_cos_sin_table``) fused with that write (vLLM attention.py,
+    PagedAttentionWithRoPE);
+  * ``paged_decode`` (and ``paged_decode_noalloc``, which needs no workspace)
+    -- one query per sequence over its pages through ``block_table`` /
+    ``cache_seqlens`` (transformers docs "paged_attention", decode path),
+    split-KV with 512-token partitions;
+  * ``varlen_prefill`` -- varlen / chunk prefill addressed by
+    ``cu_seq_lens_q`` / ``cu_seq_lens_k`` (transformers docs
+    "paged_attention", varlen path), keys read from the pages, causal or not;
+    ``varlen_prefill_contiguous`` reads them from [total_k, Hkv, D] arrays;
+  * ``minference_prefill`` -- MInference's vertical + slash sparse prefill of
+    one sequence (nano-vllm minference.py): pattern estimate, top-k, then
+    attention over the kept keys.
+The attention calls support GQA, ``window_left``, the per-head attention sink
+of FlashInfer's sink_attention_reference.py, ALiBi slopes, head sizes 64, 80,
+96, 112, 128 and 256, and NHD or HND page layouts.
 """
 from __future__ import annotations
 
