@@ -46,17 +46,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of the same launch as the bench step's call, valid
-# only while the kernel source is unchanged (sha256 prefix of the files it is
-# compiled from).
+# only while the kernel's code is unchanged (sha256 prefix of the files it is
+# compiled from, comments and layout aside).
 NCU_TRAFFIC = {
     # decode call of the mixed step (split-KV kernel + merge): 3157.7 MB read
     # and 7.2 MB of partials written by the partition kernel, 27.8 MB of
     # partials read back by the merge (cold caches under ncu; live they are
     # L2 hits); mean of two calls
-    "decode": {"bytes": 3192652800, "sha": "5be47219c2ce090e"},
+    "decode": {"bytes": 3192652800, "sha": "39e52c11020f41c0"},
     # prefill launch of the mixed step: 665.1 MB read + 85.6 MB written
     # (mean of two launches)
-    "prefill": {"bytes": 750740096, "sha": "637ca5d85c79f669"},
+    "prefill": {"bytes": 750740096, "sha": "933746382003040d"},
 }
 
 
@@ -263,11 +263,37 @@ PREFILL_SOURCES = ("prefill.cu", "prefill_common.cuh", "pkv_tcgen05.cuh", "pkv_d
 DECODE_SOURCES = ("decode.cu", "pkv_device.cuh", "pkv_internal.h")
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source with its comments removed and each line's whitespace
+    collapsed, string and character literals kept: what the compiler sees."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (" ".join(line.split()) for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_sha(*names):
+    """sha256 prefix of the code (comments and layout aside) of csrc files."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "paged_kv_cache_attention_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_attention_gb300", "csrc", n)) as f:
+            h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,14 +22,18 @@
 //               (page, 64-dim half) of K and of V into a 2-stage ring
 //               (128-byte swizzle); pages past the end are fetched out of
 //               bounds, which fills zeros;
-//   warp 1      owns TMEM; one thread issues tcgen05.mma:
-//                 S_x = Q_x K^T   (A, B K-major in smem, fp32 in TMEM)
+//   warp 1      owns TMEM; one thread issues tcgen05.mma (each group of 8
+//               k-steps from one PTX block, descriptors built once):
+//                 S_x = Q_x K^T   (A, B K-major in smem, fp32 in TMEM; with
+//                                  ALiBi one more k-step adds the bias)
 //                 O_x += P_x V    (A = P in TMEM as bf16, B = V MN-major)
-//   warps 2..9  two softmax warpgroups, one per query tile; thread = row =
-//               TMEM lane.  Each reads its S row with tcgen05.ld, masks,
-//               updates the running max (O is rescaled in TMEM only when the
-//               max grows by more than 2^8), writes P back to TMEM in place of
-//               S, and finally normalises O (sink included) and stores it.
+//   warps 2-17  softmax, eight per query tile: two per TMEM lane quarter,
+//               each owning half of its 32 rows' 128 key columns (thread =
+//               row = TMEM lane).  They read S with tcgen05.ld, mask, combine
+//               their partial row maxima through shared memory, rescale O in
+//               TMEM only when the maximum grows by more than 2^8, write P
+//               back to TMEM in place of S, and finally normalise O (sink
+//               included) and store it.
 // A small single-CTA kernel first builds the work list on the device
 // (counting sort by key-tile count, heaviest first).
 #include <type_traits>
