@@ -93,3 +93,15 @@ def test_max_over_ranks_with_gloo():
         assert p.exitcode == 0
     got = dict(q.get(timeout=10) for _ in range(world))
     assert got == {0: 2.5, 1: 2.5}
+
+
+def test_traffic_key_ignores_comments_only():
+    # the stored ncu traffic stays valid across comment edits and is dropped
+    # on any code change
+    code = 'int a = 1;  // one\n/* block\n   comment */ const char *s = "x // kept";\n'
+    assert bench.strip_c_comments(code) == 'int a = 1;\nconst char *s = "x // kept";'
+    assert bench.strip_c_comments(code.replace("// one", "// uno")) == \
+        bench.strip_c_comments(code)
+    assert bench.strip_c_comments(code.replace("a = 1", "a = 2")) != \
+        bench.strip_c_comments(code)
+    assert bench.strip_c_comments("x = '\\'' ; /* c */ y") == "x = '\\'' ; y"
