@@ -76,7 +76,7 @@ def test_adaptive_budget(S, Hq, Hkv, D):
     _check(S, Hq, Hkv, D, seed=S + D)
 
 
-@pytest.mark.parametrize("S,Hq,Hkv", [(1800, 8, 2), (2048, 16, 4)])
+@pytest.mark.parametrize("S,Hq,Hkv", [(1800, 8, 2), (2048, 16, 4), (16384, 4, 2)])
 def test_structured_long_sequence(S, Hq, Hkv):
     """Attention with local (slash) and stripe (vertical) structure, the kind
     the pattern is built to capture."""
