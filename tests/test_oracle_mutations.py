@@ -71,6 +71,26 @@ MUTATIONS = {
         "if (!(isv[j] || iss[i - j]))", "if (!(isv[j] && iss[i - j]))"),
     "cache write ignores the skip marker": (
         "if (s < 0) continue;", "if (s < -1) continue;"),
+    "lse in log2 units": (
+        "J->lse[(int64_t)out_row * Hq + h] = m + log(z);",
+        "J->lse[(int64_t)out_row * Hq + h] = m + log2(z);"),
+    "lse without the row maximum": (
+        "J->lse[(int64_t)out_row * Hq + h] = m + log(z);",
+        "J->lse[(int64_t)out_row * Hq + h] = log(z);"),
+    "minference: estimate softmax not normalised": (
+        "const double p = exp(s[j] - m) / z;\n                vh[j] += p;",
+        "const double p = exp(s[j] - m);\n                vh[j] += p;"),
+    "minference: estimate ignores the scale": (
+        "for (int j = 0; j <= pos; ++j) {\n                const int64_t kb = ((int64_t)j * Hkv + kvh) * D;\n"
+        "                double dot = 0.0;\n"
+        "                for (int d = 0; d < D; ++d) dot += widen(q, dtype, qb + d) * widen(k, dtype, kb + d);\n"
+        "                s[j] = scale * dot;",
+        "for (int j = 0; j <= pos; ++j) {\n                const int64_t kb = ((int64_t)j * Hkv + kvh) * D;\n"
+        "                double dot = 0.0;\n"
+        "                for (int d = 0; d < D; ++d) dot += widen(q, dtype, qb + d) * widen(k, dtype, kb + d);\n"
+        "                s[j] = dot;"),
+    "sparse attention: diagonal indexed by the key": (
+        "if (!(isv[j] || iss[i - j]))", "if (!(isv[j] || iss[j]))"),
 }
 
 
