@@ -137,6 +137,9 @@ def load_library(path: Optional[str] = None):
         lib.pkv_minference_prefill.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64,
                                                i32, i32, f32, P, P, P, sz, P, P]
         lib.pkv_minference_prefill.restype = i32
+        lib.pkv_paged_decode_noalloc.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, i32,
+                                                 i32, i32, f32, i32, P, P, P]
+        lib.pkv_paged_decode_noalloc.restype = i32
         _lib = lib
         return lib
 
@@ -321,6 +324,31 @@ def rope_reshape_and_cache(query, key, value, k_cache, v_cache, positions, slot_
     _check("pkv_rope_reshape_and_cache", st)
 
 
+def _decode_args(q, k_cache, v_cache, block_table, cache_seqlens, sink, out, lse, layout):
+    """Checks shared by the two decode entry points; returns (cache desc, out)."""
+    torch = _torch()
+    desc = _cache_desc(k_cache, v_cache, layout)
+    _cuda_contig("q", q, k_cache.dtype, 3)
+    _cuda_contig("block_table", block_table, torch.int32, 2)
+    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32, 1)
+    B, Hq, D = q.shape
+    _require(D == desc.head_dim, "head_dim of q and cache differ")
+    _require(block_table.shape[0] == B and cache_seqlens.shape[0] == B,
+             "block_table / cache_seqlens batch mismatch")
+    if sink is not None:
+        _cuda_contig("sink", sink, torch.float32, 1)
+        _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_contig("out", out, q.dtype, 3)
+        _require(out.shape == q.shape, "out must be shaped like q")
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32, 2)
+        _require(tuple(lse.shape) == (B, Hq), "lse must be [B, Hq]")
+    return desc, out
+
+
 def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: int,
                  sink=None, window_left: int = -1, sm_scale: Optional[float] = None,
                  partition_size: int = 512, out=None, lse=None, workspace=None,
@@ -336,26 +364,10 @@ def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: in
     [num_blocks, Hkv, block_size, D].
     """
     torch = _torch()
-    desc = _cache_desc(k_cache, v_cache, layout)
-    _cuda_contig("q", q, k_cache.dtype, 3)
-    _cuda_contig("block_table", block_table, torch.int32, 2)
-    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32, 1)
+    desc, out = _decode_args(q, k_cache, v_cache, block_table, cache_seqlens, sink, out, lse,
+                             layout)
     B, Hq, D = q.shape
-    _require(D == desc.head_dim, "head_dim of q and cache differ")
-    _require(block_table.shape[0] == B and cache_seqlens.shape[0] == B,
-             "block_table / cache_seqlens batch mismatch")
-    if sink is not None:
-        _cuda_contig("sink", sink, torch.float32, 1)
-        _require(sink.shape[0] == Hq, "sink must have num_qo_heads entries")
     _head_vector("alibi_slopes", alibi_slopes, Hq)
-    if out is None:
-        out = torch.empty_like(q)
-    else:
-        _cuda_contig("out", out, q.dtype, 3)
-        _require(out.shape == q.shape, "out must be shaped like q")
-    if lse is not None:
-        _cuda_contig("lse", lse, torch.float32, 2)
-        _require(tuple(lse.shape) == (B, Hq), "lse must be [B, Hq]")
     scale = float(sm_scale) if sm_scale is not None else D ** -0.5
     need = paged_decode_workspace_size(B, Hq, D, max_seqlen, partition_size, window_left)
     ws = _workspace(need, q.device, workspace)
@@ -539,27 +551,12 @@ def paged_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, max_se
     GPU.  The first call on a device should come before any stream capture.
     ``out`` (and ``lse``) should be preallocated when the caller must not
     allocate at all."""
-    torch = _torch()
-    lib = load_library()
-    fn = lib.pkv_paged_decode_noalloc
-    if fn.argtypes is None:
-        P, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        fn.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, i32, i32, i32, f32, i32, P, P,
-                       P]
-        fn.restype = i32
-    desc = _cache_desc(k_cache, v_cache, layout)
-    _cuda_contig("q", q, k_cache.dtype, 3)
-    _cuda_contig("block_table", block_table, torch.int32, 2)
-    _cuda_contig("cache_seqlens", cache_seqlens, torch.int32, 1)
+    desc, out = _decode_args(q, k_cache, v_cache, block_table, cache_seqlens, sink, out, lse,
+                             layout)
     B, Hq, D = q.shape
-    if sink is not None:
-        _cuda_contig("sink", sink, torch.float32, 1)
-    if out is None:
-        out = torch.empty_like(q)
     scale = float(sm_scale) if sm_scale is not None else D ** -0.5
-    st = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
-            block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink),
-        _ptr(alibi_slopes), B, Hq,
+    st = load_library().pkv_paged_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
+            block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink), B, Hq,
             int(window_left), scale, int(partition_size), _ptr(lse), _ptr(dev_error),
             _stream_handle(stream))
     _check("pkv_paged_decode_noalloc", st)

@@ -217,3 +217,99 @@ def test_ntk_scaled_base():
     # the lowest frequency base^(-(rd-2)/rd) is divided by exactly alpha
     b = pkv.ntk_scaled_base(10000.0, 128, 4.0)
     assert abs(b ** (-126 / 128) * 4.0 - 10000.0 ** (-126 / 128)) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# the binding against the header: ctypes passes arguments by the declared
+# types, so a declaration that drifts from include/pkv.h would pass wrong
+# values without any error
+# ---------------------------------------------------------------------------
+def _strip_c_comments(src):
+    return re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", src, flags=re.S))
+
+
+def _prototypes():
+    """(name, return type, [parameter types]) of every PKV_API function."""
+    out = []
+    for h in HEADERS:
+        src = _strip_c_comments(open(h).read())
+        for ret, name, params in re.findall(
+                r"PKV_API\s+([\w\s\*]*?)\s*\b(pkv_\w+)\s*\(([^)]*)\)\s*;", src):
+            ps = [" ".join(p.split()) for p in params.split(",")]
+            if ps == ["void"]:
+                ps = []
+            out.append((name, " ".join(ret.split()), ps))
+    return out
+
+
+_C_TYPES = {"int": ctypes.c_int, "int32_t": ctypes.c_int32, "pkv_status": ctypes.c_int,
+            "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "float": ctypes.c_float,
+            "double": ctypes.c_double, "pkv_cache_desc": pkv.CacheDesc}
+
+
+def _ctype(decl, is_return=False):
+    """The ctypes type a C declaration (type, optionally followed by a name) maps to."""
+    if "*" in decl:
+        if is_return and decl.replace(" ", "") == "constchar*":
+            return ctypes.c_char_p
+        return ctypes.c_void_p
+    words = [w for w in decl.split() if w != "const"]
+    base = words[0] if is_return else " ".join(words[:-1])
+    return _C_TYPES[base]
+
+
+def test_binding_declares_every_function_as_the_header_does():
+    lib = pkv.load_library()
+    protos = _prototypes()
+    assert {n for n, _, _ in protos} == set(_declared_symbols())
+    for name, ret, params in protos:
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes in the binding"
+        want = [_ctype(p) for p in params]
+        assert list(fn.argtypes) == want, f"{name}: argtypes differ from the header"
+        assert fn.restype is _ctype(ret, is_return=True), f"{name}: restype differs"
+
+
+def test_cache_desc_matches_the_header_struct():
+    src = _strip_c_comments(open(os.path.join(ROOT, "include", "pkv.h")).read())
+    body = re.search(r"typedef struct pkv_cache_desc\s*\{(.*?)\}\s*pkv_cache_desc;", src,
+                     re.S).group(1)
+    fields = [f.split() for f in body.split(";") if f.strip()]
+    assert [(n, _C_TYPES[t]) for t, n in fields] == list(pkv.CacheDesc._fields_)
+
+
+def test_python_sources_define_every_name_they_read():
+    """A static check over the package, the bench, the entry points, the
+    oracle's loader and the tests: every global name a function reads is
+    defined in its module or is a builtin."""
+    import builtins
+    import glob
+    import symtable
+    files = (glob.glob(os.path.join(ROOT, "paged_kv_cache_attention_gb300", "*.py")) +
+             glob.glob(os.path.join(ROOT, "tests", "*.py")) +
+             [os.path.join(ROOT, f) for f in ("bench.py", "__graft_entry__.py",
+                                              os.path.join("oracle", "__init__.py"))])
+    missing = []
+    for path in files:
+        top = symtable.symtable(open(path).read(), path, "exec")
+        known = set(top.get_identifiers()) | set(dir(builtins))
+
+        def walk(t):
+            for s in t.get_symbols():
+                if s.is_global() and not s.is_declared_global() and s.get_name() not in known:
+                    missing.append(f"{os.path.relpath(path, ROOT)}: {t.get_name()} reads "
+                                   f"{s.get_name()}")
+            for c in t.get_children():
+                walk(c)
+        walk(top)
+    assert not missing, "\n".join(missing)
+
+
+@nogpu
+def test_noalloc_rejects_problems_beyond_the_scratch_before_any_cuda_call():
+    lib = pkv.load_library()
+    huge = 1 << 20  # 2048 partitions of 512 for 4 x 32 heads: more than the 32 MiB scratch
+    assert pkv.paged_decode_workspace_size(4, 32, 128, huge, 512, -1) > (32 << 20)
+    st = lib.pkv_paged_decode_noalloc(FAKE, FAKE, FAKE, FAKE, _desc(), FAKE, 8, FAKE, huge,
+                                      None, 4, 32, -1, 0.1, 512, None, None, None)
+    assert st == 3  # PKV_ERR_WORKSPACE

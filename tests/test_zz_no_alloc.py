@@ -100,3 +100,26 @@ def test_noalloc_rejects_problems_beyond_the_scratch():
     torch.cuda.synchronize()
     assert st == PKV_ERR_WORKSPACE
     assert int(out.abs().sum()) == 0  # nothing ran
+
+
+def test_binding_noalloc_matches_paged_decode():
+    """The Python binding of the entry point (argument marshalling only) gives
+    what the workspace entry point gives on the same inputs."""
+    case = W.make_decode([300, 17, 1024, 4096], 32, 8, 128, 16, torch.bfloat16, seed=43,
+                         sink="randn")
+    t = _tensors(case)
+    ref_lse = torch.empty(case.batch, case.num_qo_heads, dtype=torch.float32, device=dev())
+    ref = pkv.paged_decode(t["q"], t["kc"], t["vc"], t["bt"], t["sl"], case.max_seqlen,
+                           sink=t["sink"], sm_scale=case.sm_scale,
+                           partition_size=case.partition_size, lse=ref_lse)
+    lse = torch.full_like(ref_lse, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    out = pkv.paged_decode_noalloc(t["q"], t["kc"], t["vc"], t["bt"], t["sl"], case.max_seqlen,
+                                   sink=t["sink"], sm_scale=case.sm_scale,
+                                   partition_size=case.partition_size, lse=lse, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o, r = out.float().cpu().numpy(), ref.float().cpu().numpy()
+    assert np.isfinite(o).all()
+    assert np.abs(o - r).max() <= TOL[case.q.dtype]
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=0, atol=1e-5)
