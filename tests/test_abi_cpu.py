@@ -313,3 +313,16 @@ def test_noalloc_rejects_problems_beyond_the_scratch_before_any_cuda_call():
     st = lib.pkv_paged_decode_noalloc(FAKE, FAKE, FAKE, FAKE, _desc(), FAKE, 8, FAKE, huge,
                                       None, 4, 32, -1, 0.1, 512, None, None, None)
     assert st == 3  # PKV_ERR_WORKSPACE
+
+
+def test_minference_sizes_agree_with_the_oracle():
+    """The library's host-side budget arithmetic (how many columns and
+    diagonals are kept) against the oracle's, across lengths around the
+    caps and the page's default and fixed budgets."""
+    import oracle
+    for S in (1, 2, 31, 63, 64, 100, 101, 155, 517, 1000, 4096, 20000, 32768, 131072):
+        for budget in (0.3, 0.1, 0.05, 0.5, None):
+            for vs, ss in ((1000, 6096), (7, 3), (64, 4096)):
+                for sink_tokens, recent in ((30, 100), (0, 0), (4, 16)):
+                    args = (S, vs, ss, budget, sink_tokens, recent)
+                    assert pkv.minference_sizes(*args) == oracle.minference_sizes(*args), args
