@@ -374,9 +374,8 @@ def paged_decode(q, k_cache, v_cache, block_table, cache_seqlens, max_seqlen: in
     st = load_library().pkv_paged_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
         block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink),
-        _ptr(alibi_slopes), B, Hq,
-        int(window_left), scale, int(partition_size), _ptr(lse), _ptr(ws),
-        ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
+        _ptr(alibi_slopes), B, Hq, int(window_left), scale, int(partition_size), _ptr(lse),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
     _check("pkv_paged_decode", st)
     return out
 
@@ -422,9 +421,8 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
         block_table.shape[1], _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), int(max_seqlen_q),
         int(max_seqlen_k), int(total_q), _ptr(sink), _ptr(alibi_slopes), B, Hq,
-        int(bool(causal)),
-        int(window_left), scale, _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
-        _ptr(dev_error), _stream_handle(stream))
+        int(bool(causal)), int(window_left), scale, _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill", st)
     return out
 
@@ -468,8 +466,7 @@ def varlen_prefill_contiguous(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_seqlen_
         _ptr(out), _ptr(q), _ptr(k) if total_k else None, _ptr(v) if total_k else None,
         int(total_k), Hkv, D, _dtype_code(q.dtype), _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k),
         int(max_seqlen_q), int(max_seqlen_k), int(total_q), _ptr(sink), _ptr(alibi_slopes), B,
-        Hq,
-        int(bool(causal)), int(window_left), scale, _ptr(lse), _ptr(ws),
+        Hq, int(bool(causal)), int(window_left), scale, _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill_contiguous", st)
     return out

@@ -326,3 +326,24 @@ def test_minference_sizes_agree_with_the_oracle():
                 for sink_tokens, recent in ((30, 100), (0, 0), (4, 16)):
                     args = (S, vs, ss, budget, sink_tokens, recent)
                     assert pkv.minference_sizes(*args) == oracle.minference_sizes(*args), args
+
+
+def test_binding_calls_pass_as_many_arguments_as_the_header_declares():
+    """Every pkv_* call in the binding's source passes one argument per
+    parameter of its prototype (ctypes would raise only at call time)."""
+    import ast
+    nparams = {name: len(params) for name, _, params in _prototypes()}
+    path = os.path.join(ROOT, "paged_kv_cache_attention_gb300", "__init__.py")
+    seen = set()
+    for node in ast.walk(ast.parse(open(path).read())):
+        if (isinstance(node, ast.Call) and isinstance(node.func, ast.Attribute) and
+                node.func.attr in nparams):
+            assert not node.keywords and not any(isinstance(a, ast.Starred) for a in node.args)
+            assert len(node.args) == nparams[node.func.attr], \
+                f"line {node.lineno}: {node.func.attr} takes {nparams[node.func.attr]} arguments"
+            seen.add(node.func.attr)
+    # every entry point the binding wraps is called through its own name
+    assert {"pkv_reshape_and_cache", "pkv_paged_decode", "pkv_paged_decode_noalloc",
+            "pkv_varlen_prefill", "pkv_varlen_prefill_contiguous", "pkv_rope_cos_sin_table",
+            "pkv_rope_reshape_and_cache", "pkv_minference_sizes",
+            "pkv_minference_prefill"} <= seen
