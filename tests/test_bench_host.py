@@ -105,3 +105,37 @@ def test_traffic_key_ignores_comments_only():
     assert bench.strip_c_comments(code.replace("a = 1", "a = 2")) != \
         bench.strip_c_comments(code)
     assert bench.strip_c_comments("x = '\\'' ; /* c */ y") == "x = '\\'' ; y"
+
+
+def test_clock_sampler_reads_the_nvidia_smi_csv(tmp_path):
+    """The clocks record of the bench line from sampled nvidia-smi rows: the
+    median SM clock of the loaded half of the samples, the maximum clock, and
+    every throttle reason seen Active in any sample."""
+    rows = ["0, 1200, 2070, 350.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1965, 2070, 990.5, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2070, 2070, 1010.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 2040, 2070, 1005.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, [N/A], 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbage line"]
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(rows) + "\n")
+
+    class _Done:  # a sampler process that has already exited
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s = bench.ClockSampler(0)
+    s.proc, s.path = _Done(), str(path)
+    clk = s.stop()
+    assert clk["samples"] == 5
+    assert clk["sm_max_mhz"] == 2070.0
+    assert clk["sm_mhz"] == 2055.0  # median of the upper half (2040, 2070) of the four clocks
+    assert clk["reasons"] == ["sw_power_cap"]
+    assert not path.exists()
+
+    s2 = bench.ClockSampler(0)
+    s2.proc = None
+    assert s2.stop()["reasons"] == ["nvidia-smi unavailable"]
