@@ -552,9 +552,10 @@ def paged_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, max_se
                              layout)
     B, Hq, D = q.shape
     scale = float(sm_scale) if sm_scale is not None else D ** -0.5
-    st = load_library().pkv_paged_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
-            block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink), B, Hq,
-            int(window_left), scale, int(partition_size), _ptr(lse), _ptr(dev_error),
-            _stream_handle(stream))
+    st = load_library().pkv_paged_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), desc, _ptr(block_table),
+        block_table.shape[1], _ptr(cache_seqlens), int(max_seqlen), _ptr(sink), B, Hq,
+        int(window_left), scale, int(partition_size), _ptr(lse), _ptr(dev_error),
+        _stream_handle(stream))
     _check("pkv_paged_decode_noalloc", st)
     return out
