@@ -76,7 +76,7 @@ def _load():
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_rope.argtypes = [P, P, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, P,
                                         ctypes.c_int, ctypes.c_double, ctypes.c_double,
-                                        ctypes.c_int]
+                                        ctypes.c_double, ctypes.c_int]
             lib.oracle_rope.restype = None
             lib.oracle_minference_scores.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -191,10 +191,14 @@ def attention(q, k_cache, v_cache, block_table, cu_seq_lens_q, kv_lens, sink=Non
 
 
 def rope(x, positions, rotary_dim: int, base: float = 10000.0, position_scale: float = 1.0,
-         neox: bool = True) -> np.ndarray:
+         neox: bool = True, ntk_alpha: float = 1.0) -> np.ndarray:
     """Rotary position embedding of x [T, H, D] (float32, or uint16 bf16 bits)
     at positions [T]; returns float64 [T, H, D].  Dimensions past rotary_dim
-    are copied.  position_scale divides the positions (linear scaling)."""
+    are copied.  position_scale divides the positions (linear scaling);
+    ntk_alpha != 1 raises the base for NTK-aware scaling (vLLM attention.py,
+    PagedAttentionWithRoPE's "dynamic" rope_scaling, read as NTK)."""
+    if ntk_alpha != 1.0 and not (ntk_alpha > 0 and rotary_dim > 2):
+        raise ValueError("rope: ntk_alpha > 0 and rotary_dim > 2")
     x = np.ascontiguousarray(x)
     pos = np.ascontiguousarray(positions, dtype=np.int64)
     T, H, D = x.shape
@@ -202,7 +206,7 @@ def rope(x, positions, rotary_dim: int, base: float = 10000.0, position_scale: f
         raise ValueError("rope: positions must be [T]; rotary_dim even, 0 < rotary_dim <= D")
     out = np.empty((T, H, D), dtype=np.float64)
     _load().oracle_rope(_ptr(out), _ptr(x), _dtype_code(x), T, H, D, _ptr(pos), int(rotary_dim),
-                        float(base), float(position_scale), int(bool(neox)))
+                        float(base), float(position_scale), float(ntk_alpha), int(bool(neox)))
     return out
 
 

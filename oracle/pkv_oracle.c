@@ -301,12 +301,19 @@ int oracle_online_cores(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }
  *   - the pairs: neox style (a, b) = (i, i + rotary_dim/2), the two halves
  *     of the rotated part; otherwise (GPT-J style) (a, b) = (2i, 2i + 1);
  *   - dimensions rotary_dim .. head_dim-1 are not rotated.
+ * The page's "dynamic" rope_scaling is read as NTK-aware scaling: to stretch
+ * the usable context ntk_alpha times, the base is raised to
+ *   base * ntk_alpha^(rotary_dim / (rotary_dim - 2)),
+ * which divides the lowest frequency (i = rotary_dim/2 - 1) by exactly
+ * ntk_alpha and leaves the highest (i = 0) alone; ntk_alpha = 1 is no
+ * scaling.
  * x: [num_tokens, num_heads, head_dim] in dtype; out: the same shape, fp64,
  * every value exact up to the rounding of double arithmetic. */
 void oracle_rope(double *out, const void *x, int dtype, int64_t num_tokens, int num_heads,
                  int head_dim, const int64_t *positions, int rotary_dim, double base,
-                 double position_scale, int neox) {
+                 double position_scale, double ntk_alpha, int neox) {
     const int half = rotary_dim / 2;
+    if (ntk_alpha != 1.0) base = base * pow(ntk_alpha, (double)rotary_dim / (rotary_dim - 2));
     for (int64_t t = 0; t < num_tokens; ++t) {
         const double m = (double)positions[t] / position_scale;
         for (int h = 0; h < num_heads; ++h) {

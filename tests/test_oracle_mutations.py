@@ -51,6 +51,9 @@ MUTATIONS = {
         "const int b = neox ? i + half - 1 : 2 * i + 1;"),
     "rope: position scale multiplies": (
         "(double)positions[t] / position_scale", "(double)positions[t] * position_scale"),
+    "rope: NTK exponent inverted": (
+        "pow(ntk_alpha, (double)rotary_dim / (rotary_dim - 2))",
+        "pow(ntk_alpha, (double)(rotary_dim - 2) / rotary_dim)"),
     "rope: unrotated tail dropped": (
         "for (int d = 0; d < head_dim; ++d) out[row + d] = widen(x, dtype, row + d);",
         "for (int d = 0; d < head_dim; ++d) out[row + d] = 0.0;"),

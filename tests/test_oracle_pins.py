@@ -418,6 +418,33 @@ def test_rope_linear_scaling_divides_the_position():
     np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("rd,alpha", [(64, 4.0), (128, 2.5), (16, 8.0)])
+def test_rope_ntk_scaling_divides_the_lowest_frequency(rd, alpha):
+    """NTK-aware scaling (the page's "dynamic" rope_scaling) raises the base so
+    that the lowest frequency, i = rd/2 - 1, is divided by exactly alpha (its
+    wavelength stretched alpha times) while the highest, i = 0, is kept.  The
+    angle of each frequency is read back from the rotation of a unit vector
+    (neox pair (i, i + rd/2)): x_a = 1, x_b = 0 turns into (cos, sin) of
+    position * theta_i."""
+    half = rd // 2
+    x = np.zeros((half, 1, rd), np.float32)
+    for i in range(half):
+        x[i, 0, i] = 1.0
+
+    def angles(m, a):
+        out = oracle.rope(x, [m] * half, rd, ntk_alpha=a)
+        return np.array([np.arctan2(out[i, 0, i + half], out[i, 0, i]) for i in range(half)])
+
+    lo = half - 1
+    m_lo = 2000  # position * theta_lo stays below pi for both bases
+    assert abs(angles(m_lo, alpha)[lo] * alpha - angles(m_lo, 1.0)[lo]) < 1e-12
+    assert abs(angles(3, alpha)[0] - 3.0) < 1e-12 and abs(angles(3, 1.0)[0] - 3.0) < 1e-12
+    # every frequency in between is lowered, monotonically in i (position 3
+    # keeps every angle below pi)
+    r = angles(3, alpha)[1:] / angles(3, 1.0)[1:]
+    assert np.all(r < 1.0) and np.all(np.diff(r) < 0)
+
+
 def test_rope_neox_is_gptj_on_interleaved_dims():
     """neox pairs (i, i + rd/2); GPT-J pairs (2i, 2i+1): moving dim i to 2i and
     dim i + rd/2 to 2i + 1 turns one into the other."""
