@@ -58,20 +58,25 @@
  * nothing and keeps no state between calls except a process-wide cache of
  * the driver's tensor-map encoder and of per-device attributes.  Scratch
  * space (split-KV partials) lives in the caller's workspace, whose size the
- * *_workspace_size functions give.  The library never reads device memory
- * from the host and never synchronises the stream.
+ * *_workspace_size functions give.  Apart from pkv_get_device_error, the
+ * library never reads device memory from the host and never synchronises
+ * the stream.
  *
  * Errors: arguments are validated on the host before anything is launched;
  * a non-zero pkv_status is returned and nothing runs.  Metadata that only the
  * device sees (a block id outside the pool, a slot outside the pool, a
- * sequence length larger than the declared maximum) is checked in the
- * kernels: the offending page or row is skipped and a PKV_DEVERR_* bit is
- * OR-ed into *dev_error (a device int32 the caller owns and zeroes; may be
- * NULL).  No kernel traps.
+ * sequence length larger than the declared maximum or an offset outside the
+ * rows of q) is checked in the kernels: the offending page or row is skipped
+ * and a PKV_DEVERR_* bit is OR-ed into *dev_error (a device int32 the caller
+ * owns and zeroes; may be NULL).  No kernel traps.  pkv_get_device_error
+ * reads that word back and turns it into a status (PKV_ERR_OUT_OF_RANGE).
+ * The word is the caller's (not part of a workspace) so that one word can
+ * collect the checks of every call of a step, cache writes included.
  *
- * Supported in this version: head_dim 64 or 128; block_size 16 or 32;
- * num_qo_heads % num_kv_heads == 0 with G <= 16; decode in fp32 or bf16,
- * prefill in bf16 (causal only); the output has the dtype of the cache.
+ * What each call supports (head sizes, page sizes, dtypes, layouts, causal
+ * or not, ALiBi, GQA group sizes) is listed with the call below; all calls
+ * take block_size 16 or 32 and num_qo_heads % num_kv_heads == 0, and the
+ * attention output has the dtype of the cache.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -94,7 +99,13 @@ typedef enum pkv_status {
     PKV_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shape */
     PKV_ERR_UNSUPPORTED = 2, /* a shape or dtype this version has no kernel for */
     PKV_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
-    PKV_ERR_CUDA = 4         /* a CUDA call failed (launch, tensor-map encode) */
+    PKV_ERR_CUDA = 4,        /* a CUDA call failed (launch, tensor-map encode, sync) */
+    PKV_ERR_OUT_OF_RANGE = 5, /* pkv_get_device_error: the kernels found device
+                                 metadata out of range (PKV_DEVERR_BLOCK_ID, _SLOT,
+                                 _SEQLEN or _POSITION) and skipped it */
+    PKV_ERR_TIMEOUT = 6      /* pkv_get_device_error: a bounded pipeline wait gave up
+                                (PKV_DEVERR_TIMEOUT); the outputs of that call are
+                                not valid */
 } pkv_status;
 
 typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -108,7 +119,8 @@ typedef enum pkv_layout { PKV_NHD = 0, PKV_HND = 1 } pkv_layout;
 #define PKV_DEVERR_BLOCK_ID 1u /* block_table entry of an attended position outside [0, num_blocks) */
 #define PKV_DEVERR_SLOT 2u     /* slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEVERR_SEQLEN 4u   /* a length above its declared maximum, negative, or
-                                  beyond max_blocks_per_seq * block_size */
+                                  beyond max_blocks_per_seq * block_size; a
+                                  cu_seq_lens offset outside the rows of q / k */
 #define PKV_DEVERR_TIMEOUT 8u  /* a bounded pipeline wait gave up */
 #define PKV_DEVERR_POSITION 16u /* a rotary position outside [0, max_position) */
 
@@ -127,6 +139,31 @@ PKV_API const char *pkv_status_string(int status);
 
 /* Library ABI version (major * 100 + minor). */
 PKV_API int pkv_version(void);
+
+/*
+ * get_device_error: the device-side check result of the calls issued so far.
+ * Waits for `stream` to finish (cudaStreamSynchronize), reads the caller's
+ * int32 error word dev_error (device memory; the word every call of this
+ * library ORs its PKV_DEVERR_* bits into) and stores its bits in *bits
+ * (host; may be NULL).  With clear != 0 the word is then reset to zero on
+ * `stream`.  This is the one call of the library that synchronises and reads
+ * device memory from the host.
+ *
+ * Returns PKV_OK when no bit is set; PKV_ERR_TIMEOUT when PKV_DEVERR_TIMEOUT
+ * is set; otherwise PKV_ERR_OUT_OF_RANGE when a metadata bit is set (a block
+ * id, slot, length or position outside its range: the kernels skipped the
+ * offending page, row or token, so the outputs that depend on it are not the
+ * attention the caller meant); PKV_ERR_INVALID_ARG for a NULL dev_error;
+ * PKV_ERR_CUDA when the synchronisation or the copy fails.
+ *
+ * The pages put the cache write before the attention in one forward
+ * (vLLM attention.py, PagedAttention.forward) and mark unallocated block
+ * table entries with -1 (transformers docs "paged_attention", decode path);
+ * this call is how a caller learns that such an entry, or any other device
+ * metadata, was out of range.
+ */
+PKV_API pkv_status pkv_get_device_error(const int32_t *dev_error, int32_t *bits, int clear,
+                                        void *stream);
 
 /*
  * reshape_and_cache: for every t in [0, num_tokens) with slot_mapping[t] >= 0,
@@ -148,14 +185,20 @@ PKV_API pkv_status pkv_reshape_and_cache(const void *key, const void *value, voi
  *
  * rope_cos_sin_table: fill cos_sin ([max_position, rotary_dim / 2] pairs of
  * float32 (cos, sin), device memory owned by the caller, 16-byte aligned)
- * with the angles (pos / position_scale) * base^(-2i / rotary_dim) for
- * pos in [0, max_position) and i in [0, rotary_dim / 2).  The angles and
+ * with the angles (pos / position_scale) * b^(-2i / rotary_dim) for
+ * pos in [0, max_position) and i in [0, rotary_dim / 2), where
+ * b = base * ntk_alpha^(rotary_dim / (rotary_dim - 2)).  The angles and
  * their cos/sin are computed in fp64 and rounded once to fp32.  Linear
- * scaling is position_scale = factor; dynamic-NTK scaling is an adjusted
- * base (computed by the caller).  Build the table once per configuration.
+ * scaling ("linear" rope_scaling) is position_scale = factor; NTK-aware
+ * scaling (the reading taken of "dynamic" rope_scaling) is ntk_alpha =
+ * the context stretch the caller wants, which divides the lowest frequency
+ * by exactly ntk_alpha and keeps the highest; ntk_alpha = 1 is no NTK
+ * scaling (then rotary_dim may be 2).  Build the table once per
+ * configuration.
  */
 PKV_API pkv_status pkv_rope_cos_sin_table(float *cos_sin, int max_position, int rotary_dim,
-                                          double base, double position_scale, void *stream);
+                                          double base, double position_scale, double ntk_alpha,
+                                          void *stream);
 
 /*
  * rope_reshape_and_cache: for every token t, at position positions[t]:
@@ -352,7 +395,10 @@ PKV_API pkv_status pkv_minference_prefill(void *out, const void *q, const void *
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * capture.  The address is kept for the life of the process: after a
+ * cudaDeviceReset of that device the entry point must not be called again
+ * (the reset unloads the array; the kept address would then be stale).  A
+ * call with batch == 0 returns PKV_OK without touching the device.  All calls share the one array and it keeps the last call's
  * contents: nothing in it needs to start at zero, because every call writes
  * each partial it later reads.  Calls that can overlap on the GPU (concurrent
  * streams, or several host threads) race on the array: serialise them.

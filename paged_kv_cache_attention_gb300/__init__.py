@@ -42,7 +42,7 @@ __all__ = [
     "build", "load_library", "PkvError", "reshape_and_cache", "paged_decode",
     "varlen_prefill", "varlen_prefill_contiguous", "paged_decode_noalloc",
     "paged_decode_workspace_size", "varlen_prefill_workspace_size",
-    "rope_cos_sin_table", "rope_reshape_and_cache", "ntk_scaled_base",
+    "rope_cos_sin_table", "rope_reshape_and_cache", "get_device_error",
     "minference_sizes", "minference_prefill",
     "DEVERR_BLOCK_ID", "DEVERR_SLOT", "DEVERR_SEQLEN", "DEVERR_TIMEOUT", "DEVERR_POSITION",
     "EXPORTED_SYMBOLS",
@@ -62,6 +62,7 @@ EXPORTED_SYMBOLS = (
     "pkv_varlen_prefill_workspace_size", "pkv_varlen_prefill",
     "pkv_varlen_prefill_contiguous", "pkv_rope_cos_sin_table", "pkv_rope_reshape_and_cache",
     "pkv_minference_sizes", "pkv_minference_workspace_size", "pkv_minference_prefill",
+    "pkv_paged_decode_noalloc", "pkv_get_device_error",
 )
 
 
@@ -125,7 +126,7 @@ def load_library(path: Optional[str] = None):
                                                       P, sz, P, P]
         lib.pkv_varlen_prefill_contiguous.restype = i32
         f64 = ctypes.c_double
-        lib.pkv_rope_cos_sin_table.argtypes = [P, i32, i32, f64, f64, P]
+        lib.pkv_rope_cos_sin_table.argtypes = [P, i32, i32, f64, f64, f64, P]
         lib.pkv_rope_cos_sin_table.restype = i32
         lib.pkv_rope_reshape_and_cache.argtypes = [P, P, P, P, P, P, P, i64, i32, CacheDesc, P,
                                                    i32, i32, i32, P, P]
@@ -140,6 +141,8 @@ def load_library(path: Optional[str] = None):
         lib.pkv_paged_decode_noalloc.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, P, i32,
                                                  i32, i32, f32, i32, P, P, P]
         lib.pkv_paged_decode_noalloc.restype = i32
+        lib.pkv_get_device_error.argtypes = [P, P, i32, P]
+        lib.pkv_get_device_error.restype = i32
         _lib = lib
         return lib
 
@@ -264,27 +267,37 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, dev_error=None
     _check("pkv_reshape_and_cache", st)
 
 
-def ntk_scaled_base(base: float, rotary_dim: int, alpha: float) -> float:
-    """Base of NTK-aware rotary scaling: stretching the context alpha times
-    raises the base to base * alpha^(rotary_dim / (rotary_dim - 2)), so that
-    the lowest frequency is interpolated by alpha while the highest is kept.
-    A dynamic-NTK caller picks alpha from the length it needs and passes the
-    result as ``base`` to rope_cos_sin_table."""
-    _require(rotary_dim > 2 and alpha > 0, "ntk_scaled_base: rotary_dim > 2, alpha > 0")
-    return float(base) * float(alpha) ** (rotary_dim / (rotary_dim - 2))
+def get_device_error(dev_error, clear: bool = False, stream=None, raise_on_error: bool = False):
+    """The PKV_DEVERR_* bits the calls so far ORed into ``dev_error`` (an int32
+    device tensor of one element).  Waits for ``stream`` (the current one by
+    default); with ``clear`` the word is then zeroed on that stream.  With
+    ``raise_on_error`` a set bit raises PkvError (PKV_ERR_OUT_OF_RANGE, or
+    PKV_ERR_TIMEOUT for a pipeline wait that gave up)."""
+    torch = _torch()
+    _cuda_contig("dev_error", dev_error, torch.int32, 1)
+    bits = ctypes.c_int32(0)
+    st = load_library().pkv_get_device_error(_ptr(dev_error), ctypes.addressof(bits),
+                                             int(bool(clear)), _stream_handle(stream))
+    if st != 0 and (raise_on_error or st not in (5, 6)):
+        _check("pkv_get_device_error", st)
+    return int(bits.value)
 
 
 def rope_cos_sin_table(max_position: int, rotary_dim: int, base: float = 10000.0,
-                       position_scale: float = 1.0, device=None, stream=None):
+                       position_scale: float = 1.0, ntk_alpha: float = 1.0, device=None,
+                       stream=None):
     """The rotary table [max_position, rotary_dim // 2, 2] float32 of
-    (cos, sin) of (pos / position_scale) * base^(-2i / rotary_dim), computed
-    in fp64 on the GPU.  position_scale is the linear scaling factor."""
+    (cos, sin) of (pos / position_scale) * b^(-2i / rotary_dim), computed in
+    fp64 on the GPU, b = base * ntk_alpha^(rotary_dim / (rotary_dim - 2)).
+    position_scale is the linear scaling factor, ntk_alpha the NTK-aware
+    context stretch (1: none)."""
     torch = _torch()
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     tab = torch.empty(max(max_position, 0), rotary_dim // 2, 2, dtype=torch.float32, device=dev)
     st = load_library().pkv_rope_cos_sin_table(_ptr(tab) if tab.numel() else None,
                                                int(max_position), int(rotary_dim), float(base),
-                                               float(position_scale), _stream_handle(stream))
+                                               float(position_scale), float(ntk_alpha),
+                                               _stream_handle(stream))
     _check("pkv_rope_cos_sin_table", st)
     return tab
 

@@ -65,6 +65,30 @@ __device__ __forceinline__ int window_start(int L, int window_left) {
     return s > 0 ? s : 0;
 }
 
+// The partition a CTA of the partition grid (x = kv head, y = sequence,
+// z = slot) takes, and its token range [tok_lo, tok_hi).  Sequence b has
+// n_b partitions (absolute P-aligned blocks meeting [start, L)); slot z takes
+// partition pidx = n_b - gridDim.z + z, so the last slot of every sequence
+// holds its last partition -- the partial one -- and those are launched last
+// (the block scheduler dispatches in grid order): the tail of the launch is
+// short partitions, and the slots a short sequence does not use are at the
+// front, where their CTAs exit at once.  Returns false for an unused slot.
+__device__ __forceinline__ bool decode_partition(const DecodeParams &p, int b, int z,
+                                                 int block_size, bool report, int &L,
+                                                 int &pidx, int &tok_lo, int &tok_hi) {
+    L = clipped_seqlen(p, b, block_size, report);
+    tok_lo = tok_hi = 0;
+    const int start = window_start(L, p.window_left);
+    const int P = p.partition_size;
+    const int n = L > 0 ? (L - 1) / P - start / P + 1 : 0;
+    pidx = n - (int)gridDim.z + z;
+    if (pidx < 0) return false;
+    const int part = start / P + pidx;
+    tok_lo = max(part * P, start);
+    tok_hi = min((part + 1) * P, L);
+    return tok_lo < tok_hi;
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023);
     return reinterpret_cast<uint8_t *>(a);
@@ -150,16 +174,15 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
     float *s_l = reinterpret_cast<float *>(smem + C::L_OFF);
 
     // grid: x = kv head (fastest, so the heads reading one page run together),
-    // y = partition index, z = sequence
-    const int b = blockIdx.z, g = blockIdx.x, pidx = blockIdx.y;
+    // y = sequence, z = partition slot (decode_partition)
+    pdl_trigger();  // the merge kernel may launch once every CTA has started
+    const int b = blockIdx.y, g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = clipped_seqlen(p, b, BS, pidx == 0 && g == 0 && threadIdx.x == 0);
-    const int start = window_start(L, p.window_left);
-    const int P = p.partition_size;
-    const int part = start / P + pidx;
-    const int tok_lo = max(part * P, start);
-    const int tok_hi = min((part + 1) * P, L);
-    if (tok_lo >= tok_hi) return;  // this partition holds no attended key
+    int L, pidx, tok_lo, tok_hi;
+    if (!decode_partition(p, b, blockIdx.z, BS,
+                          blockIdx.z == gridDim.z - 1 && g == 0 && threadIdx.x == 0, L, pidx,
+                          tok_lo, tok_hi))
+        return;  // this slot holds no attended key
     const int pg_lo = tok_lo / BS;
     const int npages = (tok_hi - 1) / BS - pg_lo + 1;
 
@@ -257,7 +280,7 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
     for (int j = 0; j < nmine; ++j) {
         const int i = warp + j * kDecWarps;
         const int s = j % NST;
-        if (!mbar_wait_bounded(wbars + 8 * s, (j / NST) & 1, p.dev_error)) break;
+        if (!warp_wait_bounded(wbars + 8 * s, (j / NST) & 1, p.dev_error)) break;
         consumed = j + 1;
         const int blk = s_blk[i];
         if (blk >= 0) {
@@ -436,15 +459,14 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
     __shared__ float s_m[kDecWarps * kMaxGroup], s_l[kDecWarps * kMaxGroup];
     __shared__ float s_o[kMaxGroup * D];
 
-    const int b = blockIdx.z, g = blockIdx.x, pidx = blockIdx.y;
+    pdl_trigger();  // the merge kernel may launch once every CTA has started
+    const int b = blockIdx.y, g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = clipped_seqlen(p, b, block_size, pidx == 0 && g == 0 && threadIdx.x == 0);
-    const int start = window_start(L, p.window_left);
-    const int P = p.partition_size;
-    const int part = start / P + pidx;
-    const int tok_lo = max(part * P, start);
-    const int tok_hi = min((part + 1) * P, L);
-    if (tok_lo >= tok_hi) return;
+    int L, pidx, tok_lo, tok_hi;
+    if (!decode_partition(p, b, blockIdx.z, block_size,
+                          blockIdx.z == gridDim.z - 1 && g == 0 && threadIdx.x == 0, L, pidx,
+                          tok_lo, tok_hi))
+        return;
 
     const int G = p.group, Hkv = p.num_kv_heads;
     const int Dh = p.head_dim;  // <= D; dims past it are zero in q and skipped in k, v
@@ -564,6 +586,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_kernel(const DecodeParams p, int D, int block_size) {
     extern __shared__ float s_w[];  // [num_parts] partition weights
     __shared__ float scratch[kMergeThreads / 32];
+    pdl_wait();  // the partition kernel's partials
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = clipped_seqlen(p, b, block_size, false);
     const int start = window_start(L, p.window_left);
@@ -652,6 +675,7 @@ template <typename OutT, int D>
 __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_warp_kernel(const DecodeParams p, int block_size) {
     constexpr int VEC = D / 32;  // columns per lane: 2, 4 or 8
+    pdl_wait();  // the partition kernel's partials
     const int lane = threadIdx.x & 31;
     const int64_t unit = (int64_t)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
     if (unit >= (int64_t)p.batch * p.num_qo_heads) return;
@@ -729,20 +753,20 @@ cudaError_t launch_merge(const DecodeParams &p, int D, int BS, cudaStream_t stre
         (D == 64 || D == 128 || D == 256)) {
         const unsigned blocks = (unsigned)((units + kMergeThreads / 32 - 1) / (kMergeThreads / 32));
         if (D == 64)
-            decode_merge_warp_kernel<OutT, 64><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
-        else if (D == 128)
-            decode_merge_warp_kernel<OutT, 128><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
-        else
-            decode_merge_warp_kernel<OutT, 256><<<blocks, kMergeThreads, 0, stream>>>(p, BS);
-        return cudaGetLastError();
+            return launch_pdl(decode_merge_warp_kernel<OutT, 64>, dim3(blocks),
+                              dim3(kMergeThreads), 0, stream, p, BS);
+        if (D == 128)
+            return launch_pdl(decode_merge_warp_kernel<OutT, 128>, dim3(blocks),
+                              dim3(kMergeThreads), 0, stream, p, BS);
+        return launch_pdl(decode_merge_warp_kernel<OutT, 256>, dim3(blocks), dim3(kMergeThreads),
+                          0, stream, p, BS);
     }
     const int merge_smem = p.num_parts * (int)sizeof(float);
     auto k = decode_merge_kernel<OutT>;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(k), merge_smem);
     if (e != cudaSuccess) return e;
-    dim3 grid2(p.num_qo_heads, p.batch);
-    k<<<grid2, kMergeThreads, merge_smem, stream>>>(p, D, BS);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(p.num_qo_heads, p.batch), dim3(kMergeThreads),
+                      (size_t)merge_smem, stream, p, D, BS);
 }
 
 template <typename K>
@@ -758,7 +782,7 @@ cudaError_t launch_tc(const DecodeParams &p, const CUtensorMap *tk, const CUtens
                       : decode_bf16_tc_kernel<D, BS, NHT, NST, false>;
     cudaError_t e = set_smem(kern, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
+    dim3 grid(p.num_kv_heads, p.batch, p.num_parts);
     kern<<<grid, kDecThreads, C::SMEM, stream>>>(p, *tk, *tv);
     return cudaGetLastError();
 }
@@ -784,7 +808,7 @@ cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
     if (p.group > kMaxGroup || p.partition_size > kMaxPartition) return cudaErrorNotSupported;
     if (D % 16 != 0 || D > 256 || p.head_dim != D) return cudaErrorNotSupported;
     if (cache.dtype == PKV_F32) {
-        dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
+        dim3 grid(p.num_kv_heads, p.batch, p.num_parts);
         if (T == 64)
             decode_f32_kernel<64><<<grid, kDecThreads, 0, stream>>>(p, BS);
         else if (T == 128)

@@ -41,6 +41,7 @@ extern "C" pkv_status pkv_paged_decode_noalloc(
     const int32_t *block_table, int max_blocks_per_seq, const int32_t *cache_seqlens,
     int max_seqlen, const float *sink, int batch, int num_qo_heads, int window_left,
     float sm_scale, int partition_size, float *lse_out, int32_t *dev_error, void *stream) {
+    if (batch == 0) return PKV_OK;  // nothing to do: no device lookup either
     const size_t need = pkv_paged_decode_workspace_size(batch, num_qo_heads, cache.head_dim,
                                                         max_seqlen, partition_size, window_left);
     if (need > PKV_NOALLOC_DECODE_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;

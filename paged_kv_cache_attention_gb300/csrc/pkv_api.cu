@@ -190,11 +190,30 @@ const char *pkv_status_string(int status) {
         case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
         case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
         case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_OUT_OF_RANGE: return "PKV_ERR_OUT_OF_RANGE";
+        case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
         default: return "PKV_ERR_UNKNOWN";
     }
 }
 
-int pkv_version(void) { return 400; }
+int pkv_version(void) { return 500; }
+
+pkv_status pkv_get_device_error(const int32_t *dev_error, int32_t *bits, int clear,
+                                void *stream) {
+    if (!dev_error) return PKV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    if (cudaMemcpyAsync(&word, dev_error, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (bits) *bits = word;
+    if (clear && cudaMemsetAsync(const_cast<int32_t *>(dev_error), 0, sizeof word, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (word & (int32_t)PKV_DEVERR_TIMEOUT) return PKV_ERR_TIMEOUT;
+    const int32_t metadata =
+        (int32_t)(PKV_DEVERR_BLOCK_ID | PKV_DEVERR_SLOT | PKV_DEVERR_SEQLEN | PKV_DEVERR_POSITION);
+    return (word & metadata) ? PKV_ERR_OUT_OF_RANGE : PKV_OK;
+}
 
 pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                  void *v_cache, const int64_t *slot_mapping, int64_t num_tokens,
@@ -222,11 +241,19 @@ pkv_status pkv_reshape_and_cache(const void *key, const void *value, void *k_cac
 }
 
 pkv_status pkv_rope_cos_sin_table(float *cos_sin, int max_position, int rotary_dim,
-                                  double base, double position_scale, void *stream) {
+                                  double base, double position_scale, double ntk_alpha,
+                                  void *stream) {
     if (max_position < 0 || rotary_dim <= 0 || rotary_dim % 2 != 0) return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(base) || base <= 0.0 || !std::isfinite(position_scale) ||
-        position_scale <= 0.0)
+        position_scale <= 0.0 || !std::isfinite(ntk_alpha) || ntk_alpha <= 0.0)
         return PKV_ERR_INVALID_ARG;
+    if (ntk_alpha != 1.0) {
+        // NTK-aware scaling: raise the base so that the lowest frequency,
+        // base^(-(rd - 2) / rd), is divided by ntk_alpha
+        if (rotary_dim <= 2) return PKV_ERR_INVALID_ARG;
+        base *= std::pow(ntk_alpha, (double)rotary_dim / (rotary_dim - 2));
+        if (!std::isfinite(base) || base <= 0.0) return PKV_ERR_INVALID_ARG;
+    }
     if (max_position == 0) return PKV_OK;
     if (!cos_sin || !aligned(cos_sin, 16)) return PKV_ERR_INVALID_ARG;
     return from_cuda(launch_rope_table(cos_sin, max_position, rotary_dim, base, position_scale,
@@ -317,7 +344,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
         !aligned(block_table, 4) || !aligned(cache_seqlens, 4))
         return PKV_ERR_INVALID_ARG;
     const int np = decode_num_parts(max_seqlen, P, window_left);
-    if (np > 65535) return PKV_ERR_UNSUPPORTED;  // grid.y limit
+    if (np > 65535) return PKV_ERR_UNSUPPORTED;  // grid.z limit
     const DecodeLayout lay = decode_layout(batch, num_qo_heads, cache.head_dim, np);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.total)
         return PKV_ERR_WORKSPACE;

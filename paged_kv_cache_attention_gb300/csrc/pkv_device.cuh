@@ -12,9 +12,10 @@
 
 namespace pkv {
 
-// A bounded wait gives up after this many SM clock cycles (~1 s at 2 GHz),
-// records PKV_DEVERR_TIMEOUT and lets the kernel wind down.
-constexpr long long kWaitLimitCycles = 2000000000LL;
+// A bounded wait gives up after this many SM clock cycles (0.2-0.3 s at the
+// GB300's 1.4-2.1 GHz, about 10^4 times the longest wait of a working
+// pipeline), records PKV_DEVERR_TIMEOUT and lets the kernel wind down.
+constexpr long long kWaitLimitCycles = 400000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -22,6 +23,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 
 __device__ __forceinline__ void flag_error(int32_t *dev_error, uint32_t bits) {
     if (dev_error) atomicOr(reinterpret_cast<int *>(dev_error), static_cast<int>(bits));
+}
+
+// Programmatic dependent launch.  A kernel launched with the
+// programmatic-stream-serialization attribute may begin while the kernel
+// before it on the stream is still finishing; pdl_wait() blocks until that
+// kernel has completed and its writes are visible, so it must come before
+// the first read of anything that kernel wrote (without the attribute it
+// returns at once).  pdl_trigger() lets the next such kernel begin launching
+// once every CTA of this one has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -65,17 +79,49 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete.  Returns false (and
 // flags PKV_DEVERR_TIMEOUT) if it does not complete within the limit.
+//
+// abort (may be null) is a word of the launch's own workspace that is zero
+// when the launch starts.  A wait that gives up sets it, and every other wait
+// of the launch that is still pending, in any CTA, then gives up at its next
+// poll: one broken pipeline ends the whole launch within one wait limit
+// instead of one limit per wait.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  int32_t *dev_error) {
+                                                  int32_t *dev_error, int32_t *abort = nullptr) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
+        if (abort && *reinterpret_cast<volatile int32_t *>(abort) != 0) return false;
         if (clock64() - t0 > kWaitLimitCycles) {
             flag_error(dev_error, PKV_DEVERR_TIMEOUT);
+            if (abort) atomicExch(reinterpret_cast<int *>(abort), 1);
             return false;
         }
     }
     return true;
+}
+
+// The same wait taken by a whole warp, with one answer for all of its lanes
+// (each lane polls; the warp goes on only if every lane saw the phase
+// complete), so that the warp never splits at a later warp-wide instruction.
+__device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  int32_t *dev_error, int32_t *abort = nullptr) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, dev_error, abort));
+}
+
+// Named barrier over `nthreads` threads (whole warps) that also ANDs a
+// predicate across them: every participant gets the same answer, so warps
+// that share a barrier agree on whether to go on or wind down.
+__device__ __forceinline__ bool bar_sync_and(uint32_t bar_id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(bar_id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -145,6 +145,25 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, 
                            const CUtensorMap *tmap_q, const CUtensorMap *tmap_k,
                            const CUtensorMap *tmap_v, cudaStream_t stream);
 
+// Launch `kernel` with the programmatic-stream-serialization attribute: it may
+// begin while the previous kernel on the stream finishes and must call
+// pdl_wait() before reading that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

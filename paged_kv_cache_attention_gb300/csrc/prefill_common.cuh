@@ -29,24 +29,56 @@ __device__ __forceinline__ int clip_len(int v, int cap, int32_t *err, bool repor
     return v;
 }
 
-// The item's request lengths, clipped to the declared maxima, to the block
-// table's capacity and, for contiguous K/V, to the rows that exist.
+// Word 1 of the work list's 256-byte header: the attention launch's abort
+// word (mbar_wait_bounded), zeroed by the work-list kernel before each launch.
+__device__ __forceinline__ int32_t *abort_word(const PrefillParams &p) { return p.tiles + 1; }
+
+__device__ __forceinline__ int clip_len64(long long v, int cap, int32_t *err, bool report) {
+    return clip_len(v < 0 ? -1 : (v > cap ? cap + 1 : (int)v), cap, err, report);
+}
+
+// Request r's query rows [q_start, q_start + q_len) of the total_q rows of q,
+// out and lse.  cu_seq_lens_q lives on the device, so its entries are checked
+// here: an offset outside [0, total_q], a negative length, a length above
+// max_seqlen_q or one running past total_q is clipped and flagged
+// (PKV_DEVERR_SEQLEN).  No row outside [0, total_q) is ever read or written.
+__device__ __forceinline__ void q_rows(const PrefillParams &p, int r, int &q_start, int &q_len,
+                                       bool report) {
+    const int a = p.cu_q[r], b = p.cu_q[r + 1];
+    int s = a;
+    if (s < 0 || s > p.total_q) {
+        if (report) flag_error(p.dev_error, PKV_DEVERR_SEQLEN);
+        s = s < 0 ? 0 : p.total_q;
+    }
+    int len = clip_len64((long long)b - a, p.max_seqlen_q, p.dev_error, report);
+    if (len > p.total_q - s) {
+        if (report) flag_error(p.dev_error, PKV_DEVERR_SEQLEN);
+        len = p.total_q - s;
+    }
+    q_start = s;
+    q_len = len;
+}
+
+// The item's request lengths, clipped to the declared maxima, to the rows of
+// q, to the block table's capacity and, for contiguous K/V, to the rows that
+// exist.
 __device__ __forceinline__ Geo item_geo(const PrefillParams &p, int4 item, int block_size,
                                         bool contiguous, bool report) {
     Geo G;
     G.r = item.x;
     G.t0 = item.y;
     G.g = item.z;
-    G.q_start = p.cu_q[G.r];
-    G.q_len = clip_len(p.cu_q[G.r + 1] - G.q_start, p.max_seqlen_q, p.dev_error, report);
+    q_rows(p, G.r, G.q_start, G.q_len, report);
     int cap_k = p.max_seqlen_k;
     const long long cap_blocks = (long long)p.max_blocks_per_seq * block_size;
     if (cap_blocks < cap_k) cap_k = (int)cap_blocks;
     if (contiguous) {  // request r's key rows must lie inside the arrays
-        const int room = p.total_k - p.cu_k[G.r];
-        if (room < cap_k) cap_k = max(room, 0);
+        const int k0 = p.cu_k[G.r];
+        const long long room = k0 < 0 ? 0 : (long long)p.total_k - k0;
+        if (k0 < 0 && report) flag_error(p.dev_error, PKV_DEVERR_SEQLEN);
+        if (room < cap_k) cap_k = room > 0 ? (int)room : 0;
     }
-    G.kv_len = clip_len(p.cu_k[G.r + 1] - p.cu_k[G.r], cap_k, p.dev_error, report);
+    G.kv_len = clip_len64((long long)p.cu_k[G.r + 1] - p.cu_k[G.r], cap_k, p.dev_error, report);
     return G;
 }
 

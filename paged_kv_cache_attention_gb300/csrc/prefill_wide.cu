@@ -59,7 +59,8 @@ struct WideLayout {
     static constexpr int B_PFULL = B_SFULL + 2;
     static constexpr int B_ODONE = B_PFULL + 2;
     static constexpr int B_OFREE = B_ODONE + 2;
-    static constexpr int NBARS = B_OFREE + 1;
+    static constexpr int B_DRAIN = B_OFREE + 1;  // the MMAs in flight, after a failed wait
+    static constexpr int NBARS = B_DRAIN + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     // row-max exchange [2 (tile parity)][128][2] and row-sum exchange
     // [2 (query tile)][128][2] between the two warps of a row
@@ -98,6 +99,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
     using Lay = WideLayout;
     constexpr int NPG = kTileN / BS;  // pages per key tile
 
+    pdl_wait();  // the work list
     if ((int)blockIdx.x >= p.tiles[0]) return;  // beyond the work list
     const int4 item = reinterpret_cast<const int4 *>(p.tiles + 64)[blockIdx.x];
 
@@ -111,6 +113,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const pf::Geo geo = pf::item_geo(p, item, BS, CONTIG, threadIdx.x == 0);
+    int32_t *const abort = pf::abort_word(p);
     const TileRange tr[2] = {tile_range(p, geo, 0), tile_range(p, geo, 1)};
     const int G = p.group;
     const int TPR = p.rows_per_head;
@@ -146,6 +149,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
         const int npages_kv = (geo.kv_len + BS - 1) / BS;
         bool alive = true;
         int kv_t = 0, q_loads = 0;
+        int nk = 0, nv = 0;  // key / value tiles whose loads were issued
         if (lane == 0) {
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
@@ -155,7 +159,8 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
             const TileRange t = tr[x];
             if (t.n == 0) continue;
             if (q_loads > 0)  // the previous tile's S products have read Q
-                alive = mbar_wait_bounded(bar(Lay::B_QEMPTY), (q_loads - 1) & 1, p.dev_error);
+                alive = warp_wait_bounded(bar(Lay::B_QEMPTY), (q_loads - 1) & 1, p.dev_error,
+                                          abort);
             if (!alive) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(Lay::B_Q), Lay::Q_BYTES);
@@ -188,7 +193,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 int row = __shfl_sync(0xffffffffu, ids_row,
                                       ((rel & 31) + min(lane >> 2, NPG - 1)) & 31);
                 if constexpr (CONTIG) row = p.cu_k[geo.r] + key0;  // rows past kv_len are masked
-                alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error);
+                alive = warp_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error, abort);
                 if (!alive) break;
                 if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_KFULL + s), Lay::T_BYTES);
                 __syncwarp();
@@ -197,7 +202,8 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                     tma_load_3d(sK + s * Lay::T_BYTES + c * Lay::T_CHUNK + pg * BS * 128, &tmk,
                                 bar(Lay::B_KFULL + s), c * 64, cy, row);
                 }
-                alive = mbar_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error);
+                ++nk;
+                alive = warp_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error, abort);
                 if (!alive) break;
                 if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_VFULL + s), Lay::T_BYTES);
                 __syncwarp();
@@ -206,10 +212,11 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                     tma_load_3d(sV + s * Lay::T_BYTES + c * Lay::T_CHUNK + pg * BS * 128, &tmv,
                                 bar(Lay::B_VFULL + s), c * 64, cy, row);
                 }
+                ++nv;
                 if (is_tail(t, j)) {
                     // value rows at or past kv_len may hold any bits: zero them
                     // so that P = 0 never meets a non-finite value
-                    alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
+                    alive = warp_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error, abort);
                     if (!alive) break;
                     const int first = max(geo.kv_len - key0, 0);
                     const uint32_t vb = sV + s * Lay::T_BYTES;
@@ -226,11 +233,20 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
         // let the MMA issuer's last arrivals land before the CTA can exit
         for (int k = max(0, kv_t - 2); k < kv_t && alive; ++k) {
             const uint32_t ph = (k >> 1) & 1;
-            alive = mbar_wait_bounded(bar(Lay::B_KEMPTY + (k & 1)), ph, p.dev_error) &&
-                    mbar_wait_bounded(bar(Lay::B_VEMPTY + (k & 1)), ph, p.dev_error);
+            alive = warp_wait_bounded(bar(Lay::B_KEMPTY + (k & 1)), ph, p.dev_error, abort) &&
+                    warp_wait_bounded(bar(Lay::B_VEMPTY + (k & 1)), ph, p.dev_error, abort);
         }
         if (alive && q_loads > 0)
-            mbar_wait_bounded(bar(Lay::B_QEMPTY), (q_loads - 1) & 1, p.dev_error);
+            warp_wait_bounded(bar(Lay::B_QEMPTY), (q_loads - 1) & 1, p.dev_error, abort);
+        if (!alive) {
+            // a wait gave up: let this warp's copies still in flight land
+            // (bounded) before the CTA's shared memory is released
+            if (q_loads > 0) warp_wait_bounded(bar(Lay::B_Q), (q_loads - 1) & 1, p.dev_error);
+            for (int t = max(0, nk - 2); t < nk; ++t)
+                warp_wait_bounded(bar(Lay::B_KFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
+            for (int t = max(0, nv - 2); t < nv; ++t)
+                warp_wait_bounded(bar(Lay::B_VFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -254,7 +270,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
             for (int x = 0; x < pf::kItemTiles && alive; ++x) {
                 const TileRange t = tr[x];
                 if (t.n == 0) continue;
-                alive = mbar_wait_bounded(bar(Lay::B_Q), q_waits & 1, p.dev_error);
+                alive = mbar_wait_bounded(bar(Lay::B_Q), q_waits & 1, p.dev_error, abort);
                 ++q_waits;
                 if (!alive) break;
                 tc::fence_after_sync();
@@ -262,7 +278,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 for (int jj = 0; jj < 2 && jj < t.n && alive; ++jj) {
                     const int tt = base + jj;
                     alive = mbar_wait_bounded(bar(Lay::B_KFULL + (tt & 1)), (tt >> 1) & 1,
-                                              p.dev_error);
+                                              p.dev_error, abort);
                     if (!alive) break;
                     tc::fence_after_sync();
                     issue_s(jj & 1, tt & 1);
@@ -272,19 +288,22 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 for (int j = 0; j < t.n && alive; ++j) {
                     const int tt = base + j, s = tt & 1, b = j & 1;
                     const uint32_t ph = (tt >> 1) & 1;
-                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + b), pu[b] & 1, p.dev_error);
+                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + b), pu[b] & 1, p.dev_error,
+                                              abort);
                     ++pu[b];
                     if (!alive) break;
                     if (is_tail(t, j)) {
                         alive = mbar_wait_bounded(bar(Lay::B_VFIX + s), vfix_cnt[s] & 1,
-                                                  p.dev_error);
+                                                  p.dev_error, abort);
                         ++vfix_cnt[s];
                     } else {
-                        alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
+                        alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error,
+                                                  abort);
                     }
                     if (!alive) break;
                     if (j == 0 && pv_cnt > 0) {  // the previous tile's epilogue has read O
-                        alive = mbar_wait_bounded(bar(Lay::B_OFREE), ofree_waits & 1, p.dev_error);
+                        alive = mbar_wait_bounded(bar(Lay::B_OFREE), ofree_waits & 1,
+                                                  p.dev_error, abort);
                         ++ofree_waits;
                         if (!alive) break;
                     }
@@ -302,12 +321,12 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                     if (j + 2 < t.n) {
                         const int t2 = base + j + 2;
                         alive = mbar_wait_bounded(bar(Lay::B_KFULL + (t2 & 1)), (t2 >> 1) & 1,
-                                                  p.dev_error);
+                                                  p.dev_error, abort);
                         if (!alive) break;
                         // P(j) lives where S(j+2) goes: PV(j) must be done
                         const int k = pv_cnt - 1;
                         alive = mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
-                                                  p.dev_error);
+                                                  p.dev_error, abort);
                         if (!alive) break;
                         tc::fence_after_sync();
                         issue_s(b, t2 & 1);
@@ -316,6 +335,12 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                     }
                 }
                 kv_t += t.n;
+            }
+            if (!alive) {
+                // a wait gave up: let the MMAs already issued finish (bounded)
+                // before tensor memory is released
+                tc::commit(bar(Lay::B_DRAIN));
+                mbar_wait_bounded(bar(Lay::B_DRAIN), 0, p.dev_error);
             }
         }
     } else {
@@ -338,7 +363,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
         const int wl = p.window_left;
         const float al2 = ALIBI ? p.alibi[head] * kLog2e : 0.f;
         const float sink_l2 = p.sink ? p.sink[head] * kLog2e : kNegInf;
-        bool alive = true;
+        bool alive = true, o_ok = true;
         int pv_base = 0, jg = 0;
         int su[2] = {0, 0};
         for (int x = 0; x < pf::kItemTiles; ++x) {
@@ -351,10 +376,11 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
             float m_run = kNegInf, l_run = 0.f;
             for (int j = 0; j < t.n && alive; ++j, ++jg) {
                 const int b = j & 1;
-                alive = __all_sync(0xffffffffu, mbar_wait_bounded(bar(Lay::B_SFULL + b),
-                                                                   su[b] & 1, p.dev_error));
+                // a warp whose wait gave up still meets its partner at the pair
+                // barrier below, and both leave together
+                const bool s_ok = o_ok && warp_wait_bounded(bar(Lay::B_SFULL + b), su[b] & 1,
+                                                            p.dev_error, abort);
                 ++su[b];
-                if (!alive) break;
                 tc::fence_after_sync();
                 const int key0 = (t.kt_lo + tile_of(t.n, j)) * kTileN + hc * 32;
                 const bool full = (key0 + 31 <= cpos) && (key0 + 32 <= geo.kv_len) &&
@@ -362,8 +388,13 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 const int khi = min(cpos, geo.kv_len - 1) - key0;
                 const int klo = wl < 0 ? -1 : qpos - wl - key0;
                 uint32_t ra[32];
-                tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 32, ra);
-                tc::wait_ld();
+                if (s_ok) {
+                    tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 32, ra);
+                    tc::wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ra[i] = __float_as_uint(kNegInf);
+                }
                 if (!full) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -397,7 +428,8 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 const float mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
                 float *slot = xmax + ((jg & 1) * 128 + row) * 2;
                 slot[hc] = mine;
-                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                alive = bar_sync_and(pair_bar, 64, s_ok);
+                if (!alive) break;
                 const float mx = fmaxf(mine, slot[hc ^ 1]);
                 const float m_tile = ALIBI ? mx : mx * sl2;
                 const bool grow = m_tile > m_run + (ALIBI ? 0.f : kRescaleThreshold);
@@ -405,12 +437,13 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                     const float alpha = grow ? fast_exp2(m_run - m_tile) : 1.f;
                     l_run *= alpha;
                     if (j > 0) {
-                        // O is written by PV(j-1): wait for it before rescaling
+                        // O is written by PV(j-1): wait for it before rescaling (a
+                        // wait that gives up is reported at the next pair barrier)
                         const int k = pv_base + j - 1;
-                        alive = __all_sync(0xffffffffu,
-                                           mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)),
-                                                             (k >> 1) & 1, p.dev_error));
-                        if (!alive) break;
+                        o_ok = warp_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
+                                                 p.dev_error, abort);
+                    }
+                    if (j > 0 && o_ok) {
                         tc::fence_after_sync();
                         const uint32_t tO = tmem + lane_off + Lay::O_COL + hc * 128;
 #pragma unroll
@@ -456,9 +489,8 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
             if (have_o) {
                 // the last PV's commit covers every earlier MMA
                 const int k = pv_base + t.n - 1;
-                have_o = __all_sync(0xffffffffu,
-                                    mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
-                                                      p.dev_error));
+                have_o = warp_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
+                                           p.dev_error, abort);
                 tc::fence_after_sync();
             }
             float *lslot = xl + (x * 128 + row) * 2;
@@ -536,9 +568,8 @@ cudaError_t launch_prefill_wide(const PrefillParams &p, const pkv_cache_desc &ca
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = set_smem_wide(kern, WideLayout::SMEM);
         if (e != cudaSuccess) return e;
-        kern<<<grid, WideLayout::THREADS, WideLayout::SMEM, stream>>>(p, *tmap_q, *tmap_k,
-                                                                      *tmap_v);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3(grid), dim3(WideLayout::THREADS), WideLayout::SMEM, stream,
+                          p, *tmap_q, *tmap_k, *tmap_v);
     };
     auto paged = [&](auto alibi_tag) -> cudaError_t {
         constexpr bool AL = decltype(alibi_tag)::value;

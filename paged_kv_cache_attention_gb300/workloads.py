@@ -299,12 +299,13 @@ class RopeCase:
     position_scale: float
     neox: bool
     max_position: int
+    ntk_alpha: float = 1.0        # NTK-aware context stretch of the rotary base (1: none)
 
 
 def make_rope(num_tokens: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
               rotary_dim: int, block_size: int, dtype, seed: int, max_position: int = 8192,
               base: float = 10000.0, position_scale: float = 1.0, neox: bool = True,
-              skip_every: int = 7, name: str = "rope") -> RopeCase:
+              skip_every: int = 7, name: str = "rope", ntk_alpha: float = 1.0) -> RopeCase:
     """num_tokens tokens at uniform positions in [0, max_position) (the first
     two at 0 and max_position - 1), written to distinct random slots of a NaN
     pool with a quarter of spare room; every skip_every-th token has slot -1."""
@@ -326,7 +327,7 @@ def make_rope(num_tokens: int, num_qo_heads: int, num_kv_heads: int, head_dim: i
     kc = torch.full(shape, float("nan"), dtype=dtype)
     vc = torch.full(shape, float("nan"), dtype=dtype)
     return RopeCase(name, q, k, v, kc, vc, pos, slots, int(rotary_dim), float(base),
-                    float(position_scale), bool(neox), int(max_position))
+                    float(position_scale), bool(neox), int(max_position), float(ntk_alpha))
 
 
 def make_long_sequence(seq_len: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,

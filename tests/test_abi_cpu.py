@@ -43,6 +43,8 @@ def test_status_strings_and_version():
     assert lib.pkv_version() >= 100
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
+    assert lib.pkv_status_string(5) == b"PKV_ERR_OUT_OF_RANGE"
+    assert lib.pkv_status_string(6) == b"PKV_ERR_TIMEOUT"
     assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
 
 
@@ -205,18 +207,19 @@ def test_rope_reshape_and_cache_validation(change, expected):
 @nogpu
 def test_rope_table_validation():
     f = pkv.load_library().pkv_rope_cos_sin_table
-    assert f(FAKE, 0, 64, 10000.0, 1.0, None) == 0       # nothing to fill
-    assert f(FAKE, 10, 63, 10000.0, 1.0, None) == 1      # odd rotary_dim
-    assert f(FAKE, 10, 64, -1.0, 1.0, None) == 1         # base must be positive
-    assert f(FAKE, 10, 64, 10000.0, 0.0, None) == 1      # scale must be positive
-    assert f(None, 10, 64, 10000.0, 1.0, None) == 1
+    assert f(FAKE, 0, 64, 10000.0, 1.0, 1.0, None) == 0       # nothing to fill
+    assert f(FAKE, 10, 63, 10000.0, 1.0, 1.0, None) == 1      # odd rotary_dim
+    assert f(FAKE, 10, 64, -1.0, 1.0, 1.0, None) == 1         # base must be positive
+    assert f(FAKE, 10, 64, 10000.0, 0.0, 1.0, None) == 1      # scale must be positive
+    assert f(FAKE, 10, 64, 10000.0, 1.0, 0.0, None) == 1      # ntk_alpha must be positive
+    assert f(FAKE, 10, 2, 10000.0, 1.0, 2.0, None) == 1       # NTK needs rotary_dim > 2
+    assert f(FAKE, 0, 2, 10000.0, 1.0, 1.0, None) == 0        # rotary_dim 2 without NTK
+    assert f(None, 10, 64, 10000.0, 1.0, 1.0, None) == 1
 
 
-def test_ntk_scaled_base():
-    assert pkv.ntk_scaled_base(10000.0, 128, 1.0) == 10000.0
-    # the lowest frequency base^(-(rd-2)/rd) is divided by exactly alpha
-    b = pkv.ntk_scaled_base(10000.0, 128, 4.0)
-    assert abs(b ** (-126 / 128) * 4.0 - 10000.0 ** (-126 / 128)) < 1e-15
+@nogpu
+def test_get_device_error_validation():
+    assert pkv.load_library().pkv_get_device_error(None, None, 0, None) == 1
 
 
 # ---------------------------------------------------------------------------

@@ -189,11 +189,13 @@ def test_varlen_prefill_contiguous(lib):
 
 
 def test_rope(lib, monkeypatch):
-    tab = pkv.rope_cos_sin_table(33, 32, base=5e5, position_scale=4.0, device="cpu")
+    tab = pkv.rope_cos_sin_table(33, 32, base=5e5, position_scale=4.0, ntk_alpha=2.5,
+                                 device="cpu")
     a = lib.last("pkv_rope_cos_sin_table")
     assert tuple(tab.shape) == (33, 16, 2)
     assert a["cos_sin"] == tab.data_ptr() and a["max_position"] == 33
     assert (a["rotary_dim"], a["base"], a["position_scale"]) == (32, 5e5, 4.0)
+    assert a["ntk_alpha"] == 2.5 and a["stream"] == STREAM
     kc, vc = _pools()
     query = torch.zeros(6, 4, 64, dtype=BF16)
     key, value = torch.zeros(6, 2, 64, dtype=BF16), torch.zeros(6, 2, 64, dtype=BF16)
@@ -235,9 +237,18 @@ def test_minference_prefill(lib):
     assert list(size.values()) == [300, 8, 2, 40, 90, 0.0, 3, 5]
 
 
+def test_get_device_error(lib, monkeypatch):
+    err = torch.zeros(1, dtype=I32)
+    assert pkv.get_device_error(err, clear=True) == 0
+    a = lib.last("pkv_get_device_error")
+    assert a["dev_error"] == err.data_ptr() and a["clear"] == 1 and a["stream"] == STREAM
+    assert isinstance(a["bits"], int) and a["bits"] != 0  # a host int32 the call fills
+
+
 def test_every_wrapped_entry_point_is_covered_here():
     src = open(os.path.abspath(__file__)).read()
     for name in ("pkv_reshape_and_cache", "pkv_paged_decode", "pkv_paged_decode_noalloc",
                  "pkv_varlen_prefill", "pkv_varlen_prefill_contiguous", "pkv_rope_cos_sin_table",
-                 "pkv_rope_reshape_and_cache", "pkv_minference_prefill"):
+                 "pkv_rope_reshape_and_cache", "pkv_minference_prefill",
+                 "pkv_get_device_error"):
         assert f'lib.last("{name}")' in src

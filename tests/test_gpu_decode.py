@@ -3,6 +3,8 @@
 Bars: max-abs error 1e-5 (fp32) / 2e-2 (bf16) on outputs; lse within 1e-5 /
 2e-3.  Pool pages no sequence owns hold NaN, so a stray read fails the test.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -151,6 +153,31 @@ def test_bad_block_id_is_flagged_not_read():
     assert max_abs(got[:1], ref) <= TOL[torch.bfloat16]
 
 
+def test_device_error_status_through_the_abi():
+    """pkv_get_device_error turns the word the kernels OR their checks into
+    into a status: an out-of-pool block id gives PKV_ERR_OUT_OF_RANGE with
+    the block-id bit, and the clear flag resets the word."""
+    case = W.make_decode([64, 64], 8, 2, 64, 16, torch.bfloat16, seed=12)
+    case.block_table[1, 2] = case.k_cache.shape[0] + 5  # outside the pool
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    gpu_decode(case, err=err)
+    lib = pkv.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    bits = ctypes.c_int32(0)
+    st = lib.pkv_get_device_error(err.data_ptr(), ctypes.addressof(bits), 1, stream)
+    assert lib.pkv_status_string(st) == b"PKV_ERR_OUT_OF_RANGE"
+    assert bits.value & pkv.DEVERR_BLOCK_ID and not bits.value & pkv.DEVERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0  # cleared on the stream
+    assert lib.pkv_get_device_error(err.data_ptr(), None, 0, stream) == 0
+    # the binding: bits back, or an exception on request
+    gpu_decode(case, err=err)
+    assert pkv.get_device_error(err) & pkv.DEVERR_BLOCK_ID
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.get_device_error(err, raise_on_error=True)
+    assert e.value.status_name == "PKV_ERR_OUT_OF_RANGE"
+
+
 def test_seqlen_above_declared_max_is_flagged():
     case = W.make_decode([100, 40], 8, 2, 64, 16, torch.bfloat16, seed=13)
     err = torch.zeros(1, dtype=torch.int32, device=dev())
@@ -172,19 +199,19 @@ def test_config2_decode_full():
 
 @pytest.mark.parametrize("layer", [0, 1])
 def test_config3_long_context(layer):
-    """Long-context split-KV decode: layer 0 (window 127) checked on every
-    sequence, layer 1 (full 32K-128K context) on two sampled sequences."""
+    """Long-context split-KV decode, every sequence of both layers against the
+    oracle: layer 0 (window 127) and layer 1 (full 32K-128K context, up to
+    256 partitions merged per head), outputs and lse."""
     case = W.config3_long(layer)
-    got = gpu_decode(case)
-    rows = None if layer == 0 else [0, 5]
-    ref = oracle_decode(case, rows=rows)
-    sel = got if rows is None else got[rows]
-    assert max_abs(sel, ref) <= TOL[torch.bfloat16]
+    got, glse = gpu_decode(case, with_lse=True)
+    ref, rlse = oracle_decode(case, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.bfloat16]
 
 
 def test_config5_decode_half_after_cache_write():
     """The decode half of the mixed step: write the new tokens, then attend
-    over cache length + 1 (sampled sequences)."""
+    over cache length + 1; all 256 sequences against the oracle."""
     case = W.config5_mixed()
     d = dev()
     kc, vc = case.k_cache.to(d), case.v_cache.to(d)
@@ -192,10 +219,10 @@ def test_config5_decode_half_after_cache_write():
     torch.cuda.synchronize()
     dec = case.decode
     dec.k_cache, dec.v_cache = kc.cpu(), vc.cpu()
-    got = gpu_decode(dec)
-    rows = list(range(0, 256, 17))
-    ref = oracle_decode(dec, rows=rows)
-    assert max_abs(got[rows], ref) <= TOL[torch.bfloat16]
+    got, glse = gpu_decode(dec, with_lse=True)
+    ref, rlse = oracle_decode(dec, with_lse=True)
+    assert max_abs(got, ref) <= TOL[torch.bfloat16]
+    assert lse_err(glse, rlse) <= LSE_TOL[torch.bfloat16]
 
 
 # ---------------------------------------------------------------------------

@@ -350,6 +350,35 @@ def test_bad_block_id_is_flagged():
     assert max_abs(got[:40], ref) <= TOL[BF16]
 
 
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("cu_q", [[0, 40, 80], [0, 70, 80], [0, 50, 30]])
+def test_query_offsets_past_total_q_are_clipped_and_flagged(D, cu_q):
+    """cu_seq_lens_q lives on the device: offsets past total_q (the rows of q
+    the caller declared), a request running past them, or a decreasing pair
+    must be clipped to the declared rows and flagged, and nothing past the
+    output and lse rows may be written (sentinel tail)."""
+    Hq, Hkv, T = 8, 2, 60
+    case = W.make_varlen([40, 40], [100, 100], Hq, Hkv, D, 16, BF16, seed=27)
+    d = dev()
+    q_full = case.q.to(d)                  # 80 rows; the call sees the first 60
+    out_buf = torch.full((80, Hq, D), 7.0, dtype=BF16, device=d)
+    lse_buf = torch.full((80, Hq), 7.0, dtype=torch.float32, device=d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    cuq = torch.tensor(cu_q, dtype=torch.int32, device=d)
+    pkv.varlen_prefill(q_full[:T], case.k_cache.to(d), case.v_cache.to(d),
+                       case.block_table.to(d), cuq, case.cu_seq_lens_k.to(d), 80,
+                       case.max_seqlen_k, sm_scale=case.sm_scale, out=out_buf[:T],
+                       lse=lse_buf[:T], dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.DEVERR_SEQLEN
+    assert torch.all(out_buf[T:] == 7.0) and torch.all(lse_buf[T:] == 7.0)
+    got = out_buf[:T].float().cpu().numpy()
+    assert np.isfinite(got).all()
+    if cu_q[1] == 40:  # request 0 is intact: its rows match the oracle
+        ref = oracle_prefill(case, rows=list(range(40)))
+        assert max_abs(got[:40], ref) <= TOL[BF16]
+
+
 def _sample_rows(case, n_per_req=4):
     rows = []
     cu = case.cu_seq_lens_q.tolist()
@@ -360,23 +389,36 @@ def _sample_rows(case, n_per_req=4):
     return rows
 
 
-def test_config4_prefill_full_size_sampled():
+def _every_nth_row(case, n):
+    """Every n-th query row of the batch, plus each request's first and last
+    row (the rows at the ends of the causal ranges)."""
+    rows = set(range(0, case.total_q, n))
+    cu = case.cu_seq_lens_q.tolist()
+    for r in range(case.batch):
+        if cu[r + 1] > cu[r]:
+            rows |= {cu[r], cu[r + 1] - 1}
+    return sorted(rows)
+
+
+def test_config4_prefill_full_size():
+    """The B16 varlen batch at full size: every query row of every request
+    (16 requests, prefixes up to 8K keys) against the oracle, with lse."""
     case = W.config4_prefill()
-    _check(case, rows=_sample_rows(case))
+    _check(case)
 
 
-def test_config4_prefill_alibi_full_size_sampled():
+def test_config4_prefill_alibi_full_size():
     # the B16 batch with geometric slopes: prefixes up to ~10K keys, so the
     # per-tile ALiBi constant slope * (tile start - position) reaches its
-    # largest magnitudes; sampled rows of every request
+    # largest magnitudes; every fourth row and each request's ends
     case = W.config4_prefill()
     case.alibi = W.alibi_slopes("geometric", case.q.shape[1], None)
-    _check(case, rows=_sample_rows(case))
+    _check(case, rows=_every_nth_row(case, 4))
 
 
-def test_config4_prefill_head_size_256_full_size_sampled():
+def test_config4_prefill_head_size_256_full_size():
     case = W.config4_prefill(16, 8, 256)
-    _check(case, rows=_sample_rows(case, 3))
+    _check(case, rows=_every_nth_row(case, 4))
 
 
 def test_config5_prefill_half_after_cache_write():
@@ -387,7 +429,7 @@ def test_config5_prefill_half_after_cache_write():
     torch.cuda.synchronize()
     pre = case.prefill
     pre.k_cache, pre.v_cache = kc.cpu(), vc.cpu()
-    _check(pre, rows=_sample_rows(pre, 3), lse=False)
+    _check(pre)  # all 8192 query rows, with lse
 
 
 def test_many_requests_work_list():

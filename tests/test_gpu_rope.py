@@ -30,7 +30,7 @@ def _run(case, err=None):
     q, k, v = case.query.to(d), case.key.to(d), case.value.to(d)
     kc, vc = case.k_cache.to(d), case.v_cache.to(d)
     tab = pkv.rope_cos_sin_table(case.max_position, case.rotary_dim, case.base,
-                                 case.position_scale)
+                                 case.position_scale, ntk_alpha=case.ntk_alpha)
     pkv.rope_reshape_and_cache(q, k, v, kc, vc, case.positions.to(d), case.slot_mapping.to(d),
                                tab, case.rotary_dim, case.neox, dev_error=err)
     torch.cuda.synchronize()
@@ -39,7 +39,8 @@ def _run(case, err=None):
 
 def _oracle_rot(case, x):
     return oracle.rope(W.to_oracle(x), case.positions.numpy(), case.rotary_dim, base=case.base,
-                       position_scale=case.position_scale, neox=case.neox)
+                       position_scale=case.position_scale, neox=case.neox,
+                       ntk_alpha=case.ntk_alpha)
 
 
 def _assert_rotated(case, got, x, ref):
@@ -90,14 +91,16 @@ def test_rope_cache_matches_oracle(dtype, neox, Hq, Hkv, D, rd):
     _check_case(case)
 
 
-@pytest.mark.parametrize("base,scale,max_pos", [(10000.0, 1.0, 131072), (500000.0, 8.0, 32768),
-                                                (pkv.ntk_scaled_base(10000.0, 128, 4.0), 1.0,
-                                                 16384)])
-def test_rope_long_positions_and_scaling(base, scale, max_pos):
+@pytest.mark.parametrize("base,scale,ntk,max_pos", [(10000.0, 1.0, 1.0, 131072),
+                                                    (500000.0, 8.0, 1.0, 32768),
+                                                    (10000.0, 1.0, 4.0, 16384),
+                                                    (10000.0, 2.0, 2.5, 65536)])
+def test_rope_long_positions_and_scaling(base, scale, ntk, max_pos):
     """Angles up to ~1.3e5 rad: the fp64-built table keeps the rotation exact
-    to fp32 rounding even there."""
-    case = W.make_rope(512, 8, 2, 128, 128, 32, torch.bfloat16, seed=int(scale) + 7,
-                       max_position=max_pos, base=base, position_scale=scale)
+    to fp32 rounding even there; linear and NTK-aware scaling (the table's
+    ntk_alpha against the oracle's own NTK base) included."""
+    case = W.make_rope(512, 8, 2, 128, 128, 32, torch.bfloat16, seed=int(scale + ntk) + 7,
+                       max_position=max_pos, base=base, position_scale=scale, ntk_alpha=ntk)
     _check_case(case)
 
 

@@ -7,8 +7,9 @@ fixed 32 MiB device array inside the library instead of a caller workspace.
 This file is collected last, so a run that stops at its first failure has
 already run every other test.  It checks, through the C ABI, that two calls
 in a row (the second one reusing the array the first one left behind) match
-the workspace entry point within the suite's tolerances, and that a problem
-needing more scratch than the array holds is rejected before any launch.
+the workspace entry point (the same kernels with the same arithmetic, so the
+outputs must be bit-identical), and that a problem needing more scratch than
+the array holds is rejected before any launch.
 """
 import ctypes
 
@@ -78,8 +79,9 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls_in_a_row():
         assert int(err.item()) == 0
         o, r = out.float().cpu().numpy(), ref.float().cpu().numpy()
         assert np.isfinite(o).all()
-        assert np.abs(o - r).max() <= TOL[case.q.dtype]
-        np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=0, atol=1e-5)
+        assert np.abs(o - r).max() <= TOL[case.q.dtype]  # the suite's bar ...
+        assert torch.equal(out, ref)                      # ... and in fact bit-identical
+        assert torch.equal(lse, ref_lse)
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
@@ -122,4 +124,4 @@ def test_binding_noalloc_matches_paged_decode():
     o, r = out.float().cpu().numpy(), ref.float().cpu().numpy()
     assert np.isfinite(o).all()
     assert np.abs(o - r).max() <= TOL[case.q.dtype]
-    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=0, atol=1e-5)
+    assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
