@@ -245,6 +245,39 @@ def sparse_kept_pairs(seq_len, vertical, slash):
     return total
 
 
+def sparse_tile_fraction(seq_len, vertical, slash, num_kv_heads, rows=128, keys=128,
+                         tiles_per_item=2):
+    """(key tiles the sparse prefill must process, key tiles of dense causal
+    attention) at the kernel's granularity: one work item takes
+    tiles_per_item * rows / G query tokens of the G query heads of a kv head,
+    and a 128-key tile is needed iff it holds a kept (query, key) pair for
+    one of them: a kept column in the tile, or a kept diagonal between the
+    item's and the tile's positions."""
+    S = int(seq_len)
+    Hq = vertical.shape[0]
+    G = Hq // num_kv_heads
+    tok = tiles_per_item * rows // G
+    nkt = (S + keys - 1) // keys
+    need = dense = 0
+    for g in range(num_kv_heads):
+        vb = np.zeros(nkt * keys, bool)
+        sb = np.zeros(S, bool)
+        for h in range(g * G, (g + 1) * G):
+            vb[np.asarray(vertical[h])] = True
+            sb[np.asarray(slash[h])] = True
+        vcol = vb.reshape(nkt, keys).any(axis=1)
+        scum = np.concatenate([[0], np.cumsum(sb)])
+        for p0 in range(0, S, tok):
+            p1 = min(p0 + tok, S) - 1
+            nk = p1 // keys + 1
+            k0 = np.arange(nk) * keys
+            k1 = np.minimum(k0 + keys - 1, p1)
+            anys = (scum[p1 - k0 + 1] - scum[np.maximum(p0 - k1, 0)]) > 0
+            need += int((vcol[:nk] | anys).sum())
+            dense += nk
+    return need, dense
+
+
 def time_flushed(fn, K, flush):
     """Mean device time of fn over K launches, each timed alone with CUDA
     events after a write of a buffer larger than L2 (so no launch reads what
@@ -665,12 +698,14 @@ def extra_configs(dev, K, peaks):
                                                                   out=outm),
                             max(3, K // 10), flush)
     kept = sparse_kept_pairs(S, vim.cpu().numpy(), sim.cpu().numpy())
+    t_need, t_dense = sparse_tile_fraction(S, vim.cpu().numpy(), sim.cpu().numpy(), 8)
     fl_kept = 4 * 128 * kept  # per kept (query, key) pair of a head: QK^T and PV
     fl_dense = 4 * 128 * 32 * (S * (S + 1) // 2)
     out["minference_prefill_S32K_Hq32_D128"] = {
         "ms": round(ms_sparse, 4), "dense_ms": round(ms_dense, 4),
         "speedup_vs_dense": round(ms_dense / ms_sparse, 3),
         "kept_pair_fraction": round(kept / (32 * S * (S + 1) // 2), 4),
+        "key_tiles_needed_fraction": round(t_need / t_dense, 4),
         "TFLOP/s_on_kept_pairs": round(fl_kept / (ms_sparse * 1e-3) / 1e12, 1),
         "dense_TFLOP/s": round(fl_dense / (ms_dense * 1e-3) / 1e12, 1),
         "l2": "256 MB buffer written before each timed launch"}

@@ -65,14 +65,12 @@ __device__ __forceinline__ int window_start(int L, int window_left) {
     return s > 0 ? s : 0;
 }
 
-// The partition a CTA of the partition grid (x = kv head, y = sequence,
-// z = slot) takes, and its token range [tok_lo, tok_hi).  Sequence b has
-// n_b partitions (absolute P-aligned blocks meeting [start, L)); slot z takes
-// partition pidx = n_b - gridDim.z + z, so the last slot of every sequence
-// holds its last partition -- the partial one -- and those are launched last
-// (the block scheduler dispatches in grid order): the tail of the launch is
-// short partitions, and the slots a short sequence does not use are at the
-// front, where their CTAs exit at once.  Returns false for an unused slot.
+// The partition a CTA of the partition grid (x = kv head, y = partition
+// slot, z = sequence) takes, and its token range [tok_lo, tok_hi).  Sequence
+// b has n_b partitions (absolute P-aligned blocks meeting [start, L)); slot z
+// takes the z-th of them.  (Measured on GB300: this sequence-major order beat
+// a partition-major order and one that launched every sequence's partial
+// last partition at the end.)  Returns false for an unused slot.
 __device__ __forceinline__ bool decode_partition(const DecodeParams &p, int b, int z,
                                                  int block_size, bool report, int &L,
                                                  int &pidx, int &tok_lo, int &tok_hi) {
@@ -81,8 +79,8 @@ __device__ __forceinline__ bool decode_partition(const DecodeParams &p, int b, i
     const int start = window_start(L, p.window_left);
     const int P = p.partition_size;
     const int n = L > 0 ? (L - 1) / P - start / P + 1 : 0;
-    pidx = n - (int)gridDim.z + z;
-    if (pidx < 0) return false;
+    pidx = z;
+    if (pidx >= n) return false;
     const int part = start / P + pidx;
     tok_lo = max(part * P, start);
     tok_hi = min((part + 1) * P, L);
@@ -174,14 +172,13 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
     float *s_l = reinterpret_cast<float *>(smem + C::L_OFF);
 
     // grid: x = kv head (fastest, so the heads reading one page run together),
-    // y = sequence, z = partition slot (decode_partition)
+    // y = partition slot, z = sequence (decode_partition)
     pdl_trigger();  // the merge kernel may launch once every CTA has started
-    const int b = blockIdx.y, g = blockIdx.x;
+    const int b = blockIdx.z, g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int L, pidx, tok_lo, tok_hi;
-    if (!decode_partition(p, b, blockIdx.z, BS,
-                          blockIdx.z == gridDim.z - 1 && g == 0 && threadIdx.x == 0, L, pidx,
-                          tok_lo, tok_hi))
+    if (!decode_partition(p, b, blockIdx.y, BS, blockIdx.y == 0 && g == 0 && threadIdx.x == 0,
+                          L, pidx, tok_lo, tok_hi))
         return;  // this slot holds no attended key
     const int pg_lo = tok_lo / BS;
     const int npages = (tok_hi - 1) / BS - pg_lo + 1;
@@ -460,12 +457,11 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
     __shared__ float s_o[kMaxGroup * D];
 
     pdl_trigger();  // the merge kernel may launch once every CTA has started
-    const int b = blockIdx.y, g = blockIdx.x;
+    const int b = blockIdx.z, g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int L, pidx, tok_lo, tok_hi;
-    if (!decode_partition(p, b, blockIdx.z, block_size,
-                          blockIdx.z == gridDim.z - 1 && g == 0 && threadIdx.x == 0, L, pidx,
-                          tok_lo, tok_hi))
+    if (!decode_partition(p, b, blockIdx.y, block_size,
+                          blockIdx.y == 0 && g == 0 && threadIdx.x == 0, L, pidx, tok_lo, tok_hi))
         return;
 
     const int G = p.group, Hkv = p.num_kv_heads;
@@ -782,7 +778,7 @@ cudaError_t launch_tc(const DecodeParams &p, const CUtensorMap *tk, const CUtens
                       : decode_bf16_tc_kernel<D, BS, NHT, NST, false>;
     cudaError_t e = set_smem(kern, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_kv_heads, p.batch, p.num_parts);
+    dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
     kern<<<grid, kDecThreads, C::SMEM, stream>>>(p, *tk, *tv);
     return cudaGetLastError();
 }
@@ -808,7 +804,7 @@ cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
     if (p.group > kMaxGroup || p.partition_size > kMaxPartition) return cudaErrorNotSupported;
     if (D % 16 != 0 || D > 256 || p.head_dim != D) return cudaErrorNotSupported;
     if (cache.dtype == PKV_F32) {
-        dim3 grid(p.num_kv_heads, p.batch, p.num_parts);
+        dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
         if (T == 64)
             decode_f32_kernel<64><<<grid, kDecThreads, 0, stream>>>(p, BS);
         else if (T == 128)

@@ -344,7 +344,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
         !aligned(block_table, 4) || !aligned(cache_seqlens, 4))
         return PKV_ERR_INVALID_ARG;
     const int np = decode_num_parts(max_seqlen, P, window_left);
-    if (np > 65535) return PKV_ERR_UNSUPPORTED;  // grid.z limit
+    if (np > 65535) return PKV_ERR_UNSUPPORTED;  // grid.y limit
     const DecodeLayout lay = decode_layout(batch, num_qo_heads, cache.head_dim, np);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.total)
         return PKV_ERR_WORKSPACE;

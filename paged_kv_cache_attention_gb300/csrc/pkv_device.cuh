@@ -108,22 +108,6 @@ __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, dev_error, abort));
 }
 
-// Named barrier over `nthreads` threads (whole warps) that also ANDs a
-// predicate across them: every participant gets the same answer, so warps
-// that share a barrier agree on whether to go on or wind down.
-__device__ __forceinline__ bool bar_sync_and(uint32_t bar_id, uint32_t nthreads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(bar_id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) tile loads into shared memory
 // ---------------------------------------------------------------------------

@@ -24,22 +24,16 @@
 //               bounds, which fills zeros;
 //   warp 1      owns TMEM; one thread issues tcgen05.mma (each group of 8
 //               k-steps from one PTX block, descriptors built once):
-//                 S_x = Q_x K^T   (A, B K-major in smem, fp32 into the one S
-//                                  buffer of TMEM; with ALiBi one more
-//                                  k-step adds the bias)
-//                 O_x += P_x V    (A = P_x in TMEM as bf16, B = V MN-major)
-//               Tensor memory holds O_0, O_1, one S buffer and P_0, P_1 apart
-//               (512 columns): the two query tiles take the S buffer in turn,
-//               and S of one tile is computed while the other tile's softmax
-//               runs, so neither S nor PV lies on a softmax's critical path;
+//                 S_x = Q_x K^T   (A, B K-major in smem, fp32 in TMEM; with
+//                                  ALiBi one more k-step adds the bias)
+//                 O_x += P_x V    (A = P in TMEM as bf16, B = V MN-major)
 //   warps 2-17  softmax, eight per query tile: two per TMEM lane quarter,
 //               each owning half of its 32 rows' 128 key columns (thread =
-//               row = TMEM lane).  They read S with tcgen05.ld (and release
-//               the buffer at once), mask, combine their partial row maxima
-//               through shared memory, rescale O in TMEM only when the
-//               maximum grows by more than 2^8, write P to their tile's P
-//               columns, and finally normalise O (sink included) and store
-//               it.
+//               row = TMEM lane).  They read S with tcgen05.ld, mask, combine
+//               their partial row maxima through shared memory, rescale O in
+//               TMEM only when the maximum grows by more than 2^8, write P
+//               back to TMEM in place of S, and finally normalise O (sink
+//               included) and store it.
 // A small single-CTA kernel first builds the work list on the device
 // (counting sort by key-tile count, heaviest first).
 #include <type_traits>
@@ -87,10 +81,9 @@ struct PfLayout {
     static constexpr int B_VFULL = B_KEMPTY + kStages;
     static constexpr int B_VEMPTY = B_VFULL + kStages;
     static constexpr int B_VFIX = B_VEMPTY + kStages;
-    static constexpr int B_SFULL = B_VFIX + 1;     // S_x(j) computed        (MMA commit)
-    static constexpr int B_SFREE = B_SFULL + kNQ;  // S_x(j) in registers    (256 threads)
-    static constexpr int B_PFULL = B_SFREE + kNQ;  // P_x(j) in TMEM         (256 threads)
-    static constexpr int B_ODONE = B_PFULL + kNQ;  // PV_x(j) done           (MMA commit)
+    static constexpr int B_SFULL = B_VFIX + 1;
+    static constexpr int B_PFULL = B_SFULL + kNQ;
+    static constexpr int B_ODONE = B_PFULL + kNQ;
     static constexpr int B_DRAIN = B_ODONE + kNQ;  // the MMAs in flight, after a failed wait
     static constexpr int NBARS = B_DRAIN + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
@@ -103,19 +96,16 @@ struct PfLayout {
     // and their number
     static constexpr int OFF_LIST = OFF_XL + kNQ * 128 * 2 * 4;
     static constexpr int OFF_NLIST = OFF_LIST + kMaxSparseTiles * 2;
-    static constexpr int SMEM = 1024 + OFF_NLIST + 16;
+    // the row pairs' wait status, double-buffered like the maxima
+    static constexpr int OFF_XOK = OFF_NLIST + 16;
+    static constexpr int SMEM = 1024 + OFF_XOK + 2 * kNQ * 128 * 2 * 4;
     static constexpr int SOFT_WARPS = 8;  // per query tile: 2 per TMEM lane quarter
     static constexpr int THREADS = 64 + kNQ * SOFT_WARPS * 32;
-    // tensor memory: O_0, O_1 (128 fp32 columns each), the S buffer both
-    // query tiles take in turn (128 fp32 columns) and P_0, P_1 (128 bf16
-    // each, packed two to a column: 64 columns each)
-    static constexpr int TMEM_COLS = 512;
-    static constexpr int S_COL = kNQ * 128;
+    static constexpr int TMEM_COLS = 512;  // O_0, O_1, S_0, S_1: 128 columns each
 };
 
 __host__ __device__ constexpr int o_col(int x) { return x * 128; }
-__host__ __device__ constexpr int p_col(int x) { return PfLayout::S_COL + 128 + x * 64; }
-static_assert(p_col(kNQ) <= PfLayout::TMEM_COLS, "tensor memory budget");
+__host__ __device__ constexpr int s_col(int x) { return kNQ * 128 + x * 128; }
 
 using pf::align1024;
 using pf::st_shared_zero16;
@@ -332,13 +322,13 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geo geo = make_geo(p, item, BS, CONTIG, threadIdx.x == 0);
-    int32_t *const abort = pf::abort_word(p);
+    int32_t *const abort = pf::abort_word(p);  // zeroed by the work-list kernel
     const int G = p.group;
     const int TPR = p.rows_per_head;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lay::NBARS; ++i)
-            mbar_init(bar(i), (i >= Lay::B_SFREE && i < Lay::B_PFULL + kNQ)
+            mbar_init(bar(i), (i >= Lay::B_PFULL && i < Lay::B_PFULL + kNQ)
                                   ? (uint32_t)(Lay::SOFT_WARPS * 32)
                                   : 1u);
         fence_barrier_init();
@@ -447,16 +437,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             const int oob_row = HND ? (int)(p.num_blocks * p.num_kv_heads) : (int)(p.num_blocks * BS);
             const int pg0 = geo.kt_lo * NPG;       // first page of the CTA's key range
             const int npages_kv = (geo.kv_len + BS - 1) / BS;
-            // lane l: pool row of page pg0 + 32 * batch + l, one cache for the
-            // key tiles and one for the value tiles (they are loaded a tile
-            // apart)
-            int idk_batch = -1, idk_row = oob_row, idv_batch = -1, idv_row = oob_row;
-            // the box row of this lane's page (lane / 2) of key tile t
-            auto row_of = [&](int &batch, int &ids_row, int t) {
-                const int rel = tile_of(t) * NPG;
-                if (!CONTIG && (rel >> 5) != batch) {  // 32 block ids per warp-wide load
-                    batch = rel >> 5;
-                    const int pg = pg0 + batch * 32 + lane;
+            int ids_batch = -1, ids_row = oob_row;  // lane l: pool row of page pg0 + 32*batch + l
+            bool alive = true;
+            int nk = 0, nv = 0;  // key / value tiles whose loads were issued
+            for (int j = 0; j < ntiles && alive; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                const int key0 = (geo.kt_lo + tile_of(j)) * kTileN;
+                const int rel = tile_of(j) * NPG;
+                if (!CONTIG && (rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
+                    ids_batch = rel >> 5;
+                    const int pg = pg0 + ids_batch * 32 + lane;
                     ids_row = oob_row;
                     if (pg < npages_kv) {
                         const int blk = bt[pg];
@@ -466,52 +457,35 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                             ids_row = HND ? blk * p.num_kv_heads + geo.g : blk * BS;
                     }
                 }
-                int row = __shfl_sync(0xffffffffu, ids_row,
-                                      ((rel & 31) + min(lane >> 1, NPG - 1)) & 31);
-                // contiguous rows past kv_len are masked
-                if constexpr (CONTIG) row = p.cu_k[geo.r] + (geo.kt_lo + tile_of(t)) * kTileN;
-                return row;
-            };
-            // key or value tile t into ring stage t % 2, once the stage is free
-            auto load = [&](bool value, int t) {
-                const int s = t & 1;
-                const uint32_t ph = (t >> 1) & 1;
-                const int row = value ? row_of(idv_batch, idv_row, t)
-                                      : row_of(idk_batch, idk_row, t);
-                const int b_empty = (value ? Lay::B_VEMPTY : Lay::B_KEMPTY) + s;
-                const int b_full = (value ? Lay::B_VFULL : Lay::B_KFULL) + s;
-                if (!warp_wait_bounded(bar(b_empty), ph ^ 1, p.dev_error, abort)) return false;
-                if (lane == 0) mbar_arrive_expect_tx(bar(b_full), Lay::T_BYTES);
+                int row = __shfl_sync(0xffffffffu, ids_row, ((rel & 31) + min(lane >> 1, NPG - 1)) & 31);
+                if constexpr (CONTIG) row = p.cu_k[geo.r] + key0;  // rows past kv_len are masked
+                // K
+                alive = warp_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error, abort);
+                if (!alive) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_KFULL + s), Lay::T_BYTES);
                 __syncwarp();
                 if (lane < 2 * NPG) {
                     const int pg = lane >> 1, h = lane & 1;
-                    tma_load_3d((value ? sV : sK) + s * Lay::T_BYTES + h * Lay::HALF +
-                                    pg * BS * 128,
-                                value ? &tmv : &tmk, bar(b_full), h * 64, cy, row);
+                    tma_load_3d(sK + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmk,
+                                bar(Lay::B_KFULL + s), h * 64, cy, row);
                 }
-                return true;
-            };
-            // Order of the loads: the order the MMA issuer consumes them in,
-            // K(j+1) (for S_0(j+1)) before V(j) (for PV_0(j), at the end of
-            // tile 0's softmax of key tile j).
-            int nk = 0, nv = 0;  // key / value tiles whose loads were issued
-            bool alive = load(false, 0);
-            if (alive) nk = 1;
-            for (int j = 0; j < ntiles && alive; ++j) {
-                if (j + 1 < ntiles) {
-                    if (!(alive = load(false, j + 1))) break;
-                    ++nk;
+                ++nk;
+                // V
+                alive = warp_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error, abort);
+                if (!alive) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_VFULL + s), Lay::T_BYTES);
+                __syncwarp();
+                if (lane < 2 * NPG) {
+                    const int pg = lane >> 1, h = lane & 1;
+                    tma_load_3d(sV + s * Lay::T_BYTES + h * Lay::HALF + pg * BS * 128, &tmv,
+                                bar(Lay::B_VFULL + s), h * 64, cy, row);
                 }
-                if (!(alive = load(true, j))) break;
                 ++nv;
                 if (is_tail(j)) {
                     // rows at or past kv_len of the last value tile may hold any
                     // bits: zero them so P = 0 never meets a non-finite value
-                    const int s = j & 1;
-                    alive = warp_wait_bounded(bar(Lay::B_VFULL + s), (j >> 1) & 1, p.dev_error,
-                                              abort);
+                    alive = warp_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error, abort);
                     if (!alive) break;
-                    const int key0 = (geo.kt_lo + tile_of(j)) * kTileN;
                     const int first = max(geo.kv_len - key0, 0);
                     const uint32_t vb = sV + s * Lay::T_BYTES;
                     for (int e = first * 16 + lane; e < kTileN * 16; e += 32) {
@@ -542,17 +516,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // One S buffer serves both query tiles in turn; P_0 and P_1 have columns
-        // of their own.  S of the next tile is issued as soon as the softmax
-        // warps of the previous one have loaded theirs into registers, so
-        // every S product overlaps a softmax and the chain of a query tile is
-        // its softmax alone.  Issue order (it follows the order the waits are
-        // met in when the two tiles' softmaxes run staggered):
-        //   S_0(0); then per key tile j:
-        //   S_1(j) [S_0(j) loaded]; PV_1(j-1) [P_1(j-1) stored];
-        //   S_0(j+1) [S_1(j) loaded]; PV_0(j) [P_0(j) stored];
-        // and PV_1(n-1) at the end.  Each step only waits for work issued
-        // before it, so the order cannot deadlock.
+        // Order per key tile j:  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): the next
+        // S of a query tile only waits for that tile's own PV (S_x(j+1) is
+        // written where P_x(j) lives), not for the other tile's softmax.
         if (ntiles > 0 && lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
@@ -567,66 +533,74 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             const uint64_t dv0 = tc::smem_desc_sw128(sV, Lay::HALF, 1024);
             const uint64_t dqa = tc::smem_desc_noswz(sQA, 128, 256);
             const uint64_t dka = tc::smem_desc_noswz(sKA, 128, 256);
-            const uint32_t dS = tmem + Lay::S_COL;
             auto issue_s = [&](int x, int s) {
                 const uint64_t dq = dq0 + (uint64_t)((x * Lay::Q_BYTES) >> 4);
                 const uint64_t dk = dk0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
+                const uint32_t d = tmem + s_col(x);
+                auto kstep = [&](int kk) {
+                    const uint32_t koff = ((kk >> 2) * Lay::HALF + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(d, dq + koff, dk + koff, idS, kk > 0 ? 1u : 0u);
+                };
                 if (ksteps == kHeadDim / 16) {
-                    tc::mma_ss8<Lay::HALF>(dS, dq, dk, idS, 0u);
+                    tc::mma_ss8<Lay::HALF>(d, dq, dk, idS, 0u);
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                         if (kk >= ksteps) break;
-                        const uint32_t koff = ((kk >> 2) * Lay::HALF + (kk & 3) * 32) >> 4;
-                        tc::mma_ss(dS, dq + koff, dk + koff, idS, kk > 0 ? 1u : 0u);
+                        kstep(kk);
                     }
                 }
-                if constexpr (ALIBI) tc::mma_ss(dS, dqa, dka, idS, 1u);
+                if constexpr (ALIBI) tc::mma_ss(d, dqa, dka, idS, 1u);
                 tc::commit(bar(Lay::B_SFULL + x));
             };
-            // O_x (+)= P_x V(jv): the first PV of a tile overwrites O_x
-            auto issue_pv = [&](int x, int jv) {
-                const uint64_t dv = dv0 + (uint64_t)(((jv & 1) * Lay::T_BYTES) >> 4);
-                tc::mma_ts8(tmem + o_col(x), tmem + p_col(x), dv, idO, jv > 0 ? 1u : 0u);
-                tc::commit(bar(Lay::B_ODONE + x));
-            };
-            auto wait = [&](int b, uint32_t parity) {
-                const bool ok = mbar_wait_bounded(bar(b), parity, p.dev_error, abort);
+            bool alive = mbar_wait_bounded(bar(Lay::B_Q), 0, p.dev_error, abort) &&
+                         mbar_wait_bounded(bar(Lay::B_KFULL + 0), 0, p.dev_error, abort);
+            if (alive) {
                 tc::fence_after_sync();
-                return ok;
-            };
-            bool alive = wait(Lay::B_Q, 0) && wait(Lay::B_KFULL + 0, 0);
-            if (alive) issue_s(0, 0);
+                for (int x = 0; x < kNQ; ++x) issue_s(x, 0);
+                tc::commit(bar(Lay::B_KEMPTY + 0));
+            }
             for (int j = 0; j < ntiles && alive; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = (j >> 1) & 1;
-                // S_1(j): the S buffer is free once tile 0 has loaded S_0(j)
-                if (!(alive = wait(Lay::B_SFREE + 0, j & 1))) break;
-                issue_s(1, s);
-                tc::commit(bar(Lay::B_KEMPTY + s));  // K(j) is done with after S_1(j)
-                if (j > 0) {  // PV_1(j-1)
-                    if (!(alive = wait(Lay::B_PFULL + 1, (j - 1) & 1))) break;
-                    issue_pv(1, j - 1);
-                    tc::commit(bar(Lay::B_VEMPTY + (s ^ 1)));  // V(j-1) is done with
+                const int sn = (j + 1) & 1;
+                const uint32_t phn = ((j + 1) >> 1) & 1;
+                const bool more = j + 1 < ntiles;
+                for (int x = 0; x < kNQ && alive; ++x) {
+                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + x), j & 1, p.dev_error, abort);
+                    if (!alive) break;
+                    tc::fence_after_sync();
+                    if (x == 0) {
+                        if (is_tail(j))
+                            alive = mbar_wait_bounded(bar(Lay::B_VFIX), 0, p.dev_error);
+                        else
+                            alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                    }
+                    {
+                        const uint64_t dv = dv0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
+                        const uint32_t dO = tmem + o_col(x), aP = tmem + s_col(x);
+                        tc::mma_ts8(dO, aP, dv, idO, j > 0 ? 1u : 0u);
+                    }
+                    tc::commit(bar(Lay::B_ODONE + x));
+                    if (more) {
+                        if (x == 0) {
+                            alive = mbar_wait_bounded(bar(Lay::B_KFULL + sn), phn, p.dev_error,
+                                                      abort);
+                            if (!alive) break;
+                        }
+                        // P_x(j) lives where S_x(j+1) goes: PV_x(j) must be done
+                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + x), j & 1, p.dev_error,
+                                                  abort);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                        issue_s(x, sn);
+                        if (x == kNQ - 1) tc::commit(bar(Lay::B_KEMPTY + sn));
+                    }
                 }
-                if (j + 1 < ntiles) {  // S_0(j+1)
-                    if (!(alive = wait(Lay::B_SFREE + 1, j & 1))) break;
-                    if (!(alive = wait(Lay::B_KFULL + (s ^ 1), ((j + 1) >> 1) & 1))) break;
-                    issue_s(0, s ^ 1);
-                }
-                // PV_0(j)
-                if (!(alive = wait(Lay::B_PFULL + 0, j & 1))) break;
-                if (!(alive = is_tail(j) ? wait(Lay::B_VFIX, 0) : wait(Lay::B_VFULL + s, ph)))
-                    break;
-                issue_pv(0, j);
-            }
-            if (alive) {  // PV_1(n-1)
-                const int j = ntiles - 1;
-                alive = wait(Lay::B_PFULL + 1, j & 1);
-                if (alive) {
-                    issue_pv(1, j);
-                    tc::commit(bar(Lay::B_VEMPTY + (j & 1)));
-                }
+                if (!alive) break;
+                tc::commit(bar(Lay::B_VEMPTY + s));
             }
             if (!alive) {
                 // a wait gave up: let the MMAs already issued finish (bounded)
@@ -657,8 +631,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         const int cpos = p.causal ? qpos : (1 << 30);  // causal upper bound on keys
         const int head = geo.g * G + h_local;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + Lay::S_COL + hc * 64;
-        const uint32_t tP = tmem + lane_off + p_col(x) + hc * 32;
+        const uint32_t tS = tmem + lane_off + s_col(x) + hc * 64;
+        const uint32_t tP = tmem + lane_off + s_col(x) + hc * 32;
         const uint32_t tO = tmem + lane_off + o_col(x) + hc * 64;
         const uint32_t pair_bar = 1 + x * 4 + quarter;
         float *xmax = reinterpret_cast<float *>(smem + Lay::OFF_XMAX);
@@ -669,10 +643,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         const float al2 = ALIBI ? p.alibi[head] * kLog2e : 0.f;
 
         float m_run = kNegInf, l_run = 0.f;
-        // alive: the pair goes on; ok: every wait of this warp so far was met
-        // (a failed wait is reported at the next pair barrier, where both
-        // warps of the row pair leave together)
-        bool alive = true, ok = true;
+        bool alive = true;
         for (int j = 0; j < ntiles; ++j) {
             const int key0 = (geo.kt_lo + tile_of(j)) * kTileN + hc * 64;  // first key of this half
             uint64_t keep = ~0ull;  // sparse form: bit c keeps key key0 + c
@@ -684,20 +655,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                        __brevll(bits64(p.sbits + (int64_t)head * p.bit_words, p.bit_words,
                                        qpos - key0 - 63));
             }
-            ok = ok && warp_wait_bounded(bar(Lay::B_SFULL + x), j & 1, p.dev_error, abort);
+            // a warp whose wait gave up still meets its partner at the pair
+            // barrier below, and both leave together
+            const bool s_ok = warp_wait_bounded(bar(Lay::B_SFULL + x), j & 1, p.dev_error, abort);
             tc::fence_after_sync();
-            uint32_t ra[32], rb[32];
-            tc::ld_32x32b_x32(tS, ra);
-            tc::ld_32x32b_x32(tS + 32, rb);
-            tc::wait_ld();
-            // S is in registers: the other tile's S may now be written there
-            tc::fence_before_sync();
-            mbar_arrive(bar(Lay::B_SFREE + x));
             const bool full = !SPARSE && (key0 + 63 <= cpos) && (key0 + 64 <= geo.kv_len) &&
                               (wl < 0 || key0 >= qpos - wl);
             // keys this row keeps: [klo, khi] (inclusive), relative to key0
             const int khi = min(cpos, geo.kv_len - 1) - key0;
             const int klo = wl < 0 ? -1 : qpos - wl - key0;
+            uint32_t ra[32], rb[32];
+            tc::ld_32x32b_x32(tS, ra);
+            tc::ld_32x32b_x32(tS + 32, rb);
+            tc::wait_ld();
             // ALiBi: the extra k-step of S added slope / scale * (key - kt0),
             // kt0 = the tile's first key; the row's part slope * (kt0 - qpos)
             // joins here (log2 units)
@@ -742,7 +712,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             }
             float *slot = xmax + (((j & 1) * kNQ + x) * 128 + row) * 2;
             slot[hc] = mine;
-            alive = bar_sync_and(pair_bar, 64, ok);
+            int *okslot = reinterpret_cast<int *>(smem + Lay::OFF_XOK) +
+                          (((j & 1) * kNQ + x) * 128 + row) * 2;
+            okslot[hc] = s_ok;
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            // both warps of the pair read both flags: they leave together
+            alive = s_ok && okslot[hc ^ 1];
             if (!alive) break;
             const float mx = fmaxf(mine, slot[hc ^ 1]);
             const float m_tile = fmaf(mx, sl2, ct);
@@ -751,18 +726,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             // growth, so the row's largest P stays 2^0 (see the tile order
             // above).
             const bool grow = m_tile > m_run + ((ALIBI || SPARSE) ? 0.f : kRescaleThreshold);
-            // O_x and P_x belong to PV_x(j-1) until it completes
-            bool pv_done = j == 0;
             // tcgen05.ld/st are warp-collective: the warp rescales together,
             // lanes whose maximum did not grow enough multiply by 1
             if (__any_sync(0xffffffffu, grow)) {
                 const float alpha = grow ? fast_exp2(m_run - m_tile) : 1.f;
                 l_run *= alpha;
                 if (j > 0) {
-                    ok = ok && warp_wait_bounded(bar(Lay::B_ODONE + x), (j - 1) & 1,
-                                                 p.dev_error, abort);
-                    tc::fence_after_sync();
-                    pv_done = true;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r16[16];
@@ -796,14 +765,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                         ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
                         src[i] = pack_bf16(p0, p1);
                     }
+                    tc::st_32x32b_x16(tP + h * 16, src);
                 }
-                if (!pv_done) {  // PV_x(j-1) still reads P_x
-                    ok = ok && warp_wait_bounded(bar(Lay::B_ODONE + x), (j - 1) & 1,
-                                                 p.dev_error, abort);
-                    tc::fence_after_sync();
-                }
-                tc::st_32x32b_x16(tP, ra);
-                tc::st_32x32b_x16(tP + 16, rb);
             }
             float s0, s1, s2, s3;
             f2_unpack(ps2[0], s0, s1);
@@ -815,10 +778,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         }
         // epilogue: combine the two halves' sums, normalise (sink in the
         // denominator) and store this warp's 64 output columns
-        bool have_o = ntiles > 0 && alive && ok;
+        bool have_o = ntiles > 0 && alive;
         if (have_o) {
-            have_o = warp_wait_bounded(bar(Lay::B_ODONE + x), (ntiles - 1) & 1, p.dev_error,
-                                       abort);
+            have_o = __all_sync(0xffffffffu, mbar_wait_bounded(bar(Lay::B_ODONE + x),
+                                                               (ntiles - 1) & 1, p.dev_error));
             tc::fence_after_sync();
         }
         float *lslot = xl + (x * 128 + row) * 2;

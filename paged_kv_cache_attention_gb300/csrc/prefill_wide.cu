@@ -66,7 +66,10 @@ struct WideLayout {
     // [2 (query tile)][128][2] between the two warps of a row
     static constexpr int OFF_XMAX = OFF_TMEM + 16;
     static constexpr int OFF_XL = OFF_XMAX + 2 * 128 * 2 * 4;
-    static constexpr int SMEM = 1024 + OFF_XL + 2 * 128 * 2 * 4;
+    // the row pairs' wait status ([2][128][2] ints, double-buffered like the
+    // maxima)
+    static constexpr int OFF_XOK = OFF_XL + 2 * 128 * 2 * 4;
+    static constexpr int SMEM = 1024 + OFF_XOK + 2 * 128 * 2 * 4;
     static constexpr int SOFT_THREADS = 256;
     static constexpr int THREADS = 64 + SOFT_THREADS;
     static constexpr int TMEM_COLS = 512;  // O: 0..255, S0: 256..319, S1: 320..383
@@ -388,13 +391,9 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 const int khi = min(cpos, geo.kv_len - 1) - key0;
                 const int klo = wl < 0 ? -1 : qpos - wl - key0;
                 uint32_t ra[32];
-                if (s_ok) {
-                    tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 32, ra);
-                    tc::wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ra[i] = __float_as_uint(kNegInf);
-                }
+                // loaded even after a failed wait (the values are then unused)
+                tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 32, ra);
+                tc::wait_ld();
                 if (!full) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -428,7 +427,12 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 const float mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
                 float *slot = xmax + ((jg & 1) * 128 + row) * 2;
                 slot[hc] = mine;
-                alive = bar_sync_and(pair_bar, 64, s_ok);
+                int *okslot = reinterpret_cast<int *>(smem + Lay::OFF_XOK) +
+                              ((jg & 1) * 128 + row) * 2;
+                okslot[hc] = s_ok;
+                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                // both warps of the pair read both flags: they leave together
+                alive = s_ok && okslot[hc ^ 1];
                 if (!alive) break;
                 const float mx = fmaxf(mine, slot[hc ^ 1]);
                 const float m_tile = ALIBI ? mx : mx * sl2;
