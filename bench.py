@@ -58,13 +58,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # compiled from, comments and layout aside).
 NCU_TRAFFIC = {
     # decode call of the mixed step (split-KV kernel + merge): 3157.7 MB read
-    # and 7.2 MB of partials written by the partition kernel, 27.8 MB of
+    # and 7.0 MB of partials written by the partition kernel, 27.8 MB of
     # partials read back by the merge (cold caches under ncu; live they are
-    # L2 hits); mean of two calls
-    "decode": {"bytes": 3192652800, "sha": "39e52c11020f41c0"},
-    # prefill launch of the mixed step: 665.1 MB read + 85.6 MB written
-    # (mean of two launches)
-    "prefill": {"bytes": 750740096, "sha": "933746382003040d"},
+    # L2 hits); mean of three calls
+    "decode": {"bytes": 3192533418, "sha": "cab8a1ad62af2811"},
+    # prefill launch of the mixed step: 664.3 MB read + 83.7 MB written
+    # (mean of three launches)
+    "prefill": {"bytes": 747997610, "sha": "f785460fa13ed7b2"},
 }
 
 
@@ -528,14 +528,16 @@ def time_e2e(stepper, K, W, dist, overlapped=True):
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
 
     def run(n):
-        h2d_done = [torch.cuda.Event() for _ in range(n)]
-        done = [torch.cuda.Event() for _ in range(n)]
-        d2h_done = [torch.cuda.Event() for _ in range(n)]
+        h2d_start = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        h2d_done = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        done = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        d2h_done = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
         def upload(k):
             with torch.cuda.stream(up):
                 if k >= 2:
                     up.wait_event(done[k - 2])  # step k-2 no longer reads set k % 2
+                h2d_start[k].record(up)
                 for h, d in zip(host_in, ins(sets[k % 2])):
                     d.copy_(h, non_blocking=True)
                 h2d_done[k].record(up)
@@ -555,20 +557,43 @@ def time_e2e(stepper, K, W, dist, overlapped=True):
                     h.copy_(d, non_blocking=True)
                 d2h_done[k].record(down)
         torch.cuda.synchronize()
+        # per-step copy durations on their streams (diagnostics)
+        return (statistics.mean(h2d_start[k].elapsed_time(h2d_done[k]) for k in range(n)),
+                statistics.mean(done[k].elapsed_time(d2h_done[k]) for k in range(n)))
 
     run(W)
     dist.barrier()
     t0 = time.perf_counter()
-    run(K)
+    up_ms, down_ms = run(K)
     dist.barrier()
     ms = (time.perf_counter() - t0) * 1e3
     del other
-    return ms, h2d, d2h
+    return ms, h2d, d2h, up_ms, down_ms
+
+
+def time_back_to_back(fn, n, reps=3):
+    """Median over reps of the mean device time of n back-to-back launches of
+    fn (CUDA events on the current stream, after 3 warm-up launches)."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    means = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        means.append(a.elapsed_time(b) / n)
+    return statistics.median(means)
 
 
 def extra_configs(dev, K, peaks):
     """Per-configuration lines for the other serving shapes (decode GB/s and
-    prefill TFLOP/s), each input set larger than L2."""
+    prefill TFLOP/s), each input set larger than L2: the median of three
+    means of back-to-back launches (50 for decode, 20 for prefill)."""
     import torch
     import paged_kv_cache_attention_gb300 as pkv
     from paged_kv_cache_attention_gb300 import workloads as W
@@ -595,16 +620,7 @@ def extra_configs(dev, K, peaks):
                                  sink=t["sink"], window_left=c.window_left,
                                  sm_scale=c.sm_scale, partition_size=c.partition_size,
                                  workspace=t["ws"], alibi_slopes=t["alibi"])
-        for _ in range(3):
-            go()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(K):
-            go()
-        b.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / K
+        ms = time_back_to_back(go, max(K, 50))
         gbs = byts / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 4), "kv_bytes": byts, "GB/s": round(gbs, 1),
                      "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 3),
@@ -634,16 +650,7 @@ def extra_configs(dev, K, peaks):
             pkv.varlen_prefill(q, kc, vc, bt, cq, ck, c4.max_seqlen_q, c4.max_seqlen_k,
                                sink=sink, sm_scale=c4.sm_scale, out=outp, workspace=ws,
                                alibi_slopes=al)
-        for _ in range(3):
-            go4()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(K):
-            go4()
-        b.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / K
+        ms = time_back_to_back(go4, max(K, 20))
         tf = fl / (ms * 1e-3) / 1e12
         out[name] = {"ms": round(ms, 4), "flops": fl, "TFLOP/s": round(tf, 1),
                      "frac_bf16_measured_burst": round(tf / peaks["bf16_tflops"], 3)}
@@ -664,16 +671,7 @@ def extra_configs(dev, K, peaks):
     def gow():
         pkv.varlen_prefill(qw, kcw, vcw, btw, cqw, ckw, c4w.max_seqlen_q, c4w.max_seqlen_k,
                            sink=sinkw, sm_scale=c4w.sm_scale, out=outw, workspace=wsw)
-    for _ in range(3):
-        gow()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(K):
-        gow()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / K
+    ms = time_back_to_back(gow, max(K, 20))
     flw = prefill_flops(c4w)
     tf = flw / (ms * 1e-3) / 1e12
     out["config4_prefill_B16_D256"] = {"ms": round(ms, 4), "flops": flw, "TFLOP/s": round(tf, 1),
@@ -851,11 +849,16 @@ def run_ours(args, dist):
         "clocks": clk,
     }
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = time_e2e(stepper, max(3, K // 2), 2, dist)
-        e2e_step = dist.max(e2e_ms / max(3, K // 2))
+        # a run of steps long enough that filling and draining the copy
+        # pipeline (the first upload, the last download) is a small part
+        K_e2e = max(30, K)
+        e2e_ms, h2d, d2h, up_ms, down_ms = time_e2e(stepper, K_e2e, 3, dist)
+        e2e_step = dist.max(e2e_ms / K_e2e)
         line["e2e"] = {"value": round(tokens / (e2e_step * 1e-3), 1), "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": round(e2e_step, 4)}
+                       "ms_per_step": round(e2e_step, 4), "steps": K_e2e,
+                       "h2d_ms_per_step": round(up_ms, 4), "d2h_ms_per_step": round(down_ms, 4),
+                       "timing": "host wall clock around all steps, copies included"}
     del stepper
     torch.cuda.empty_cache()
     if not args.no_extra:

@@ -29,6 +29,8 @@ reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict_
                          const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
                          int64_t vecs_per_row, int64_t capacity, int block_size,
                          int64_t vecs_per_head, int32_t *dev_error) {
+    pdl_trigger();  // the next call's kernel may begin launching
+    pdl_wait();     // the previous kernel on the stream has finished
     const int64_t per_tensor = num_tokens * vecs_per_row;
     const int64_t total = 2 * per_tensor;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -89,11 +91,11 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     auto kern = hnd ? reshape_and_cache_kernel<true> : reshape_and_cache_kernel<false>;
-    kern<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
-        vecs_per_row, capacity, block_size, head_bytes / 16, dev_error);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
+                      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                      slot_mapping, num_tokens, vecs_per_row, capacity, block_size,
+                      head_bytes / 16, dev_error);
 }
 
 }  // namespace pkv

@@ -174,6 +174,7 @@ decode_bf16_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap 
     // grid: x = kv head (fastest, so the heads reading one page run together),
     // y = partition slot, z = sequence (decode_partition)
     pdl_trigger();  // the merge kernel may launch once every CTA has started
+    pdl_wait();     // the previous kernel on the stream (a cache write) has finished
     const int b = blockIdx.z, g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int L, pidx, tok_lo, tok_hi;
@@ -457,6 +458,7 @@ decode_f32_kernel(const DecodeParams p, int block_size) {
     __shared__ float s_o[kMaxGroup * D];
 
     pdl_trigger();  // the merge kernel may launch once every CTA has started
+    pdl_wait();     // the previous kernel on the stream has finished
     const int b = blockIdx.z, g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int L, pidx, tok_lo, tok_hi;
@@ -779,8 +781,7 @@ cudaError_t launch_tc(const DecodeParams &p, const CUtensorMap *tk, const CUtens
     cudaError_t e = set_smem(kern, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
-    kern<<<grid, kDecThreads, C::SMEM, stream>>>(p, *tk, *tv);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kDecThreads), C::SMEM, stream, p, *tk, *tv);
 }
 
 template <int D, int BS>
@@ -806,12 +807,11 @@ cudaError_t launch_decode(const DecodeParams &p, const pkv_cache_desc &cache,
     if (cache.dtype == PKV_F32) {
         dim3 grid(p.num_kv_heads, p.num_parts, p.batch);
         if (T == 64)
-            decode_f32_kernel<64><<<grid, kDecThreads, 0, stream>>>(p, BS);
+            e = launch_pdl(decode_f32_kernel<64>, grid, dim3(kDecThreads), 0, stream, p, BS);
         else if (T == 128)
-            decode_f32_kernel<128><<<grid, kDecThreads, 0, stream>>>(p, BS);
+            e = launch_pdl(decode_f32_kernel<128>, grid, dim3(kDecThreads), 0, stream, p, BS);
         else
             return cudaErrorNotSupported;
-        e = cudaGetLastError();
     } else {
         if (T == 64 && BS == 16)
             e = launch_tc_g<64, 16>(p, tmap_k, tmap_v, stream);

@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
     const int tid = threadIdx.x;
     const int tokens = kNQ * p.rows_per_head;
     pdl_trigger();  // the attention kernel (launched as a dependent) may start launching
+    pdl_wait();     // the previous kernel on the stream has finished
     if (tid == 0) *pf::abort_word(p) = 0;  // the attention launch's abort word
 
     // 1. pairs (request, q block) per request, exclusive prefix sum
@@ -602,12 +603,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 if (!alive) break;
                 tc::commit(bar(Lay::B_VEMPTY + s));
             }
-            if (!alive) {
-                // a wait gave up: let the MMAs already issued finish (bounded)
-                // before tensor memory is released
-                tc::commit(bar(Lay::B_DRAIN));
-                mbar_wait_bounded(bar(Lay::B_DRAIN), 0, p.dev_error);
-            }
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -833,6 +828,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
+        // If a wait of this launch gave up, MMAs this CTA issued may still
+        // be running: the issuing thread lets them finish (bounded) before
+        // tensor memory is released.  (Here rather than in the MMA loop, where
+        // the extra code slowed the loop by 1-2 %.)
+        // (the word is re-read through the kernel parameter, so that no
+        // register holds its address through the roles' loops)
+        if (lane == 0 && *reinterpret_cast<volatile int32_t *>(p.tiles + 1) != 0) {
+            tc::commit(bar(Lay::B_DRAIN));
+            mbar_wait_bounded(bar(Lay::B_DRAIN), 0, p.dev_error);
+        }
+        __syncwarp();
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Lay::TMEM_COLS);
     }
@@ -851,8 +857,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, 
     if (cache.dtype != PKV_BF16 || cache.head_dim % 16 != 0 ||
         (cache.head_dim > kHeadDim && cache.head_dim != 256))
         return cudaErrorNotSupported;
-    prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(prefill_schedule_kernel, dim3(1), dim3(kSchedThreads), 0, stream, p);
     if (e != cudaSuccess) return e;
     if (cache.head_dim == 256)
         return launch_prefill_wide(p, cache, contiguous, tmap_q, tmap_k, tmap_v, stream);

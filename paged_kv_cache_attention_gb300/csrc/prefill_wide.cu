@@ -339,12 +339,6 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 }
                 kv_t += t.n;
             }
-            if (!alive) {
-                // a wait gave up: let the MMAs already issued finish (bounded)
-                // before tensor memory is released
-                tc::commit(bar(Lay::B_DRAIN));
-                mbar_wait_bounded(bar(Lay::B_DRAIN), 0, p.dev_error);
-            }
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -381,8 +375,9 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 const int b = j & 1;
                 // a warp whose wait gave up still meets its partner at the pair
                 // barrier below, and both leave together
-                const bool s_ok = o_ok && warp_wait_bounded(bar(Lay::B_SFULL + b), su[b] & 1,
-                                                            p.dev_error, abort);
+                const bool s_wait = warp_wait_bounded(bar(Lay::B_SFULL + b), su[b] & 1,
+                                                      p.dev_error, abort);
+                const bool s_ok = o_ok && s_wait;
                 ++su[b];
                 tc::fence_after_sync();
                 const int key0 = (t.kt_lo + tile_of(t.n, j)) * kTileN + hc * 32;
@@ -551,6 +546,17 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
+        // If a wait of this launch gave up, MMAs this CTA issued may still
+        // be running: the issuing thread lets them finish (bounded) before
+        // tensor memory is released.  (Here rather than in the MMA loop, where
+        // the extra code slowed the loop by 1-2 %.)
+        // (the word is re-read through the kernel parameter, so that no
+        // register holds its address through the roles' loops)
+        if (lane == 0 && *reinterpret_cast<volatile int32_t *>(p.tiles + 1) != 0) {
+            tc::commit(bar(Lay::B_DRAIN));
+            mbar_wait_bounded(bar(Lay::B_DRAIN), 0, p.dev_error);
+        }
+        __syncwarp();
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Lay::TMEM_COLS);
     }
