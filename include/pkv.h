@@ -295,6 +295,12 @@ PKV_API size_t pkv_varlen_prefill_workspace_size(int batch, int num_qo_heads, in
  *   tiles are padded to 128 with zeros), block_size 16 or 32,
  *   G = num_qo_heads / num_kv_heads a power of two <= 16; anything else
  *   returns PKV_ERR_UNSUPPORTED.
+ *   max_ctas       host int: at most this many CTAs of the attention kernel
+ *                  run at once (each takes one SM and draws work items until
+ *                  none is left); 0 means one per SM.  A smaller number
+ *                  leaves SMs free for work the caller runs beside the call
+ *                  on another stream (a decode, for example); the result
+ *                  does not depend on it.  Head size 256 ignores it.
  */
 PKV_API pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
                               const void *v_cache, pkv_cache_desc cache,
@@ -304,7 +310,7 @@ PKV_API pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_ca
                               const float *sink, const float *alibi_slopes, int batch,
                               int num_qo_heads, int causal, int window_left, float sm_scale,
                               float *lse_out, void *workspace, size_t workspace_bytes,
-                              int32_t *dev_error, void *stream);
+                              int max_ctas, int32_t *dev_error, void *stream);
 
 /*
  * varlen_prefill_contiguous: varlen_prefill with the keys and values of all

@@ -119,7 +119,7 @@ def load_library(path: Optional[str] = None):
         lib.pkv_varlen_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.pkv_varlen_prefill_workspace_size.restype = sz
         lib.pkv_varlen_prefill.argtypes = [P, P, P, P, CacheDesc, P, i32, P, P, i32, i32, i32, P,
-                                           P, i32, i32, i32, i32, f32, P, P, sz, P, P]
+                                           P, i32, i32, i32, i32, f32, P, P, sz, i32, P, P]
         lib.pkv_varlen_prefill.restype = i32
         lib.pkv_varlen_prefill_contiguous.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, i32,
                                                       i32, i32, P, P, i32, i32, i32, i32, f32, P,
@@ -397,13 +397,15 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
                    max_seqlen_q: int, max_seqlen_k: int, sink=None, causal: bool = True,
                    window_left: int = -1, sm_scale: Optional[float] = None, out=None, lse=None,
                    workspace=None, dev_error=None, stream=None, alibi_slopes=None,
-                   layout: str = "NHD"):
+                   layout: str = "NHD", max_ctas: int = 0):
     """Varlen / chunk prefill over the paged pools; returns out [total_q, Hq, D].
 
     q: [total_q, Hq, D] bf16; cu_seq_lens_q / cu_seq_lens_k: [B+1] int32;
     max_seqlen_q / max_seqlen_k: host ints; request r's queries sit at the end
     of its kv_len keys.  causal=False drops the j <= position bound (a window
-    still bounds keys from below).
+    still bounds keys from below).  max_ctas: at most this many attention
+    CTAs (one SM each) at once, 0 = one per SM; fewer leave SMs free for
+    work on another stream.
     """
     torch = _torch()
     desc = _cache_desc(k_cache, v_cache, layout)
@@ -435,7 +437,7 @@ def varlen_prefill(q, k_cache, v_cache, block_table, cu_seq_lens_q, cu_seq_lens_
         block_table.shape[1], _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), int(max_seqlen_q),
         int(max_seqlen_k), int(total_q), _ptr(sink), _ptr(alibi_slopes), B, Hq,
         int(bool(causal)), int(window_left), scale, _ptr(lse), _ptr(ws),
-        ws.numel() * ws.element_size(), _ptr(dev_error), _stream_handle(stream))
+        ws.numel() * ws.element_size(), int(max_ctas), _ptr(dev_error), _stream_handle(stream))
     _check("pkv_varlen_prefill", st)
     return out
 

@@ -419,12 +419,14 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
                        const float *alibi_slopes, int batch, int num_qo_heads, int causal,
                        int window_left, float sm_scale,
                        float *lse_out, void *workspace, size_t workspace_bytes,
-                       int32_t *dev_error, void *stream, const SparseMask *sparse = nullptr) {
+                       int32_t *dev_error, void *stream, const SparseMask *sparse = nullptr,
+                       int max_ctas = 0) {
     if (cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (cache.head_dim % 16 != 0 || (cache.head_dim > 128 && cache.head_dim != 256))
         return PKV_ERR_UNSUPPORTED;
     if (batch < 0 || num_qo_heads <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
-        total_q < 0 || max_blocks_per_seq <= 0 || window_left < -1 || !std::isfinite(sm_scale))
+        total_q < 0 || max_blocks_per_seq <= 0 || window_left < -1 || !std::isfinite(sm_scale) ||
+        max_ctas < 0)
         return PKV_ERR_INVALID_ARG;
     if (num_qo_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     const int G = num_qo_heads / cache.num_kv_heads;
@@ -477,6 +479,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
     p.total_k = contiguous ? (int)kv_rows : 0;
     p.rows_per_head = 128 / G;
     p.max_tiles = (int)lay.max_items;
+    p.max_ctas = max_ctas;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
 
     // With no contiguous keys at all every request clips to kv_len 0 and no
@@ -519,14 +522,15 @@ pkv_status pkv_varlen_prefill(void *out, const void *q, const void *k_cache,
                               const float *sink, const float *alibi_slopes, int batch,
                               int num_qo_heads, int causal, int window_left, float sm_scale,
                               float *lse_out, void *workspace, size_t workspace_bytes,
-                              int32_t *dev_error, void *stream) {
+                              int max_ctas, int32_t *dev_error, void *stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     return prefill_run(out, q, k_cache, v_cache, cache, false,
                        cache.num_blocks * cache.block_size, block_table, max_blocks_per_seq,
                        cu_seq_lens_q, cu_seq_lens_k, max_seqlen_q, max_seqlen_k, total_q, sink,
                        alibi_slopes, batch, num_qo_heads, causal, window_left, sm_scale,
-                       lse_out, workspace, workspace_bytes, dev_error, stream);
+                       lse_out, workspace, workspace_bytes, dev_error, stream, nullptr,
+                       max_ctas);
 }
 
 pkv_status pkv_varlen_prefill_contiguous(void *out, const void *q, const void *k, const void *v,

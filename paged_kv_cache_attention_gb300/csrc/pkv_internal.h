@@ -65,6 +65,7 @@ struct PrefillParams {
     int bit_words;
     int rows_per_head;             // query tokens per 128-row tile (128 / group)
     int max_tiles;                 // capacity of the work list
+    int max_ctas;                  // attention CTAs of the launch (0: one per SM)
     float scale_log2;
 };
 

@@ -80,21 +80,29 @@ struct PfLayout {
     static constexpr int B_KEMPTY = B_KFULL + kStages;
     static constexpr int B_VFULL = B_KEMPTY + kStages;
     static constexpr int B_VEMPTY = B_VFULL + kStages;
-    static constexpr int B_VFIX = B_VEMPTY + kStages;
-    static constexpr int B_SFULL = B_VFIX + 1;
+    static constexpr int B_VFIX = B_VEMPTY + kStages;  // [kStages] tail rows of V zeroed
+    static constexpr int B_SFULL = B_VFIX + kStages;
     static constexpr int B_PFULL = B_SFULL + kNQ;
     static constexpr int B_ODONE = B_PFULL + kNQ;
     static constexpr int B_DRAIN = B_ODONE + kNQ;  // the MMAs in flight, after a failed wait
-    static constexpr int NBARS = B_DRAIN + 1;
+    // a CTA takes work items one after another (persistent form):
+    static constexpr int B_QEMPTY = B_DRAIN + 1;   // every S of the item done: Q may be reloaded
+    static constexpr int B_OFREE = B_QEMPTY + 1;   // [kNQ] the epilogue has read O_x
+    static constexpr int RING = 4;                 // item indices handed from the producer
+    static constexpr int B_IFULL = B_OFREE + kNQ;  // [RING] slot written
+    static constexpr int B_IEMPTY = B_IFULL + RING;  // [RING] slot read by the MMA thread and
+                                                     // the 16 softmax warps
+    static constexpr int NBARS = B_IEMPTY + RING;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     // row-max exchange between the two warps sharing a row ([2][kNQ][128][2]
-    // floats, double-buffered by tile parity) and the row-sum exchange
-    // ([kNQ][128][2])
+    // floats, double-buffered by key-tile parity) and the row-sum exchange
+    // ([2][kNQ][128][2], double-buffered by item parity)
     static constexpr int OFF_XMAX = OFF_TMEM + 16;
     static constexpr int OFF_XL = OFF_XMAX + 2 * kNQ * 128 * 2 * 4;
+    static constexpr int OFF_RING = OFF_XL + 2 * kNQ * 128 * 2 * 4;  // [RING] item indices
     // sparse form: the key tiles the item attends ([kMaxSparseTiles] uint16)
     // and their number
-    static constexpr int OFF_LIST = OFF_XL + kNQ * 128 * 2 * 4;
+    static constexpr int OFF_LIST = OFF_RING + RING * 4;
     static constexpr int OFF_NLIST = OFF_LIST + kMaxSparseTiles * 2;
     // the row pairs' wait status, double-buffered like the maxima
     static constexpr int OFF_XOK = OFF_NLIST + 16;
@@ -153,7 +161,10 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
     const int tokens = kNQ * p.rows_per_head;
     pdl_trigger();  // the attention kernel (launched as a dependent) may start launching
     pdl_wait();     // the previous kernel on the stream has finished
-    if (tid == 0) *pf::abort_word(p) = 0;  // the attention launch's abort word
+    if (tid == 0) {
+        *pf::abort_word(p) = 0;    // the attention launch's abort word
+        *pf::item_counter(p) = 0;  // items drawn by persistent attention CTAs
+    }
 
     // 1. pairs (request, q block) per request, exclusive prefix sum
     int carry = 0;
@@ -307,10 +318,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using Lay = PfLayout;
     constexpr int NPG = kTileN / BS;  // pages per key tile
+    // The dense forms are persistent: a CTA takes work item blockIdx.x, then
+    // draws further items from a counter of the work list until none is left,
+    // keeping its barriers, tensor memory and shared-memory layout; every
+    // barrier's phase carries on from item to item.  The sparse form takes
+    // one item per CTA (its per-item list of key tiles is built by the whole
+    // CTA before the roles split).
+    constexpr bool PERSIST = !SPARSE;
 
     pdl_wait();  // the work list: the attention grid launches while it is built
-    if ((int)blockIdx.x >= p.tiles[0]) return;  // beyond the work list
-    const int4 item = reinterpret_cast<const int4 *>(p.tiles + 64)[blockIdx.x];
+    const int n_items = p.tiles[0];
+    if ((int)blockIdx.x >= n_items) return;  // beyond the work list
+    const int4 *items = reinterpret_cast<const int4 *>(p.tiles + 64);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
@@ -320,18 +339,23 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     const uint32_t bars = sbase + Lay::OFF_BAR;
     auto bar = [&](int i) { return bars + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
+    volatile int *ring = reinterpret_cast<volatile int *>(smem + Lay::OFF_RING);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Geo geo = make_geo(p, item, BS, CONTIG, threadIdx.x == 0);
     int32_t *const abort = pf::abort_word(p);  // zeroed by the work-list kernel
     const int G = p.group;
     const int TPR = p.rows_per_head;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < Lay::NBARS; ++i)
-            mbar_init(bar(i), (i >= Lay::B_PFULL && i < Lay::B_PFULL + kNQ)
-                                  ? (uint32_t)(Lay::SOFT_WARPS * 32)
-                                  : 1u);
+        for (int i = 0; i < Lay::NBARS; ++i) {
+            uint32_t count = 1;
+            if ((i >= Lay::B_PFULL && i < Lay::B_PFULL + kNQ) ||
+                (i >= Lay::B_OFREE && i < Lay::B_OFREE + kNQ))
+                count = Lay::SOFT_WARPS * 32;
+            if (i >= Lay::B_IEMPTY && i < Lay::B_IEMPTY + Lay::RING)
+                count = 1 + kNQ * Lay::SOFT_WARPS;  // the MMA thread + one per softmax warp
+            mbar_init(bar(i), count);
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -339,23 +363,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         tc::tmem_relinquish();
     }
     if constexpr (ALIBI) {
-        // the ALiBi blocks (see PfLayout): element (row r, k) at byte
-        // (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.  The Q
-        // block serves both query tiles: row r's head is g * G + r % G in each.
+        // the ALiBi k-step's blocks (see PfLayout): element (row r, k) at
+        // byte (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
+        // The key side holds r for k < 3; the query side's k < 3 entries
+        // depend on the item's kv head and are written by the producer per
+        // item, the rest stay zero
         for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
             const int r = i >> 4, k = i & 15;
             const int off = (r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
-            float qa = 0.f;
-            if (k < 3) {
-                // slope / scale = hi + mid + lo to about 2^-24 relative
-                const float a = p.alibi[geo.g * G + r % G] * kLog2e / p.scale_log2;
-                const float hi = __bfloat162float(__float2bfloat16_rn(a));
-                const float mid = __bfloat162float(__float2bfloat16_rn(a - hi));
-                qa = k == 0 ? hi : k == 1 ? mid : a - hi - mid;
-            }
-            *reinterpret_cast<__nv_bfloat16 *>(smem + Lay::OFF_QA + off) = __float2bfloat16_rn(qa);
             *reinterpret_cast<__nv_bfloat16 *>(smem + Lay::OFF_KA + off) =
                 __float2bfloat16_rn(k < 3 ? (float)r : 0.f);
+            *reinterpret_cast<__nv_bfloat16 *>(smem + Lay::OFF_QA + off) = __float2bfloat16_rn(0.f);
         }
         fence_proxy_async_smem();
     }
@@ -368,9 +386,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     if constexpr (SPARSE) {
         // the key tiles with at least one kept key for some row of the item
         // (a superset is harmless: every key of a tile is masked per element)
+        const Geo geo = make_geo(p, items[blockIdx.x], BS, CONTIG, false);
         if (threadIdx.x == 0) *s_nlist = 0;
         __syncthreads();
-        const int G = p.group;
         const int t_end = min(geo.t0 + kNQ * p.rows_per_head, geo.q_len);
         const int pos_lo = geo.kv_len - geo.q_len + geo.t0;
         const int pos_hi = geo.kv_len - geo.q_len + t_end - 1;
@@ -404,48 +422,139 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         }
         __syncthreads();
     }
-    const int ntiles = SPARSE ? *s_nlist : geo.ntiles;
-    const int last_key_end = (geo.kt_lo + geo.ntiles) * kTileN;
-    const bool tail = geo.ntiles > 0 && last_key_end > geo.kv_len;
-    // Key tiles in processing order (offsets from kt_lo).  With ALiBi they run
-    // from the query's end backwards: the nearest keys carry the largest
-    // bias, so the first tile usually holds the row maximum and its P = 2^0
-    // is exact in bf16.  The sparse form runs its list of tiles, also from the
-    // end: its rows are dominated by their nearest (slash) keys.
-    auto tile_of = [&](int j) {
-        if constexpr (SPARSE) return (int)s_list[ntiles - 1 - j];
-        return ALIBI ? ntiles - 1 - j : j;
+
+    // One work item as every role sees it: its geometry, the key tiles it
+    // processes and their order.  Key tiles in processing order (offsets
+    // from kt_lo): with ALiBi they run from the query's end backwards (the
+    // nearest keys carry the largest bias, so the first tile usually holds
+    // the row maximum and its P = 2^0 is exact in bf16); the sparse form runs
+    // its list of tiles, also from the end (its rows are dominated by their
+    // nearest, slash, keys).
+    struct Work {
+        Geo geo;
+        int ntiles;  // key tiles processed
+        bool tail;   // the last key tile runs past kv_len
     };
-    auto is_tail = [&](int j) { return tail && tile_of(j) == geo.ntiles - 1; };
+    auto work_of = [&](int idx, bool report) {
+        Work w;
+        w.geo = make_geo(p, items[idx], BS, CONTIG, report);
+        w.ntiles = SPARSE ? *s_nlist : w.geo.ntiles;
+        w.tail = w.geo.ntiles > 0 && (w.geo.kt_lo + w.geo.ntiles) * kTileN > w.geo.kv_len;
+        return w;
+    };
+    auto tile_of = [&](const Work &w, int j) {
+        if constexpr (SPARSE) return (int)s_list[w.ntiles - 1 - j];
+        return ALIBI ? w.ntiles - 1 - j : j;
+    };
+    auto is_tail = [&](const Work &w, int j) {
+        return w.tail && tile_of(w, j) == w.geo.ntiles - 1;
+    };
+    // The n-th item of this CTA for the MMA thread and the softmax warps: the
+    // producer draws it and hands its index over through a ring of shared
+    // slots (-1: none left; -2: a wait gave up).  Each consumer releases the
+    // slot once it has read it.  whole_warp: every lane waits and reads.
+    auto item_at = [&](int n, bool whole_warp) -> int {
+        if constexpr (!PERSIST) return n == 0 ? (int)blockIdx.x : -1;
+        const int s = n % Lay::RING;
+        const uint32_t par = (uint32_t)(n / Lay::RING) & 1;
+        const bool ok = whole_warp ? warp_wait_bounded(bar(Lay::B_IFULL + s), par, p.dev_error, abort)
+                                   : mbar_wait_bounded(bar(Lay::B_IFULL + s), par, p.dev_error, abort);
+        if (!ok) return -2;
+        const int idx = ring[s];
+        if (whole_warp) __syncwarp();
+        if (!whole_warp || lane == 0) mbar_arrive(bar(Lay::B_IEMPTY + s));
+        return idx;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (ntiles > 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+        }
+        // box coordinates of (page, kv head): NHD (x, head, page * BS),
+        // HND (x, 0, page * Hkv + head); one past the pool reads zeros
+        const int oob_row = HND ? (int)(p.num_blocks * p.num_kv_heads) : (int)(p.num_blocks * BS);
+        int kt = 0;          // key tiles loaded so far, all items: ring stage kt % 2
+        int qn = 0;          // Q loads so far
+        int nk = 0, nv = 0;  // key / value tile loads issued (for the drain)
+        bool alive = true;
+        for (int n = 0; alive; ++n) {
+            int idx;
+            if constexpr (PERSIST) {
+                const int s = n % Lay::RING;
+                if (n >= Lay::RING) {  // slot s last held item n - RING
+                    alive = warp_wait_bounded(bar(Lay::B_IEMPTY + s),
+                                              (uint32_t)(n / Lay::RING - 1) & 1, p.dev_error,
+                                              abort);
+                    if (!alive) break;
+                }
+                int drawn = 0;
+                if (lane == 0)
+                    drawn = n == 0 ? (int)blockIdx.x
+                                   : (int)gridDim.x + atomicAdd(pf::item_counter(p), 1);
+                idx = __shfl_sync(0xffffffffu, drawn, 0);
+                if (idx >= n_items) idx = -1;
+                if (lane == 0) {
+                    ring[s] = idx;
+                    mbar_arrive(bar(Lay::B_IFULL + s));
+                }
+            } else {
+                idx = n == 0 ? (int)blockIdx.x : -1;
+            }
+            if (idx < 0) break;
+            const Work w = work_of(idx, lane == 0);
+            const Geo &geo = w.geo;
+            if (w.ntiles == 0) continue;
+            // Q (and the query side of the ALiBi k-step) may be rewritten
+            // once every S product of the previous item is done
+            if (qn > 0) {
+                alive = warp_wait_bounded(bar(Lay::B_QEMPTY), (uint32_t)(qn - 1) & 1,
+                                          p.dev_error, abort);
+                if (!alive) break;
+            }
+            if constexpr (ALIBI) {
+                // the query side's k < 3 entries: row r holds the slope of
+                // head g * G + r % G divided by the scale, split into three
+                // bf16 parts (hi + mid + lo to about 2^-24 relative); the
+                // block serves both query tiles.  Lane l < G loads slope l.
+                float a = 0.f;
+                if (lane < G) a = p.alibi[geo.g * G + lane] * kLog2e / p.scale_log2;
+                for (int r = lane; r < 128; r += 32) {
+                    const float ar = __shfl_sync(0xffffffffu, a, r % G);
+                    const float hi = __bfloat162float(__float2bfloat16_rn(ar));
+                    const float mid = __bfloat162float(__float2bfloat16_rn(ar - hi));
+                    const float parts[3] = {hi, mid, ar - hi - mid};
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        const int off = (r >> 3) * 256 + (r & 7) * 16 + k * 2;
+                        *reinterpret_cast<__nv_bfloat16 *>(smem + Lay::OFF_QA + off) =
+                            __float2bfloat16_rn(parts[k]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             if (lane == 0) {
-                tma_prefetch_desc(&tmq);
-                tma_prefetch_desc(&tmk);
-                tma_prefetch_desc(&tmv);
                 mbar_arrive_expect_tx(bar(Lay::B_Q), kNQ * Lay::Q_BYTES);
                 for (int x = 0; x < kNQ; ++x)
                     for (int h = 0; h < 2; ++h)
                         tma_load_3d(sQ + x * Lay::Q_BYTES + h * Lay::HALF, &tmq, bar(Lay::B_Q),
                                     h * 64, geo.g * G, geo.q_start + geo.t0 + x * TPR);
             }
+            ++qn;
             const int32_t *bt = p.block_table + (int64_t)geo.r * p.max_blocks_per_seq;
-            // box coordinates of (page, kv head): NHD (x, head, page * BS),
-            // HND (x, 0, page * Hkv + head); one past the pool reads zeros
             const int cy = HND ? 0 : geo.g;
-            const int oob_row = HND ? (int)(p.num_blocks * p.num_kv_heads) : (int)(p.num_blocks * BS);
-            const int pg0 = geo.kt_lo * NPG;       // first page of the CTA's key range
+            const int pg0 = geo.kt_lo * NPG;       // first page of the item's key range
             const int npages_kv = (geo.kv_len + BS - 1) / BS;
             int ids_batch = -1, ids_row = oob_row;  // lane l: pool row of page pg0 + 32*batch + l
-            bool alive = true;
-            int nk = 0, nv = 0;  // key / value tiles whose loads were issued
-            for (int j = 0; j < ntiles && alive; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                const int key0 = (geo.kt_lo + tile_of(j)) * kTileN;
-                const int rel = tile_of(j) * NPG;
+            for (int j = 0; j < w.ntiles && alive; ++j) {
+                const int t = kt + j;
+                const int s = t & 1;
+                const uint32_t ph = (t >> 1) & 1;
+                const int key0 = (geo.kt_lo + tile_of(w, j)) * kTileN;
+                const int rel = tile_of(w, j) * NPG;
                 if (!CONTIG && (rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
                     ids_batch = rel >> 5;
                     const int pg = pg0 + ids_batch * 32 + lane;
@@ -482,7 +591,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                                 bar(Lay::B_VFULL + s), h * 64, cy, row);
                 }
                 ++nv;
-                if (is_tail(j)) {
+                if (is_tail(w, j)) {
                     // rows at or past kv_len of the last value tile may hold any
                     // bits: zero them so P = 0 never meets a non-finite value
                     alive = warp_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error, abort);
@@ -495,32 +604,37 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(Lay::B_VFIX));
+                    if (lane == 0) mbar_arrive(bar(Lay::B_VFIX + s));
                 }
             }
-            // Let the MMA issuer's last "stage empty" arrivals land before the
-            // CTA can exit.
-            for (int j = max(0, ntiles - kStages); j < ntiles && alive; ++j) {
-                const uint32_t ph = (j >> 1) & 1;
-                alive = warp_wait_bounded(bar(Lay::B_KEMPTY + (j & 1)), ph, p.dev_error, abort) &&
-                        warp_wait_bounded(bar(Lay::B_VEMPTY + (j & 1)), ph, p.dev_error, abort);
-            }
-            if (!alive) {
-                // a wait gave up: let this warp's copies still in flight land
-                // (bounded) before the CTA's shared memory is released
-                warp_wait_bounded(bar(Lay::B_Q), 0, p.dev_error);
-                for (int t = max(0, nk - kStages); t < nk; ++t)
-                    warp_wait_bounded(bar(Lay::B_KFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
-                for (int t = max(0, nv - kStages); t < nv; ++t)
-                    warp_wait_bounded(bar(Lay::B_VFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
-            }
+            kt += w.ntiles;
+        }
+        // Let the MMA issuer's last "stage empty" arrivals land before the
+        // CTA can exit.
+        for (int t = max(0, kt - kStages); t < kt && alive; ++t) {
+            const uint32_t ph = (t >> 1) & 1;
+            alive = warp_wait_bounded(bar(Lay::B_KEMPTY + (t & 1)), ph, p.dev_error, abort) &&
+                    warp_wait_bounded(bar(Lay::B_VEMPTY + (t & 1)), ph, p.dev_error, abort);
+        }
+        if (!alive) {
+            // a wait gave up: let this warp's copies still in flight land
+            // (bounded) before the CTA's shared memory is released
+            if (qn > 0) warp_wait_bounded(bar(Lay::B_Q), (uint32_t)(qn - 1) & 1, p.dev_error);
+            for (int t = max(0, nk - kStages); t < nk; ++t)
+                warp_wait_bounded(bar(Lay::B_KFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
+            for (int t = max(0, nv - kStages); t < nv; ++t)
+                warp_wait_bounded(bar(Lay::B_VFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Order per key tile j:  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): the next
         // S of a query tile only waits for that tile's own PV (S_x(j+1) is
         // written where P_x(j) lives), not for the other tile's softmax.
-        if (ntiles > 0 && lane == 0) {
+        // Across items the same rule holds for the first S of an item (it
+        // waits for the previous item's last PV of that tile), and the first
+        // PV of an item, which overwrites O_x, waits until the previous item's
+        // epilogue has read O_x.
+        if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
             const int ksteps = p.head_dim / 16;  // k-steps past the head size multiply zeros
@@ -554,54 +668,94 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 if constexpr (ALIBI) tc::mma_ss(d, dqa, dka, idS, 1u);
                 tc::commit(bar(Lay::B_SFULL + x));
             };
-            bool alive = mbar_wait_bounded(bar(Lay::B_Q), 0, p.dev_error, abort) &&
-                         mbar_wait_bounded(bar(Lay::B_KFULL + 0), 0, p.dev_error, abort);
-            if (alive) {
+            int kt = 0;       // key tiles consumed so far, all items
+            int gstep = 0;    // (key tile, query tile) steps so far: phases of S/P/O barriers
+            int qn = 0;       // items with key tiles so far
+            int vfn[kStages] = {0, 0};  // tail fixes consumed per stage
+            bool alive = true;
+            for (int n = 0; alive; ++n) {
+                const int idx = item_at(n, false);
+                if (idx < 0) {
+                    alive = idx == -1;
+                    break;
+                }
+                const Work w = work_of(idx, false);
+                if (w.ntiles == 0) continue;
+                alive = mbar_wait_bounded(bar(Lay::B_Q), (uint32_t)qn & 1, p.dev_error, abort) &&
+                        mbar_wait_bounded(bar(Lay::B_KFULL + (kt & 1)), (kt >> 1) & 1,
+                                          p.dev_error, abort);
+                if (!alive) break;
                 tc::fence_after_sync();
-                for (int x = 0; x < kNQ; ++x) issue_s(x, 0);
-                tc::commit(bar(Lay::B_KEMPTY + 0));
-            }
-            for (int j = 0; j < ntiles && alive; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                const int sn = (j + 1) & 1;
-                const uint32_t phn = ((j + 1) >> 1) & 1;
-                const bool more = j + 1 < ntiles;
                 for (int x = 0; x < kNQ && alive; ++x) {
-                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + x), j & 1, p.dev_error, abort);
-                    if (!alive) break;
-                    tc::fence_after_sync();
-                    if (x == 0) {
-                        if (is_tail(j))
-                            alive = mbar_wait_bounded(bar(Lay::B_VFIX), 0, p.dev_error);
-                        else
-                            alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error);
-                        if (!alive) break;
+                    if (gstep > 0) {  // the previous item's last P_x lives where S_x goes
+                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + x), (gstep - 1) & 1,
+                                                  p.dev_error, abort);
                         tc::fence_after_sync();
                     }
-                    {
-                        const uint64_t dv = dv0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
-                        const uint32_t dO = tmem + o_col(x), aP = tmem + s_col(x);
-                        tc::mma_ts8(dO, aP, dv, idO, j > 0 ? 1u : 0u);
-                    }
-                    tc::commit(bar(Lay::B_ODONE + x));
-                    if (more) {
-                        if (x == 0) {
-                            alive = mbar_wait_bounded(bar(Lay::B_KFULL + sn), phn, p.dev_error,
-                                                      abort);
-                            if (!alive) break;
-                        }
-                        // P_x(j) lives where S_x(j+1) goes: PV_x(j) must be done
-                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + x), j & 1, p.dev_error,
-                                                  abort);
-                        if (!alive) break;
-                        tc::fence_after_sync();
-                        issue_s(x, sn);
-                        if (x == kNQ - 1) tc::commit(bar(Lay::B_KEMPTY + sn));
-                    }
+                    if (alive) issue_s(x, kt & 1);
                 }
                 if (!alive) break;
-                tc::commit(bar(Lay::B_VEMPTY + s));
+                tc::commit(bar(Lay::B_KEMPTY + (kt & 1)));
+                if (w.ntiles == 1) tc::commit(bar(Lay::B_QEMPTY));
+                for (int j = 0; j < w.ntiles && alive; ++j) {
+                    const int t = kt + j, g = gstep + j;
+                    const int s = t & 1;
+                    const uint32_t ph = (t >> 1) & 1;
+                    const int sn = (t + 1) & 1;
+                    const uint32_t phn = ((t + 1) >> 1) & 1;
+                    const bool more = j + 1 < w.ntiles;
+                    for (int x = 0; x < kNQ && alive; ++x) {
+                        alive = mbar_wait_bounded(bar(Lay::B_PFULL + x), g & 1, p.dev_error, abort);
+                        if (!alive) break;
+                        tc::fence_after_sync();
+                        if (x == 0) {
+                            if (is_tail(w, j)) {
+                                alive = mbar_wait_bounded(bar(Lay::B_VFIX + s), vfn[s] & 1,
+                                                          p.dev_error, abort);
+                                ++vfn[s];
+                            } else {
+                                alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error,
+                                                          abort);
+                            }
+                            if (!alive) break;
+                            tc::fence_after_sync();
+                        }
+                        if (j == 0 && qn > 0) {  // the previous item's epilogue has read O_x
+                            alive = mbar_wait_bounded(bar(Lay::B_OFREE + x), (qn - 1) & 1,
+                                                      p.dev_error, abort);
+                            if (!alive) break;
+                            tc::fence_after_sync();
+                        }
+                        {
+                            const uint64_t dv = dv0 + (uint64_t)((s * Lay::T_BYTES) >> 4);
+                            const uint32_t dO = tmem + o_col(x), aP = tmem + s_col(x);
+                            tc::mma_ts8(dO, aP, dv, idO, j > 0 ? 1u : 0u);
+                        }
+                        tc::commit(bar(Lay::B_ODONE + x));
+                        if (more) {
+                            if (x == 0) {
+                                alive = mbar_wait_bounded(bar(Lay::B_KFULL + sn), phn, p.dev_error,
+                                                          abort);
+                                if (!alive) break;
+                            }
+                            // P_x(j) lives where S_x(j+1) goes: PV_x(j) must be done
+                            alive = mbar_wait_bounded(bar(Lay::B_ODONE + x), g & 1, p.dev_error,
+                                                      abort);
+                            if (!alive) break;
+                            tc::fence_after_sync();
+                            issue_s(x, sn);
+                            if (x == kNQ - 1) {
+                                tc::commit(bar(Lay::B_KEMPTY + sn));
+                                if (j + 2 == w.ntiles) tc::commit(bar(Lay::B_QEMPTY));
+                            }
+                        }
+                    }
+                    if (!alive) break;
+                    tc::commit(bar(Lay::B_VEMPTY + s));
+                }
+                kt += w.ntiles;
+                gstep += w.ntiles;
+                ++qn;
             }
         }
     } else {
@@ -620,11 +774,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         const int row = quarter * 32 + lane;
         const int tok_local = row / G;
         const int h_local = row - tok_local * G;
-        const int tok = geo.t0 + x * TPR + tok_local;
-        const bool row_valid = tok < geo.q_len;
-        const int qpos = geo.kv_len - geo.q_len + tok;
-        const int cpos = p.causal ? qpos : (1 << 30);  // causal upper bound on keys
-        const int head = geo.g * G + h_local;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + s_col(x) + hc * 64;
         const uint32_t tP = tmem + lane_off + s_col(x) + hc * 32;
@@ -634,13 +783,26 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         float *xl = reinterpret_cast<float *>(smem + Lay::OFF_XL);
         const float sl2 = p.scale_log2;
         const int wl = p.window_left;
+        int gstep = 0;  // key-tile steps of this query tile so far, all items
+        bool alive = true;
+        for (int n = 0; alive; ++n) {
+        const int idx = item_at(n, true);
+        if (idx < 0) break;
+        const Work wk = work_of(idx, false);
+        const Geo &geo = wk.geo;
+        const int ntiles = wk.ntiles;
+        const int tok = geo.t0 + x * TPR + tok_local;
+        const bool row_valid = tok < geo.q_len;
+        const int qpos = geo.kv_len - geo.q_len + tok;
+        const int cpos = p.causal ? qpos : (1 << 30);  // causal upper bound on keys
+        const int head = geo.g * G + h_local;
         // ALiBi slope of this row's head in log2 units
         const float al2 = ALIBI ? p.alibi[head] * kLog2e : 0.f;
 
         float m_run = kNegInf, l_run = 0.f;
-        bool alive = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int key0 = (geo.kt_lo + tile_of(j)) * kTileN + hc * 64;  // first key of this half
+            const int g = gstep + j;
+            const int key0 = (geo.kt_lo + tile_of(wk, j)) * kTileN + hc * 64;  // first key of this half
             uint64_t keep = ~0ull;  // sparse form: bit c keeps key key0 + c
             if constexpr (SPARSE) {
                 // vertical bits of keys [key0, key0 + 64) and slash bits of the
@@ -652,7 +814,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             }
             // a warp whose wait gave up still meets its partner at the pair
             // barrier below, and both leave together
-            const bool s_ok = warp_wait_bounded(bar(Lay::B_SFULL + x), j & 1, p.dev_error, abort);
+            const bool s_ok = warp_wait_bounded(bar(Lay::B_SFULL + x), g & 1, p.dev_error, abort);
             tc::fence_after_sync();
             const bool full = !SPARSE && (key0 + 63 <= cpos) && (key0 + 64 <= geo.kv_len) &&
                               (wl < 0 || key0 >= qpos - wl);
@@ -705,10 +867,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
                 }
                 mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             }
-            float *slot = xmax + (((j & 1) * kNQ + x) * 128 + row) * 2;
+            float *slot = xmax + (((g & 1) * kNQ + x) * 128 + row) * 2;
             slot[hc] = mine;
             int *okslot = reinterpret_cast<int *>(smem + Lay::OFF_XOK) +
-                          (((j & 1) * kNQ + x) * 128 + row) * 2;
+                          (((g & 1) * kNQ + x) * 128 + row) * 2;
             okslot[hc] = s_ok;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             // both warps of the pair read both flags: they leave together
@@ -775,11 +937,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         // denominator) and store this warp's 64 output columns
         bool have_o = ntiles > 0 && alive;
         if (have_o) {
-            have_o = __all_sync(0xffffffffu, mbar_wait_bounded(bar(Lay::B_ODONE + x),
-                                                               (ntiles - 1) & 1, p.dev_error));
+            have_o = warp_wait_bounded(bar(Lay::B_ODONE + x), (gstep + ntiles - 1) & 1,
+                                       p.dev_error, abort);
             tc::fence_after_sync();
         }
-        float *lslot = xl + (x * 128 + row) * 2;
+        float *lslot = xl + (((n & 1) * kNQ + x) * 128 + row) * 2;
         lslot[hc] = l_run;
         asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
         const float l_tot = l_run + lslot[hc ^ 1];
@@ -824,6 +986,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         }
         if (row_valid && hc == 0 && p.lse_out)
             p.lse_out[(int64_t)(geo.q_start + tok) * p.num_qo_heads + head] = lse;
+        if (ntiles > 0) {  // O_x has been read: the next item's first PV may overwrite it
+            tc::fence_before_sync();
+            mbar_arrive(bar(Lay::B_OFREE + x));
+            gstep += ntiles;
+        }
+        }  // items
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -861,28 +1029,34 @@ cudaError_t launch_prefill(const PrefillParams &p, const pkv_cache_desc &cache, 
     if (e != cudaSuccess) return e;
     if (cache.head_dim == 256)
         return launch_prefill_wide(p, cache, contiguous, tmap_q, tmap_k, tmap_v, stream);
-    const int grid = p.max_tiles;
-    if (grid <= 0) return cudaSuccess;
-    auto go = [&](auto kern) -> cudaError_t {
+    if (p.max_tiles <= 0) return cudaSuccess;
+    // the dense forms are persistent: one CTA per SM (or the caller's cap),
+    // each drawing work items until none is left; the sparse form takes one
+    // item per CTA
+    const int ctas = p.max_ctas > 0 ? p.max_ctas : device_sm_count();
+    const int persistent_grid = p.max_tiles < ctas ? p.max_tiles : ctas;
+    auto go = [&](auto kern, bool persistent) -> cudaError_t {
         cudaError_t e2 = set_smem(kern, PfLayout::SMEM);
         if (e2 != cudaSuccess) return e2;
+        const int grid = persistent ? persistent_grid : p.max_tiles;
         return launch_pdl(kern, dim3(grid), dim3(PfLayout::THREADS), PfLayout::SMEM, stream, p,
                           *tmap_q, *tmap_k, *tmap_v);
     };
     auto paged = [&](auto alibi_tag) -> cudaError_t {
         constexpr bool AL = decltype(alibi_tag)::value;
         if (cache.block_size == 16)
-            return p.hnd ? go(prefill_tc_kernel<16, false, AL, true>)
-                         : go(prefill_tc_kernel<16, false, AL, false>);
+            return p.hnd ? go(prefill_tc_kernel<16, false, AL, true>, true)
+                         : go(prefill_tc_kernel<16, false, AL, false>, true);
         if (cache.block_size == 32)
-            return p.hnd ? go(prefill_tc_kernel<32, false, AL, true>)
-                         : go(prefill_tc_kernel<32, false, AL, false>);
+            return p.hnd ? go(prefill_tc_kernel<32, false, AL, true>, true)
+                         : go(prefill_tc_kernel<32, false, AL, false>, true);
         return cudaErrorNotSupported;
     };
-    if (contiguous && p.vbits) return go(prefill_tc_kernel<kTileN, true, false, false, true>);
+    if (contiguous && p.vbits)
+        return go(prefill_tc_kernel<kTileN, true, false, false, true>, false);
     if (contiguous)
-        return p.alibi ? go(prefill_tc_kernel<kTileN, true, true, false>)
-                       : go(prefill_tc_kernel<kTileN, true, false, false>);
+        return p.alibi ? go(prefill_tc_kernel<kTileN, true, true, false>, true)
+                       : go(prefill_tc_kernel<kTileN, true, false, false>, true);
     return p.alibi ? paged(std::true_type{}) : paged(std::false_type{});
 }
 

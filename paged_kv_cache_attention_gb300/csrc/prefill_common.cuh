@@ -33,6 +33,10 @@ __device__ __forceinline__ int clip_len(int v, int cap, int32_t *err, bool repor
 // word (mbar_wait_bounded), zeroed by the work-list kernel before each launch.
 __device__ __forceinline__ int32_t *abort_word(const PrefillParams &p) { return p.tiles + 1; }
 
+// Word 2: the count of work items drawn beyond the first one of every CTA
+// (persistent attention CTAs), zeroed by the work-list kernel.
+__device__ __forceinline__ int32_t *item_counter(const PrefillParams &p) { return p.tiles + 2; }
+
 __device__ __forceinline__ int clip_len64(long long v, int cap, int32_t *err, bool report) {
     return clip_len(v < 0 ? -1 : (v > cap ? cap + 1 : (int)v), cap, err, report);
 }

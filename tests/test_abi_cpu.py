@@ -131,15 +131,18 @@ def test_reshape_and_cache_validation():
     (dict(hq=24), 2),               # group of 3 (not a power of two)
     (dict(total_q=0), 0),
     (dict(ws_bytes=16), 3),
+    (dict(max_ctas=-1), 1),         # a negative CTA cap
 ])
 def test_prefill_validation(change, expected):
     lib = pkv.load_library()
-    a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30, window=-1, d=128)
+    a = dict(causal=1, dtype=1, hq=32, total_q=100, ws_bytes=1 << 30, window=-1, d=128,
+             max_ctas=0)
     a.update(change)
     st = lib.pkv_varlen_prefill(FAKE, FAKE, FAKE, FAKE, _desc(dtype=a["dtype"], d=a["d"]), FAKE,
                                 8, FAKE,
                                 FAKE, 64, 128, a["total_q"], None, None, 2, a["hq"], a["causal"],
-                                a["window"], 0.1, None, FAKE, a["ws_bytes"], None, None)
+                                a["window"], 0.1, None, FAKE, a["ws_bytes"], a["max_ctas"], None,
+                                None)
     assert st == expected
 
 

@@ -152,8 +152,9 @@ def test_varlen_prefill(lib):
     lse, err = torch.zeros(20, 8, dtype=F32), torch.zeros(1, dtype=I32)
     pkv.varlen_prefill(q, kc, vc, bt, cuq, cuk, 12, 140, sink=sink, causal=False,
                        window_left=7, sm_scale=0.5, out=out, lse=lse, dev_error=err,
-                       alibi_slopes=alibi)
+                       alibi_slopes=alibi, max_ctas=37)
     a = lib.last("pkv_varlen_prefill")
+    assert a["max_ctas"] == 37
     assert a["out"] == out.data_ptr() and a["q"] == q.data_ptr()
     assert a["k_cache"] == kc.data_ptr() and a["v_cache"] == vc.data_ptr()
     assert _desc_fields(a["cache"]) == (10, 16, 2, 64, pkv.PKV_BF16, 0)
