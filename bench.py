@@ -58,14 +58,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # only while the kernel's code is unchanged (sha256 prefix of the files it is
 # compiled from, comments and layout aside).
 NCU_TRAFFIC = {
-    # decode call of the mixed step (split-KV kernel + merge): 3157.7 MB read
-    # and 7.0 MB of partials written by the partition kernel, 27.8 MB of
+    # decode call of the mixed step (split-KV kernel + merge): 3157.8 MB read
+    # and 7.6 MB of partials written by the partition kernel, 27.8 MB of
     # partials read back by the merge (cold caches under ncu; live they are
     # L2 hits); mean of three calls
-    "decode": {"bytes": 3192533418, "sha": "cab8a1ad62af2811"},
-    # prefill launch of the mixed step: 664.3 MB read + 83.7 MB written
+    "decode": {"bytes": 3193203285, "sha": "f65c0ecb16b8e406"},
+    # prefill launch of the mixed step: 677.8 MB read + 78.7 MB written
     # (mean of three launches)
-    "prefill": {"bytes": 747997610, "sha": "f785460fa13ed7b2"},
+    "prefill": {"bytes": 756499370, "sha": "021cc1df15861ab3"},
 }
 
 

@@ -490,7 +490,7 @@ pkv_status prefill_run(void *out, const void *q, const void *k, const void *v,
         kv_rows = 1;
     }
     alignas(64) CUtensorMap tq, tk, tv;
-    const int box_rows = contiguous ? (cache.head_dim == 256 ? 64 : 128) : cache.block_size;
+    const int box_rows = contiguous ? 128 : cache.block_size;
     pkv_status st;
     if ((st = encode_rows_map(&tq, q, cache.head_dim, num_qo_heads, total_q, G, 128 / G)) !=
         PKV_OK)

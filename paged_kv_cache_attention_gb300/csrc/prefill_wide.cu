@@ -9,13 +9,17 @@
 //   * an O accumulator of a 128-row tile takes 256 of the SM's 512 TMEM
 //     columns, so the two query tiles of an item run one after the other
 //     (each with its own key range), not side by side;
-//   * shared memory holds Q (64 KB) and 2-stage K and V rings of 64-key tiles
-//     (32 KB each): 192 KB;
-//   * S is double-buffered in TMEM (2 x 64 columns): the MMA issuer computes
-//     S(j+1) while the softmax warps work on S(j), so the tensor pipe is not
-//     idle during the softmax of one tile.
+//   * the key tiles stay 128 wide, so that S = Q K^T runs as N = 128 MMAs at
+//     the tensor pipe's full rate (an N = 64 MMA takes as long as an N = 128
+//     one); S is double-buffered in the other 256 TMEM columns, and the MMA
+//     issuer computes S(j+1) while the softmax warps work on S(j);
+//   * a K or V tile of 128 keys x 256 dims is 64 KB, so shared memory holds
+//     Q (64 KB) and a ring of four 32 KB units, each 128 keys x 128 dims (one
+//     half of a K or V tile): 192 KB.  The units are filled in the order the
+//     MMAs consume them -- K(0), K(1), V(0), K(2), V(1), ... -- and a unit is
+//     released as soon as the MMAs of its half are done.
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps
-// 2..9 softmax (two per TMEM lane quarter, each owning 32 of a row's 64 key
+// 2..9 softmax (two per TMEM lane quarter, each owning 64 of a row's 128 key
 // columns and 128 of its 256 output columns).
 #include <type_traits>
 
@@ -32,37 +36,35 @@ using pf::kNegInf;
 
 constexpr int kD = 256;
 constexpr int kTileM = 128;
-constexpr int kTileN = 64;                 // keys per tile
+constexpr int kTileN = 128;                // keys per tile
+constexpr int kSlots = 4;                  // ring units
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct WideLayout {
     static constexpr int Q_BYTES = kTileM * kD * 2;       // 64 KB
     static constexpr int Q_CHUNK = kTileM * 128;          // one 64-dim chunk: 16 KB
-    static constexpr int T_BYTES = kTileN * kD * 2;       // 32 KB per K or V tile
-    static constexpr int T_CHUNK = kTileN * 128;          // one 64-dim chunk: 8 KB
+    static constexpr int U_BYTES = kTileN * 128 * 2;      // one unit, 128 dims: 32 KB
+    static constexpr int U_CHUNK = kTileN * 128;          // one 64-dim chunk of it: 16 KB
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + 2 * T_BYTES;
-    static constexpr int OFF_BAR = OFF_V + 2 * T_BYTES;
+    static constexpr int OFF_RING = OFF_Q + Q_BYTES;
+    static constexpr int OFF_BAR = OFF_RING + kSlots * U_BYTES;
     static constexpr int B_Q = 0;
     static constexpr int B_QEMPTY = 1;
-    static constexpr int B_KFULL = 2;
-    static constexpr int B_KEMPTY = B_KFULL + 2;
-    static constexpr int B_VFULL = B_KEMPTY + 2;
-    static constexpr int B_VEMPTY = B_VFULL + 2;
+    static constexpr int B_FULL = 2;
+    static constexpr int B_EMPTY = B_FULL + kSlots;
     // A parity wait is only valid within one phase of the barrier, so the
     // barriers that can have two completions outstanding come in pairs:
-    // ODONE[k & 1] completes PV number k (phase k >> 1), VFIX[s] the zeroed
-    // tail of V stage s.
-    static constexpr int B_VFIX = B_VEMPTY + 2;
-    static constexpr int B_SFULL = B_VFIX + 2;
+    // SFULL / PFULL / ODONE [g & 1] complete step g (phase g >> 1); VFIX[u]
+    // the zeroed tail of the value unit in ring slot u.
+    static constexpr int B_VFIX = B_EMPTY + kSlots;
+    static constexpr int B_SFULL = B_VFIX + kSlots;
     static constexpr int B_PFULL = B_SFULL + 2;
     static constexpr int B_ODONE = B_PFULL + 2;
     static constexpr int B_OFREE = B_ODONE + 2;
     static constexpr int B_DRAIN = B_OFREE + 1;  // the MMAs in flight, after a failed wait
     static constexpr int NBARS = B_DRAIN + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
-    // row-max exchange [2 (tile parity)][128][2] and row-sum exchange
+    // row-max exchange [2 (step parity)][128][2] and row-sum exchange
     // [2 (query tile)][128][2] between the two warps of a row
     static constexpr int OFF_XMAX = OFF_TMEM + 16;
     static constexpr int OFF_XL = OFF_XMAX + 2 * 128 * 2 * 4;
@@ -72,11 +74,12 @@ struct WideLayout {
     static constexpr int SMEM = 1024 + OFF_XOK + 2 * 128 * 2 * 4;
     static constexpr int SOFT_THREADS = 256;
     static constexpr int THREADS = 64 + SOFT_THREADS;
-    static constexpr int TMEM_COLS = 512;  // O: 0..255, S0: 256..319, S1: 320..383
+    static constexpr int TMEM_COLS = 512;  // O: 0..255, S0: 256..383, S1: 384..511
     static constexpr int O_COL = 0;
 };
+static_assert(WideLayout::SMEM <= 227 * 1024, "shared memory budget");
 
-__host__ __device__ constexpr int s_col(int b) { return 256 + b * 64; }
+__host__ __device__ constexpr int s_col(int b) { return 256 + b * 128; }
 
 // The key tiles of query tile x of the item.
 struct TileRange {
@@ -109,7 +112,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = pf::align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + Lay::OFF_Q, sK = sbase + Lay::OFF_K, sV = sbase + Lay::OFF_V;
+    const uint32_t sQ = sbase + Lay::OFF_Q, sR = sbase + Lay::OFF_RING;
     const uint32_t bars = sbase + Lay::OFF_BAR;
     auto bar = [&](int i) { return bars + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
@@ -146,18 +149,73 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Per query tile the units go in the order K(0) | K(1) V(0) | K(2)
+        // V(1) | ... | V(n-1), two units (dims 0..127, 128..255) per tile;
+        // unit u sits in ring slot u % 4.
         const int32_t *bt = p.block_table + (int64_t)geo.r * p.max_blocks_per_seq;
         const int cy = HND ? 0 : geo.g;
         const int oob_row = HND ? (int)(p.num_blocks * p.num_kv_heads) : (int)(p.num_blocks * BS);
         const int npages_kv = (geo.kv_len + BS - 1) / BS;
         bool alive = true;
-        int kv_t = 0, q_loads = 0;
-        int nk = 0, nv = 0;  // key / value tiles whose loads were issued
+        int u = 0, q_loads = 0;
         if (lane == 0) {
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
         }
+        int ids_batch = -1, ids_row = oob_row;
+        // the pool row of the page this lane loads (lane / 2) in key tile kt
+        auto page_row = [&](int kt_lo, int tile) -> int {
+            if constexpr (CONTIG) {
+                return p.cu_k[geo.r] + (kt_lo + tile) * kTileN;  // rows past kv_len are masked
+            } else {
+                const int rel = tile * NPG;
+                if ((rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
+                    ids_batch = rel >> 5;
+                    const int pg = kt_lo * NPG + ids_batch * 32 + lane;
+                    ids_row = oob_row;
+                    if (pg < npages_kv) {
+                        const int blk = bt[pg];
+                        if (blk < 0 || blk >= p.num_blocks)
+                            flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
+                        else
+                            ids_row = HND ? blk * p.num_kv_heads + geo.g : blk * BS;
+                    }
+                }
+                return __shfl_sync(0xffffffffu, ids_row,
+                                   ((rel & 31) + min(lane >> 1, NPG - 1)) & 31);
+            }
+        };
+        // one unit: half h of the K (tm = &tmk) or V tile whose page rows the
+        // lanes hold; a value unit of the partial last tile gets its rows at
+        // or past kv_len zeroed (they may hold any bits, and P = 0 must never
+        // meet a non-finite value)
+        auto load_unit = [&](const CUtensorMap *tm, int row, int h, int tail_first) {
+            const int slot = u & (kSlots - 1);
+            const uint32_t ph = (u >> 2) & 1;
+            alive = warp_wait_bounded(bar(Lay::B_EMPTY + slot), ph ^ 1, p.dev_error, abort);
+            if (!alive) return;
+            const uint32_t dst = sR + slot * Lay::U_BYTES;
+            if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_FULL + slot), Lay::U_BYTES);
+            __syncwarp();
+            if (lane < 2 * NPG) {
+                const int pg = lane >> 1, c = lane & 1;
+                tma_load_3d(dst + c * Lay::U_CHUNK + pg * BS * 128, tm, bar(Lay::B_FULL + slot),
+                            (2 * h + c) * 64, cy, row);
+            }
+            ++u;
+            if (tail_first >= 0) {
+                alive = warp_wait_bounded(bar(Lay::B_FULL + slot), ph, p.dev_error, abort);
+                if (!alive) return;
+                for (int e = tail_first * 16 + lane; e < kTileN * 16; e += 32) {
+                    const int rr = e >> 4, c = e & 15;
+                    pf::st_shared_zero16(dst + (c >> 3) * Lay::U_CHUNK + sw128(rr, c & 7));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Lay::B_VFIX + slot));
+            }
+        };
         for (int x = 0; x < pf::kItemTiles && alive; ++x) {
             const TileRange t = tr[x];
             if (t.n == 0) continue;
@@ -172,104 +230,101 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                                 geo.q_start + geo.t0 + x * TPR);
             }
             ++q_loads;
-            const int pg0 = t.kt_lo * NPG;
-            int ids_batch = -1, ids_row = oob_row;
-            for (int j = 0; j < t.n && alive; ++j, ++kv_t) {
-                const int s = kv_t & 1;
-                const uint32_t ph = (kv_t >> 1) & 1;
-                const int tile = tile_of(t.n, j);
-                const int key0 = (t.kt_lo + tile) * kTileN;
-                const int rel = tile * NPG;
-                if (!CONTIG && (rel >> 5) != ids_batch) {  // 32 block ids per warp-wide load
-                    ids_batch = rel >> 5;
-                    const int pg = pg0 + ids_batch * 32 + lane;
-                    ids_row = oob_row;
-                    if (pg < npages_kv) {
-                        const int blk = bt[pg];
-                        if (blk < 0 || blk >= p.num_blocks)
-                            flag_error(p.dev_error, PKV_DEVERR_BLOCK_ID);
-                        else
-                            ids_row = HND ? blk * p.num_kv_heads + geo.g : blk * BS;
-                    }
+            ids_batch = -1;
+            int row_cur = page_row(t.kt_lo, tile_of(t.n, 0));
+            for (int h = 0; h < 2 && alive; ++h) load_unit(&tmk, row_cur, h, -1);
+            for (int j = 0; j < t.n && alive; ++j) {
+                int row_next = row_cur;
+                if (j + 1 < t.n) {
+                    row_next = page_row(t.kt_lo, tile_of(t.n, j + 1));
+                    for (int h = 0; h < 2 && alive; ++h) load_unit(&tmk, row_next, h, -1);
                 }
-                // lane l loads page l / 4, 64-dim chunk l % 4
-                int row = __shfl_sync(0xffffffffu, ids_row,
-                                      ((rel & 31) + min(lane >> 2, NPG - 1)) & 31);
-                if constexpr (CONTIG) row = p.cu_k[geo.r] + key0;  // rows past kv_len are masked
-                alive = warp_wait_bounded(bar(Lay::B_KEMPTY + s), ph ^ 1, p.dev_error, abort);
-                if (!alive) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_KFULL + s), Lay::T_BYTES);
-                __syncwarp();
-                if (lane < 4 * NPG) {
-                    const int pg = lane >> 2, c = lane & 3;
-                    tma_load_3d(sK + s * Lay::T_BYTES + c * Lay::T_CHUNK + pg * BS * 128, &tmk,
-                                bar(Lay::B_KFULL + s), c * 64, cy, row);
-                }
-                ++nk;
-                alive = warp_wait_bounded(bar(Lay::B_VEMPTY + s), ph ^ 1, p.dev_error, abort);
-                if (!alive) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar(Lay::B_VFULL + s), Lay::T_BYTES);
-                __syncwarp();
-                if (lane < 4 * NPG) {
-                    const int pg = lane >> 2, c = lane & 3;
-                    tma_load_3d(sV + s * Lay::T_BYTES + c * Lay::T_CHUNK + pg * BS * 128, &tmv,
-                                bar(Lay::B_VFULL + s), c * 64, cy, row);
-                }
-                ++nv;
-                if (is_tail(t, j)) {
-                    // value rows at or past kv_len may hold any bits: zero them
-                    // so that P = 0 never meets a non-finite value
-                    alive = warp_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error, abort);
-                    if (!alive) break;
-                    const int first = max(geo.kv_len - key0, 0);
-                    const uint32_t vb = sV + s * Lay::T_BYTES;
-                    for (int e = first * 32 + lane; e < kTileN * 32; e += 32) {
-                        const int rr = e >> 5, c = e & 31;
-                        pf::st_shared_zero16(vb + (c >> 3) * Lay::T_CHUNK + sw128(rr, c & 7));
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(Lay::B_VFIX + s));
-                }
+                const int key0 = (t.kt_lo + tile_of(t.n, j)) * kTileN;
+                const int first = is_tail(t, j) ? max(geo.kv_len - key0, 0) : -1;
+                for (int h = 0; h < 2 && alive; ++h) load_unit(&tmv, row_cur, h, first);
+                row_cur = row_next;
             }
         }
         // let the MMA issuer's last arrivals land before the CTA can exit
-        for (int k = max(0, kv_t - 2); k < kv_t && alive; ++k) {
-            const uint32_t ph = (k >> 1) & 1;
-            alive = warp_wait_bounded(bar(Lay::B_KEMPTY + (k & 1)), ph, p.dev_error, abort) &&
-                    warp_wait_bounded(bar(Lay::B_VEMPTY + (k & 1)), ph, p.dev_error, abort);
-        }
+        for (int k = max(0, u - kSlots); k < u && alive; ++k)
+            alive = warp_wait_bounded(bar(Lay::B_EMPTY + (k & (kSlots - 1))), (k >> 2) & 1,
+                                      p.dev_error, abort);
         if (alive && q_loads > 0)
             warp_wait_bounded(bar(Lay::B_QEMPTY), (q_loads - 1) & 1, p.dev_error, abort);
         if (!alive) {
             // a wait gave up: let this warp's copies still in flight land
             // (bounded) before the CTA's shared memory is released
             if (q_loads > 0) warp_wait_bounded(bar(Lay::B_Q), (q_loads - 1) & 1, p.dev_error);
-            for (int t = max(0, nk - 2); t < nk; ++t)
-                warp_wait_bounded(bar(Lay::B_KFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
-            for (int t = max(0, nv - 2); t < nv; ++t)
-                warp_wait_bounded(bar(Lay::B_VFULL + (t & 1)), (t >> 1) & 1, p.dev_error);
+            for (int k = max(0, u - kSlots); k < u; ++k)
+                warp_wait_bounded(bar(Lay::B_FULL + (k & (kSlots - 1))), (k >> 2) & 1,
+                                  p.dev_error);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
-            constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, kD, 0, 1);
-            auto issue_s = [&](int b, int s) {
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t a =
-                        tc::smem_desc_sw128(sQ + (kk >> 2) * Lay::Q_CHUNK + off, 16, 1024);
-                    const uint64_t bd = tc::smem_desc_sw128(
-                        sK + s * Lay::T_BYTES + (kk >> 2) * Lay::T_CHUNK + off, 16, 1024);
-                    tc::mma_ss(tmem + s_col(b), a, bd, idS, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(bar(Lay::B_SFULL + b));
-            };
+            constexpr uint32_t idO = tc::idesc_bf16_f32(kTileM, 128, 0, 1);
             bool alive = true;
-            int kv_t = 0, q_waits = 0, pv_cnt = 0, ofree_waits = 0;
-            int pu[2] = {0, 0}, vfix_cnt[2] = {0, 0};
+            int u = 0, q_waits = 0, ofree_waits = 0, g = 0;
+            uint32_t vfix_par = 0;  // bit u: parity of the next tail fix in slot u
+            // S(g) = Q K^T into buffer g & 1, from the two K units of its tile
+            auto issue_s = [&]() {
+                const int b = g & 1;
+                for (int h = 0; h < 2 && alive; ++h) {
+                    const int slot = u & (kSlots - 1);
+                    alive = mbar_wait_bounded(bar(Lay::B_FULL + slot), (u >> 2) & 1, p.dev_error,
+                                              abort);
+                    if (!alive) return;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(
+                            sQ + (2 * h + (kk >> 2)) * Lay::Q_CHUNK + off, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(
+                            sR + slot * Lay::U_BYTES + (kk >> 2) * Lay::U_CHUNK + off, 16, 1024);
+                        tc::mma_ss(tmem + s_col(b), a, bd, idS, (h > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(bar(Lay::B_EMPTY + slot));
+                    ++u;
+                }
+                if (alive) tc::commit(bar(Lay::B_SFULL + b));
+            };
+            // O += P(g) V, one 128-column half of O per V unit
+            auto issue_pv = [&](bool first, bool tail) {
+                const int b = g & 1;
+                for (int h = 0; h < 2 && alive; ++h) {
+                    const int slot = u & (kSlots - 1);
+                    if (tail) {
+                        alive = mbar_wait_bounded(bar(Lay::B_VFIX + slot), (vfix_par >> slot) & 1,
+                                                  p.dev_error, abort);
+                        vfix_par ^= 1u << slot;
+                    } else {
+                        alive = mbar_wait_bounded(bar(Lay::B_FULL + slot), (u >> 2) & 1,
+                                                  p.dev_error, abort);
+                    }
+                    if (!alive) return;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk) {
+                        const uint64_t bd = tc::smem_desc_sw128(
+                            sR + slot * Lay::U_BYTES + kk * 2048, Lay::U_CHUNK, 1024);
+                        tc::mma_ts(tmem + Lay::O_COL + h * 128, tmem + s_col(b) + kk * 8, bd,
+                                   idO, (!first || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(bar(Lay::B_EMPTY + slot));
+                    ++u;
+                }
+                if (alive) tc::commit(bar(Lay::B_ODONE + b));
+            };
+            // S(g) overwrites P(g - 2): PV(g - 2) must be done
+            auto free_s = [&]() {
+                if (g < 2) return;
+                const int k = g - 2;
+                alive = mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1, p.dev_error,
+                                          abort);
+                tc::fence_after_sync();
+            };
             for (int x = 0; x < pf::kItemTiles && alive; ++x) {
                 const TileRange t = tr[x];
                 if (t.n == 0) continue;
@@ -277,73 +332,38 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 ++q_waits;
                 if (!alive) break;
                 tc::fence_after_sync();
-                const int base = kv_t;
-                for (int jj = 0; jj < 2 && jj < t.n && alive; ++jj) {
-                    const int tt = base + jj;
-                    alive = mbar_wait_bounded(bar(Lay::B_KFULL + (tt & 1)), (tt >> 1) & 1,
+                const int base = g;
+                free_s();
+                if (alive) issue_s();
+                if (alive && t.n == 1) tc::commit(bar(Lay::B_QEMPTY));
+                for (int j = 0; j < t.n && alive; ++j) {
+                    g = base + j + 1;
+                    if (j + 1 < t.n) {
+                        free_s();
+                        if (alive) issue_s();
+                        if (alive && j + 2 == t.n) tc::commit(bar(Lay::B_QEMPTY));
+                    }
+                    g = base + j;
+                    if (!alive) break;
+                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + (g & 1)), (g >> 1) & 1,
                                               p.dev_error, abort);
                     if (!alive) break;
-                    tc::fence_after_sync();
-                    issue_s(jj & 1, tt & 1);
-                    tc::commit(bar(Lay::B_KEMPTY + (tt & 1)));
-                    if (jj == t.n - 1) tc::commit(bar(Lay::B_QEMPTY));
-                }
-                for (int j = 0; j < t.n && alive; ++j) {
-                    const int tt = base + j, s = tt & 1, b = j & 1;
-                    const uint32_t ph = (tt >> 1) & 1;
-                    alive = mbar_wait_bounded(bar(Lay::B_PFULL + b), pu[b] & 1, p.dev_error,
-                                              abort);
-                    ++pu[b];
-                    if (!alive) break;
-                    if (is_tail(t, j)) {
-                        alive = mbar_wait_bounded(bar(Lay::B_VFIX + s), vfix_cnt[s] & 1,
-                                                  p.dev_error, abort);
-                        ++vfix_cnt[s];
-                    } else {
-                        alive = mbar_wait_bounded(bar(Lay::B_VFULL + s), ph, p.dev_error,
-                                                  abort);
-                    }
-                    if (!alive) break;
-                    if (j == 0 && pv_cnt > 0) {  // the previous tile's epilogue has read O
+                    if (j == 0 && base > 0) {  // the previous tile's epilogue has read O
                         alive = mbar_wait_bounded(bar(Lay::B_OFREE), ofree_waits & 1,
                                                   p.dev_error, abort);
                         ++ofree_waits;
                         if (!alive) break;
                     }
                     tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < kTileN / 16; ++kk) {
-                        const uint64_t bd = tc::smem_desc_sw128(sV + s * Lay::T_BYTES + kk * 2048,
-                                                                Lay::T_CHUNK, 1024);
-                        tc::mma_ts(tmem + Lay::O_COL, tmem + s_col(b) + kk * 8, bd, idO,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::commit(bar(Lay::B_ODONE + (pv_cnt & 1)));
-                    tc::commit(bar(Lay::B_VEMPTY + s));
-                    ++pv_cnt;
-                    if (j + 2 < t.n) {
-                        const int t2 = base + j + 2;
-                        alive = mbar_wait_bounded(bar(Lay::B_KFULL + (t2 & 1)), (t2 >> 1) & 1,
-                                                  p.dev_error, abort);
-                        if (!alive) break;
-                        // P(j) lives where S(j+2) goes: PV(j) must be done
-                        const int k = pv_cnt - 1;
-                        alive = mbar_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
-                                                  p.dev_error, abort);
-                        if (!alive) break;
-                        tc::fence_after_sync();
-                        issue_s(b, t2 & 1);
-                        tc::commit(bar(Lay::B_KEMPTY + (t2 & 1)));
-                        if (j + 2 == t.n - 1) tc::commit(bar(Lay::B_QEMPTY));
-                    }
+                    issue_pv(j == 0, is_tail(t, j));
                 }
-                kv_t += t.n;
+                g = base + t.n;
             }
         }
     } else {
         // ------------------------------------------------------------ softmax
         // Two warps per TMEM lane quarter: half hc owns key columns
-        // [32 hc, 32 hc + 32) of S, packed P columns [16 hc, 16 hc + 16) and
+        // [64 hc, 64 hc + 64) of S, packed P columns [32 hc, 32 hc + 32) and
         // output columns [128 hc, 128 hc + 128).
         const int w = warp - 2;
         const int quarter = warp & 3;
@@ -361,8 +381,7 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
         const float al2 = ALIBI ? p.alibi[head] * kLog2e : 0.f;
         const float sink_l2 = p.sink ? p.sink[head] * kLog2e : kNegInf;
         bool alive = true, o_ok = true;
-        int pv_base = 0, jg = 0;
-        int su[2] = {0, 0};
+        int g = 0;  // steps so far, both query tiles
         for (int x = 0; x < pf::kItemTiles; ++x) {
             const TileRange t = tr[x];
             if (!t.rows) continue;
@@ -371,28 +390,29 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
             const int qpos = geo.kv_len - geo.q_len + tok;
             const int cpos = p.causal ? qpos : (1 << 30);  // causal upper bound on keys
             float m_run = kNegInf, l_run = 0.f;
-            for (int j = 0; j < t.n && alive; ++j, ++jg) {
-                const int b = j & 1;
+            const int base = g;
+            for (int j = 0; j < t.n && alive; ++j, ++g) {
+                const int b = g & 1;
                 // a warp whose wait gave up still meets its partner at the pair
                 // barrier below, and both leave together
-                const bool s_wait = warp_wait_bounded(bar(Lay::B_SFULL + b), su[b] & 1,
+                const bool s_wait = warp_wait_bounded(bar(Lay::B_SFULL + b), (g >> 1) & 1,
                                                       p.dev_error, abort);
                 const bool s_ok = o_ok && s_wait;
-                ++su[b];
                 tc::fence_after_sync();
-                const int key0 = (t.kt_lo + tile_of(t.n, j)) * kTileN + hc * 32;
-                const bool full = (key0 + 31 <= cpos) && (key0 + 32 <= geo.kv_len) &&
+                const int key0 = (t.kt_lo + tile_of(t.n, j)) * kTileN + hc * 64;
+                const bool full = (key0 + 63 <= cpos) && (key0 + 64 <= geo.kv_len) &&
                                   (wl < 0 || key0 >= qpos - wl);
                 const int khi = min(cpos, geo.kv_len - 1) - key0;
                 const int klo = wl < 0 ? -1 : qpos - wl - key0;
-                uint32_t ra[32];
+                uint32_t ra[2][32];
                 // loaded even after a failed wait (the values are then unused)
-                tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 32, ra);
+                tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 64, ra[0]);
+                tc::ld_32x32b_x32(tmem + lane_off + s_col(b) + hc * 64 + 32, ra[1]);
                 tc::wait_ld();
                 if (!full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (!(i <= khi && i >= klo)) ra[i] = __float_as_uint(kNegInf);
+                    for (int i = 0; i < 64; ++i)
+                        if (!(i <= khi && i >= klo)) ra[i >> 5][i & 31] = __float_as_uint(kNegInf);
                 }
                 float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
                 if constexpr (ALIBI) {
@@ -402,28 +422,28 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                     uint64_t bc[2] = {f2_pack(b0, b0 + al2),
                                       f2_pack(b0 + 2.f * al2, b0 + 3.f * al2)};
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 32; ++i) {
+                        uint32_t &r0 = ra[i >> 4][(2 * i) & 31], &r1 = ra[i >> 4][(2 * i + 1) & 31];
                         float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]),
-                                                 __uint_as_float(ra[2 * i + 1])),
-                                         sc2, bc[i & 1]),
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(r0), __uint_as_float(r1)), sc2,
+                                         bc[i & 1]),
                                   x0, x1);
                         bc[i & 1] = f2_add(bc[i & 1], step2);
-                        ra[2 * i] = __float_as_uint(x0);
-                        ra[2 * i + 1] = __float_as_uint(x1);
+                        r0 = __float_as_uint(x0);
+                        r1 = __float_as_uint(x1);
                         mx4[i & 3] = fmax3(mx4[i & 3], x0, x1);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        mx4[i & 3] = fmax3(mx4[i & 3], __uint_as_float(ra[2 * i]),
-                                           __uint_as_float(ra[2 * i + 1]));
+                    for (int i = 0; i < 32; ++i)
+                        mx4[i & 3] = fmax3(mx4[i & 3], __uint_as_float(ra[i >> 4][(2 * i) & 31]),
+                                           __uint_as_float(ra[i >> 4][(2 * i + 1) & 31]));
                 }
                 const float mine = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
-                float *slot = xmax + ((jg & 1) * 128 + row) * 2;
+                float *slot = xmax + ((g & 1) * 128 + row) * 2;
                 slot[hc] = mine;
                 int *okslot = reinterpret_cast<int *>(smem + Lay::OFF_XOK) +
-                              ((jg & 1) * 128 + row) * 2;
+                              ((g & 1) * 128 + row) * 2;
                 okslot[hc] = s_ok;
                 asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
                 // both warps of the pair read both flags: they leave together
@@ -436,9 +456,9 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                     const float alpha = grow ? fast_exp2(m_run - m_tile) : 1.f;
                     l_run *= alpha;
                     if (j > 0) {
-                        // O is written by PV(j-1): wait for it before rescaling (a
+                        // O is written by PV(g-1): wait for it before rescaling (a
                         // wait that gives up is reported at the next pair barrier)
-                        const int k = pv_base + j - 1;
+                        const int k = g - 1;
                         o_ok = warp_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
                                                  p.dev_error, abort);
                     }
@@ -462,18 +482,19 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 const float psc = ALIBI ? 1.f : sl2;
                 const uint64_t scale2 = f2_pack(psc, psc), neg2 = f2_pack(-msub, -msub);
                 uint64_t ps2[2] = {0ull, 0ull};
+                uint32_t pw[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     float t0, t1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[2 * i]),
-                                             __uint_as_float(ra[2 * i + 1])),
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[i >> 4][(2 * i) & 31]),
+                                             __uint_as_float(ra[i >> 4][(2 * i + 1) & 31])),
                                      scale2, neg2),
                               t0, t1);
                     const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
                     ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
-                    ra[i] = pack_bf16(p0, p1);  // packed in place: pair i -> word i
+                    pw[i] = pack_bf16(p0, p1);
                 }
-                tc::st_32x32b_x16(tmem + lane_off + s_col(b) + hc * 16, ra);
+                tc::st_32x32b_x32(tmem + lane_off + s_col(b) + hc * 32, pw);
                 float s0, s1, s2, s3;
                 f2_unpack(ps2[0], s0, s1);
                 f2_unpack(ps2[1], s2, s3);
@@ -487,11 +508,12 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
             bool have_o = t.n > 0 && alive;
             if (have_o) {
                 // the last PV's commit covers every earlier MMA
-                const int k = pv_base + t.n - 1;
+                const int k = base + t.n - 1;
                 have_o = warp_wait_bounded(bar(Lay::B_ODONE + (k & 1)), (k >> 1) & 1,
                                            p.dev_error, abort);
                 tc::fence_after_sync();
             }
+            g = base + t.n;
             float *lslot = xl + (x * 128 + row) * 2;
             lslot[hc] = l_run;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
@@ -540,7 +562,6 @@ prefill_wide_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap t
                 tc::fence_before_sync();
                 mbar_arrive(bar(Lay::B_OFREE));  // O may be overwritten by the next tile
             }
-            pv_base += t.n;
         }
     }
     tc::fence_before_sync();
