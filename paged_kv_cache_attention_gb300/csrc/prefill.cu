@@ -325,6 +325,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
     // one item per CTA (its per-item list of key tiles is built by the whole
     // CTA before the roles split).
     constexpr bool PERSIST = !SPARSE;
+    // items a CTA may take (one: the compiler then sees straight-line code)
+    constexpr int kMaxItems = PERSIST ? (1 << 30) : 1;
 
     pdl_wait();  // the work list: the attention grid launches while it is built
     const int n_items = p.tiles[0];
@@ -480,7 +482,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         int qn = 0;          // Q loads so far
         int nk = 0, nv = 0;  // key / value tile loads issued (for the drain)
         bool alive = true;
-        for (int n = 0; alive; ++n) {
+        for (int n = 0; alive && n < kMaxItems; ++n) {
             int idx;
             if constexpr (PERSIST) {
                 const int s = n % Lay::RING;
@@ -673,7 +675,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
             int qn = 0;       // items with key tiles so far
             int vfn[kStages] = {0, 0};  // tail fixes consumed per stage
             bool alive = true;
-            for (int n = 0; alive; ++n) {
+            for (int n = 0; alive && n < kMaxItems; ++n) {
                 const int idx = item_at(n, false);
                 if (idx < 0) {
                     alive = idx == -1;
@@ -785,7 +787,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq
         const int wl = p.window_left;
         int gstep = 0;  // key-tile steps of this query tile so far, all items
         bool alive = true;
-        for (int n = 0; alive; ++n) {
+        for (int n = 0; alive && n < kMaxItems; ++n) {
         const int idx = item_at(n, true);
         if (idx < 0) break;
         const Work wk = work_of(idx, false);
