@@ -80,7 +80,7 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-configuration decode / prefill lines")
     ap.add_argument("--profile", choices=["decode", "decode_long", "decode_mixed", "prefill",
-                                          "prefill_mixed", "write", "rope"],
+                                          "prefill_d256", "prefill_mixed", "write", "rope"],
                     default=None,
                     help="run a few launches of one call on a mid-size case (for ncu)")
     return ap.parse_args()
@@ -923,7 +923,7 @@ def run_profile(which: str):
     """A few launches of one call on a case larger than L2 but a few GB at
     most: decode = the B64 / L512-4096 decode batch (~0.6 GB of KV),
     decode_mixed = the mixed step's decode call (256 sequences, ~3.2 GB of KV),
-    prefill = the B16 varlen prefill batch, write = the mixed step's cache
+    prefill = the B16 varlen prefill batch (prefill_d256: with head_dim 256), write = the mixed step's cache
     write, rope = the rotary step fused with the write for 8448 tokens."""
     import torch
     import paged_kv_cache_attention_gb300 as pkv
@@ -943,11 +943,14 @@ def run_profile(which: str):
         go = lambda: pkv.paged_decode(q, kc, vc, bt, sl, c.max_seqlen, sink=sink,
                                       window_left=c.window_left, sm_scale=c.sm_scale,
                                       partition_size=c.partition_size, workspace=ws)
-    elif which in ("prefill", "prefill_mixed"):
+    elif which in ("prefill", "prefill_d256", "prefill_mixed"):
         # prefill_mixed: the prefill launch of the mixed step (4 chunks of 2048
-        # over 4096-token prefixes), on a pool holding only those pages
-        c = W.config4_prefill() if which == "prefill" else W.make_mixed(
-            [], 2048, 4096, 4, 32, 8, 128, 16, torch.bfloat16, seed=W.seed_for(5) + 100).prefill
+        # over 4096-token prefixes), on a pool holding only those pages;
+        # prefill_d256: the B16 batch with head_dim 256 (16 query / 8 kv heads)
+        c = (W.config4_prefill() if which == "prefill" else
+             W.config4_prefill(16, 8, 256) if which == "prefill_d256" else W.make_mixed(
+                 [], 2048, 4096, 4, 32, 8, 128, 16, torch.bfloat16,
+                 seed=W.seed_for(5) + 100).prefill)
         q, kc, vc = c.q.to(dev), c.k_cache.to(dev), c.v_cache.to(dev)
         bt, cq, ck = c.block_table.to(dev), c.cu_seq_lens_q.to(dev), c.cu_seq_lens_k.to(dev)
         sink = None if c.sink is None else c.sink.to(dev)
