@@ -119,7 +119,8 @@ DecodeLayout decode_layout(int batch, int Hq, int D, int num_parts) {
 }
 
 // Work list of the prefill kernel: a 256-byte header (item count), one int4
-// per (query block, kv head) and the per-request block offsets.  A query
+// per (query block, kv head), the per-request block offsets and the
+// per-request first item.  A query
 // block holds 2 tiles of 128 / G tokens.
 struct PrefillLayout {
     int64_t max_items;
@@ -130,7 +131,7 @@ PrefillLayout prefill_layout(int batch, int G, int num_kv_heads, int total_q) {
     PrefillLayout L;
     const int64_t tokens = G > 0 && G <= 128 ? 2 * (128 / G) : 1;
     L.max_items = ((int64_t)total_q / tokens + batch) * num_kv_heads;
-    L.total = round_up(256 + (size_t)L.max_items * 16 + ((size_t)batch + 1) * 4, 256);
+    L.total = round_up(256 + (size_t)L.max_items * 16 + ((size_t)2 * batch + 1) * 4, 256);
     return L;
 }
 

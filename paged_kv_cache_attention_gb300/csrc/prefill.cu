@@ -133,8 +133,11 @@ __device__ __forceinline__ Geo make_geo(const PrefillParams &p, int4 item, int b
 }
 
 // ---------------------------------------------------------------------------
-// work list: items {request, first query token, kv head, cost} sorted by cost
-// (key tiles), heaviest first.  Single CTA.
+// work list: items {request, first query token, kv head, cost}: requests by
+// the cost (key tiles) of their heaviest query block, heaviest first, and
+// inside a request its query blocks by cost, heaviest first (the persistent
+// CTAs draw the items in this order, so the cheap ones come last).  Single
+// CTA.
 // ---------------------------------------------------------------------------
 constexpr int kSchedThreads = 1024;
 constexpr int kBuckets = 1024;
@@ -156,7 +159,8 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
     __shared__ int total_pairs_s;
     int *count = p.tiles;                                      // [0]: number of items
     int4 *items = reinterpret_cast<int4 *>(p.tiles + 64);      // 256-byte header
-    int *offs = p.tiles + 64 + 4 * p.max_tiles;                // [batch + 1] pair offsets
+    int *offs = p.tiles + 64 + 4 * p.max_tiles;                // [batch + 1] pair offsets,
+                                                               // then [batch] first items
     const int tid = threadIdx.x;
     const int tokens = kNQ * p.rows_per_head;
     pdl_trigger();  // the attention kernel (launched as a dependent) may start launching
@@ -227,11 +231,22 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
         cost = min(item_cost(p, ql, kl, t0), kBuckets - 1);
     };
 
-    // 2. histogram of costs (per pair; each pair yields num_kv_heads items)
-    for (int i = tid; i < total_pairs; i += kSchedThreads) {
-        int r, t0, c;
-        pair_of(i, r, t0, c);
-        atomicAdd(&hist[c], p.num_kv_heads);
+    // The heaviest query block of request r (causal: the last one; with a
+    // window all are about equal, so the first is checked too).
+    auto request_cost = [&](int r) {
+        const int nq = offs[r + 1] - offs[r];
+        int qs, ql;
+        pf::q_rows(p, r, qs, ql, false);
+        const int kl = pf::clip_len64((long long)p.cu_k[r + 1] - p.cu_k[r], p.max_seqlen_k,
+                                      nullptr, false);
+        const int c = max(item_cost(p, ql, kl, 0), item_cost(p, ql, kl, (nq - 1) * tokens));
+        return min(c, kBuckets - 1);
+    };
+    // 2. histogram of request costs (each request yields its blocks x
+    //    num_kv_heads items)
+    for (int r = tid; r < p.batch; r += kSchedThreads) {
+        const int nq = offs[r + 1] - offs[r];
+        if (nq > 0) atomicAdd(&hist[request_cost(r)], nq * p.num_kv_heads);
     }
     __syncthreads();
     // 3. exclusive scan from the heaviest bucket down: thread t takes bucket
@@ -261,13 +276,28 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
         hist[bk] = v - h + (wid ? wsum[wid - 1] : 0);
     }
     __syncthreads();
-    // 4. scatter
+    // 4. requests in order of their heaviest block, heaviest first; inside a
+    //    request its query blocks from the heaviest down, each with its kv
+    //    heads side by side.  The CTAs running at one time then work on one
+    //    or two requests, whose K/V stays in L2 while all their query blocks
+    //    read it (on the 4 x 2048-token prefill of the mixed step the DRAM
+    //    traffic of the launch fell from 755 MB to about a quarter of that,
+    //    against 235 MB of algorithmic bytes, when items were ordered by
+    //    their own cost across all requests).
+    int *first = offs + p.batch + 1;  // [batch] first item of each request
+    for (int r = tid; r < p.batch; r += kSchedThreads) {
+        const int nq = offs[r + 1] - offs[r];
+        first[r] = nq > 0 ? atomicAdd(&hist[request_cost(r)], nq * p.num_kv_heads) : 0;
+    }
+    __syncthreads();
     for (int i = tid; i < total_pairs; i += kSchedThreads) {
         int r, t0, c;
         pair_of(i, r, t0, c);
-        const int pos = atomicAdd(&hist[c], p.num_kv_heads);
-        for (int g = 0; g < p.num_kv_heads; ++g)
-            if (pos + g < p.max_tiles) items[pos + g] = make_int4(r, t0, g, c);
+        const int nq = offs[r + 1] - offs[r], blk = i - offs[r];
+        for (int g = 0; g < p.num_kv_heads; ++g) {
+            const int pos = first[r] + (nq - 1 - blk) * p.num_kv_heads + g;
+            if (pos < p.max_tiles) items[pos] = make_int4(r, t0, g, c);
+        }
     }
     if (tid == 0) *count = n_items;
 }
