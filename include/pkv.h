@@ -166,6 +166,20 @@ PKV_API pkv_status pkv_get_device_error(const int32_t *dev_error, int32_t *bits,
                                         void *stream);
 
 /*
+ * selftest_bounded_wait: a check of the library's bounded pipeline waits on
+ * the current device.  Launches one warp on `stream` that waits on a shared-
+ * memory barrier nothing arrives on; the wait gives up after its limit
+ * (about 4e8 SM cycles, a fraction of a second), ORs PKV_DEVERR_TIMEOUT into
+ * dev_error (device int32, caller-owned) and the kernel returns.  Afterwards
+ * pkv_get_device_error reports PKV_ERR_TIMEOUT, and the context and stream
+ * stay usable: this is the path every kernel of the library takes when one
+ * of its pipeline waits runs out, here without a broken pipeline.
+ * Returns PKV_ERR_INVALID_ARG for a NULL dev_error, PKV_ERR_CUDA if the
+ * launch fails, else PKV_OK (asynchronous).
+ */
+PKV_API pkv_status pkv_selftest_bounded_wait(int32_t *dev_error, void *stream);
+
+/*
  * reshape_and_cache: for every t in [0, num_tokens) with slot_mapping[t] >= 0,
  * copy row t of key and of value ([num_tokens, Hkv, D], contiguous, dtype of
  * the cache) into flat slot slot_mapping[t] of k_cache and v_cache.  The copy

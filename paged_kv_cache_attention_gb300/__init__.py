@@ -43,6 +43,7 @@ __all__ = [
     "varlen_prefill", "varlen_prefill_contiguous", "paged_decode_noalloc",
     "paged_decode_workspace_size", "varlen_prefill_workspace_size",
     "rope_cos_sin_table", "rope_reshape_and_cache", "get_device_error",
+    "selftest_bounded_wait",
     "minference_sizes", "minference_prefill",
     "DEVERR_BLOCK_ID", "DEVERR_SLOT", "DEVERR_SEQLEN", "DEVERR_TIMEOUT", "DEVERR_POSITION",
     "EXPORTED_SYMBOLS",
@@ -62,7 +63,7 @@ EXPORTED_SYMBOLS = (
     "pkv_varlen_prefill_workspace_size", "pkv_varlen_prefill",
     "pkv_varlen_prefill_contiguous", "pkv_rope_cos_sin_table", "pkv_rope_reshape_and_cache",
     "pkv_minference_sizes", "pkv_minference_workspace_size", "pkv_minference_prefill",
-    "pkv_paged_decode_noalloc", "pkv_get_device_error",
+    "pkv_paged_decode_noalloc", "pkv_get_device_error", "pkv_selftest_bounded_wait",
 )
 
 
@@ -143,6 +144,8 @@ def load_library(path: Optional[str] = None):
         lib.pkv_paged_decode_noalloc.restype = i32
         lib.pkv_get_device_error.argtypes = [P, P, i32, P]
         lib.pkv_get_device_error.restype = i32
+        lib.pkv_selftest_bounded_wait.argtypes = [P, P]
+        lib.pkv_selftest_bounded_wait.restype = i32
         _lib = lib
         return lib
 
@@ -281,6 +284,15 @@ def get_device_error(dev_error, clear: bool = False, stream=None, raise_on_error
     if st != 0 and (raise_on_error or st not in (5, 6)):
         _check("pkv_get_device_error", st)
     return int(bits.value)
+
+
+def selftest_bounded_wait(dev_error, stream=None):
+    """Run one bounded pipeline wait that nothing completes on ``stream``: it
+    gives up by itself and ORs DEVERR_TIMEOUT into ``dev_error`` (an int32
+    device tensor of one element); see get_device_error."""
+    _cuda_contig("dev_error", dev_error, _torch().int32, 1)
+    _check("pkv_selftest_bounded_wait",
+           load_library().pkv_selftest_bounded_wait(_ptr(dev_error), _stream_handle(stream)))
 
 
 def rope_cos_sin_table(max_position: int, rotary_dim: int, base: float = 10000.0,

@@ -197,7 +197,7 @@ const char *pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 500; }
+int pkv_version(void) { return 501; }
 
 pkv_status pkv_get_device_error(const int32_t *dev_error, int32_t *bits, int clear,
                                 void *stream) {

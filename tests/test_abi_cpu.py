@@ -223,6 +223,8 @@ def test_rope_table_validation():
 @nogpu
 def test_get_device_error_validation():
     assert pkv.load_library().pkv_get_device_error(None, None, 0, None) == 1
+    # the bounded-wait self-test needs an error word to report into
+    assert pkv.load_library().pkv_selftest_bounded_wait(None, None) == 1
 
 
 # ---------------------------------------------------------------------------

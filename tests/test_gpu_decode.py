@@ -178,6 +178,32 @@ def test_device_error_status_through_the_abi():
     assert e.value.status_name == "PKV_ERR_OUT_OF_RANGE"
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """A pipeline wait that nothing completes gives up by itself (no trap, no
+    hang): the library's self-test runs one on a barrier nothing arrives on,
+    the timeout bit lands in the error word, pkv_get_device_error reports
+    PKV_ERR_TIMEOUT, and the next calls on the same context still compute
+    the attention."""
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    pkv.selftest_bounded_wait(err)
+    lib = pkv.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    bits = ctypes.c_int32(0)
+    st = lib.pkv_get_device_error(err.data_ptr(), ctypes.addressof(bits), 1, stream)
+    assert lib.pkv_status_string(st) == b"PKV_ERR_TIMEOUT"
+    assert bits.value == pkv.DEVERR_TIMEOUT
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.selftest_bounded_wait(err)
+        pkv.get_device_error(err, clear=True, raise_on_error=True)
+    assert e.value.status_name == "PKV_ERR_TIMEOUT"
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    case = W.make_decode([37, 300], 8, 2, 64, 16, torch.bfloat16, seed=14)
+    got = gpu_decode(case, err=err)
+    assert max_abs(got, oracle_decode(case)) <= TOL[torch.bfloat16]
+    assert int(err.item()) == 0
+
+
 def test_seqlen_above_declared_max_is_flagged():
     case = W.make_decode([100, 40], 8, 2, 64, 16, torch.bfloat16, seed=13)
     err = torch.zeros(1, dtype=torch.int32, device=dev())
