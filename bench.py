@@ -63,9 +63,9 @@ NCU_TRAFFIC = {
     # partials read back by the merge (cold caches under ncu; live they are
     # L2 hits); mean of three calls
     "decode": {"bytes": 3193203285, "sha": "f65c0ecb16b8e406"},
-    # prefill launch of the mixed step: 676.8 MB read + 78.3 MB written
+    # prefill launch of the mixed step: 172.3 MB read + 48.4 MB written
     # (mean of three launches)
-    "prefill": {"bytes": 755098880, "sha": "a7daa7c8319861b3"},
+    "prefill": {"bytes": 220608427, "sha": "3b1493568a2ab8b6"},
 }
 
 

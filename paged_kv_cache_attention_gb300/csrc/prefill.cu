@@ -280,10 +280,10 @@ __global__ void __launch_bounds__(kSchedThreads) prefill_schedule_kernel(const P
     //    request its query blocks from the heaviest down, each with its kv
     //    heads side by side.  The CTAs running at one time then work on one
     //    or two requests, whose K/V stays in L2 while all their query blocks
-    //    read it (on the 4 x 2048-token prefill of the mixed step the DRAM
-    //    traffic of the launch fell from 755 MB to about a quarter of that,
-    //    against 235 MB of algorithmic bytes, when items were ordered by
-    //    their own cost across all requests).
+    //    read it.  On the 4 x 2048-token prefill of the mixed step (235 MB
+    //    of algorithmic bytes) the launch moves 221 MB through DRAM this way,
+    //    against 755 MB with the items ordered by their own cost across all
+    //    requests (measured on GB300).
     int *first = offs + p.batch + 1;  // [batch] first item of each request
     for (int r = tid; r < p.batch; r += kSchedThreads) {
         const int nq = offs[r + 1] - offs[r];
