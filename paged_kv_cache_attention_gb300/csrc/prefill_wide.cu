@@ -124,19 +124,18 @@ __device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t mask) {
         : "memory");
 }
 
-// The key tiles of query tile x of the item.
+// The key tiles of query tile x of the item (none when the tile holds no
+// query row of the request).
 struct TileRange {
     int kt_lo, n;
-    bool rows;  // the tile holds at least one query row of the request
 };
 
 __device__ __forceinline__ TileRange tile_range(const PrefillParams &p, const pf::Geo &G,
                                                 int x) {
     TileRange t;
     const int tb = G.t0 + x * p.rows_per_head;
-    t.rows = tb < G.q_len;
     pf::key_tiles(p, G, tb, tb + p.rows_per_head, kTileN, t.kt_lo, t.n);
-    if (!t.rows) t.n = 0;
+    if (tb >= G.q_len) t.n = 0;
     return t;
 }
 
@@ -148,7 +147,6 @@ __device__ __forceinline__ TileRange pair_range(const TileRange &a, const TileRa
     TileRange u;
     u.kt_lo = min(a.kt_lo, b.kt_lo);
     u.n = max(a.kt_lo + a.n, b.kt_lo + b.n) - u.kt_lo;
-    u.rows = true;
     return u;
 }
 
