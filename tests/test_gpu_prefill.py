@@ -13,7 +13,8 @@ import torch
 import paged_kv_cache_attention_gb300 as pkv
 from paged_kv_cache_attention_gb300 import workloads as W
 from tests._gpu import (LSE_TOL, TOL, contiguous_kv, dev, gpu_decode, gpu_prefill,
-                        gpu_prefill_contiguous, lse_err, max_abs, oracle_decode, oracle_prefill)
+                        gpu_prefill_contiguous, lse_err, max_abs, oracle_decode, oracle_prefill,
+                        to_dev)
 
 pytestmark = pytest.mark.gpu
 BF16 = torch.bfloat16
@@ -348,6 +349,60 @@ def test_bad_block_id_is_flagged():
     assert np.isfinite(got).all()
     ref = oracle_prefill(case, rows=list(range(40)))
     assert max_abs(got[:40], ref) <= TOL[BF16]
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_work_list_is_each_item_once_in_request_order(G):
+    """The work list the prefill builds on the device holds every (request,
+    query block, kv head) exactly once; the requests come heaviest first by
+    the key-tile count of their heaviest query block, and each request's
+    items are contiguous: its query blocks heaviest first (for causal
+    attention the later ones), each with its kv heads side by side.  The
+    output is still the attention (checked against the oracle)."""
+    Hkv = 4
+    q_lens, pre = [1, 300, 129, 700, 64, 40], [0, 5000, 100, 0, 3000, 200]
+    case = W.make_varlen(q_lens, pre, G * Hkv, Hkv, 128, 16, BF16, seed=31)
+    ws = torch.zeros(pkv.varlen_prefill_workspace_size(case.batch, G * Hkv, Hkv, case.total_q,
+                                                       case.max_seqlen_q),
+                     dtype=torch.uint8, device=dev())
+    kc, vc = to_dev(case.k_cache), to_dev(case.v_cache)
+    out = pkv.varlen_prefill(to_dev(case.q), kc, vc, to_dev(case.block_table),
+                             to_dev(case.cu_seq_lens_q), to_dev(case.cu_seq_lens_k),
+                             case.max_seqlen_q, case.max_seqlen_k, sink=to_dev(case.sink),
+                             sm_scale=case.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle_prefill(case)
+    assert max_abs(out.float().cpu().numpy(), ref) <= TOL[BF16]
+
+    w = ws.view(torch.int32).cpu().numpy()
+    n = int(w[0])
+    items = w[64:64 + 4 * n].reshape(n, 4)  # (request, first query token, kv head, cost)
+    tokens = 2 * (128 // G)
+    kv_lens = case.kv_lens.tolist()
+
+    def cost(r, t0):  # key tiles of a causal query block, from the definition
+        t_end = min(t0 + tokens, q_lens[r])
+        hi = min(kv_lens[r], kv_lens[r] - q_lens[r] + t_end)
+        return (hi - 1) // 128 + 1 if hi > 0 else 0
+
+    want = {(r, t0, g) for r in range(case.batch) for t0 in range(0, q_lens[r], tokens)
+            for g in range(Hkv)}
+    got = [tuple(int(v) for v in it[:3]) for it in items]
+    assert len(got) == len(want) and set(got) == want
+    assert all(int(it[3]) == cost(int(it[0]), int(it[1])) for it in items)
+    # each request's items contiguous, blocks from the heaviest down, heads
+    # side by side
+    order = [int(it[0]) for it in items]
+    firsts = [order.index(r) for r in range(case.batch)]
+    for r in range(case.batch):
+        nb = (q_lens[r] + tokens - 1) // tokens
+        mine = [tuple(int(v) for v in it[:3]) for it in items[firsts[r]:firsts[r] + nb * Hkv]]
+        assert mine == [(r, t0, g) for t0 in reversed(range(0, q_lens[r], tokens))
+                        for g in range(Hkv)]
+    # requests by their heaviest block, heaviest first
+    heaviest = [max(cost(r, t0) for t0 in range(0, q_lens[r], tokens)) for r in range(case.batch)]
+    seq = [heaviest[r] for r in sorted(range(case.batch), key=lambda r: firsts[r])]
+    assert seq == sorted(seq, reverse=True)
 
 
 @pytest.mark.parametrize("D", [128, 256])
